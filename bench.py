@@ -1,0 +1,513 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked KDA forward on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one chunked KDA forward over one batch of synthetic input: by
+default the pages' representative fixed training shape B=1, H=32, T=8192,
+K=V=128, bf16 q/k/v, fp32 g/beta, random fp32 initial state, final state
+returned.  Inputs are seeded and drawn on the CPU (``kda_inputs``), then held
+in HBM.  The timed region is bracketed by a barrier and a device synchronise;
+each step's kernel time is taken with CUDA events on the launching stream,
+and a 256 MiB buffer (twice the 129 MB L2) is written between steps, outside
+the events, so no step starts with its inputs in L2.
+
+One JSON line is printed by rank 0.  ``value`` is whole-job tokens/s (B*T
+tokens per forward, summed over ranks; every rank runs its own replica of the
+workload, so scaling is weak).  ``e2e`` is the same metric through the public
+call with host buffers: pinned host->device copies of the inputs and the
+device->host read of o and the final state inside the timed region.
+``roofline`` relates the dominant kernel's algorithmic bytes per launch to
+the measured HBM copy bandwidth; ``cpu_baseline`` is the fp64 oracle timed on
+this machine's host cores on a bounded sample.
+
+``--impl reference`` times the oracle itself (the slow reference program) on
+the host cores, one bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_inputs as ki  # noqa: E402
+
+METRIC = "KDA forward tokens/s (ms/fwd) at H=32 T=8192 K=V=128 bf16; % of roofline"
+HEADLINE = "fixed_bf16_h32_t8192"
+PACKED = "packed_bf16_h32_t8192_25seg"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# The pages' fastest forward on this shape (TPU v7x, tokamax #19, run 2:
+# 1.870 ms for B*T = 8192 tokens); context for vs_baseline, not the target.
+PAGES_TPU_FIXED_MS = 1.870
+PAGES_TPU_PACKED_MS = 2.891
+CHUNK = 64
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (bytes and FLOPs a perfect kernel must move / do)
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(w) -> int:
+    e = 2 if w.dtype == "bf16" else 4
+    per_th = 2 * w.K * e + w.V * e + w.K * 4 + 4 + w.V * e   # q k v g beta o
+    n = w.token_heads * per_th
+    if w.segments is not None:
+        n += w.B * w.T * 4
+    state = w.B * w.H * w.K * w.V * 4
+    if w.init_state_std is not None:
+        n += state
+    if w.output_final_state:
+        n += state
+    return n
+
+
+def flops_per_chunk_head(K, V, C=CHUNK) -> float:
+    """Masked-triangle FLOPs of one full chunk for one head: the intra-chunk
+    products (KK^T, QK^T over K; T*beta*[V|K] over V and K), the inter-chunk
+    products (w S, Q S, K^T U) and the triangular solve."""
+    tri = C * (C + 1) / 2
+    return 2 * tri * (3 * K + 2 * V) + 6 * C * K * V + C ** 3 / 3
+
+
+def algorithmic_flops(w) -> float:
+    return w.token_heads * flops_per_chunk_head(w.K, w.V) / CHUNK
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_digest(impl_name: str) -> str:
+    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu"}[impl_name]
+    path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(impl_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(impl_name, {}).get(workload)
+    if not e or e.get("source_sha") != kernel_source_digest(impl_name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; weak scaling, no collective on
+# the data path -- only the barrier and the max-over-ranks of the timings)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = f"cuda:{self.local_rank}" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.windows = []
+        try:
+            p = torch.cuda.get_device_properties(device_index)
+            self.bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception:  # older torch without the PCI fields
+            self.bus = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        return self.summarise(rows)
+
+    def summarise(self, rows):
+        import datetime as _dt
+        mine = [r for r in rows if self.bus and r[1].lower() == self.bus]
+        if not mine:
+            mine = rows
+        def ts(r):
+            try:
+                return _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in mine if ts(r) is not None and any(a <= ts(r) <= b for a, b in self.windows)]
+        window = "timed"
+        if not inside:
+            inside, window = mine, "timed+warmup (timed region shorter than the sampling period)"
+        if not inside:
+            return {"samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        mx = [num(r[3]) for r in inside if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window,
+                "power_w_max": max((num(r[4]) or 0.0) for r in inside)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def device_inputs(x, dev):
+    return {n: (x[n].to(dev) if isinstance(x.get(n), torch.Tensor) else None)
+            for n in ("q", "k", "v", "g", "beta", "initial_state", "segment_ids")}
+
+
+def time_steps(fn, steps, warmup, stream, flush, dist, clocks=None):
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t1 = time.time()
+    if clocks is not None:
+        clocks.mark(t0, t1)
+    return [a.elapsed_time(b) for a, b in evs], t1 - t0
+
+
+def run_ours(args, dist):
+    import gated_delta_rule_21_gb300 as kda
+    from gated_delta_rule_21_gb300 import build as kbuild
+    kbuild.build()
+    dev = torch.device(f"cuda:{dist.local_rank}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dist.local_rank)
+    hbm_peak, tc_peak, peak_src = measured_peaks()
+
+    def measure(wname, with_e2e, clocks_=None):
+        w = ki.WORKLOADS[wname]
+        x = ki.make_inputs(w, seed=args.seed + dist.rank)
+        d = device_inputs(x, dev)
+        has_seg = d["segment_ids"] is not None
+        o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
+        fs = torch.empty(w.B, w.H, w.K, w.V, dtype=torch.float32, device=dev)
+        ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg, dev)
+
+        def step():
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                          output_final_state=True, out=o, final_state_out=fs,
+                          workspace=ws, impl=args.kda_impl, v_tile=args.v_tile, stream=stream)
+
+        times, wall = time_steps(step, args.steps, args.warmup, stream, flush, dist, clocks_)
+        status = kda.read_device_status(ws)
+        if status:
+            raise RuntimeError(f"device status bits {status:#x} after the timed steps")
+        ms = statistics.mean(times)
+        ms_max = dist.max(ms)
+        tokens = w.B * w.T
+        res = dict(workload=w, ms=ms, ms_max=ms_max, ms_median=statistics.median(times),
+                   ms_min=min(times), wall=wall, tokens=tokens, has_seg=has_seg)
+        if with_e2e:
+            res["e2e"] = measure_e2e(kda, x, d, o, fs, ws, step_args=(w, has_seg))
+        return res
+
+    def measure_e2e(kda, x, d, o, fs, ws, step_args):
+        w, has_seg = step_args
+        names = [n for n in ("q", "k", "v", "g", "beta", "initial_state", "segment_ids")
+                 if d[n] is not None]
+        host = {n: x[n].contiguous().pin_memory() for n in names}
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = o_h.numel() * o_h.element_size() + fs_h.numel() * fs_h.element_size()
+
+        def e2e_step():
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                          output_final_state=True, out=o, final_state_out=fs,
+                          workspace=ws, impl=args.kda_impl, v_tile=args.v_tile, stream=stream)
+            o_h.copy_(o, non_blocking=True)
+            fs_h.copy_(fs, non_blocking=True)
+
+        times, _ = time_steps(e2e_step, args.steps, args.warmup, stream, flush, dist)
+        ms = dist.max(statistics.mean(times))
+        return {"value": dist.world * w.B * w.T / (ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    def roofline(res):
+        w = res["workload"]
+        nbytes = algorithmic_bytes(w)
+        flops = algorithmic_flops(w)
+        t = res["ms"] * 1e-3
+        gbs = nbytes / t / 1e9
+        impl_name = "tc" if kernel_impl(w) == "tc" else "simt"
+        traffic = profiled_traffic(impl_name, w.name)
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(gbs / hbm_peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"
+                if peak_src == "measured" else "fallback 6.8 TB/s",
+                "kernel": f"fwd_{impl_name}_kernel", "algorithmic_bytes": nbytes,
+                "algorithmic_flops": flops,
+                "tensor_frac": round(flops / t / 1e12 / tc_peak, 4),
+                "roofline_ms": round(max(nbytes / (hbm_peak * 1e9), flops / (tc_peak * 1e12)) * 1e3, 4)}
+
+    def kernel_impl(w):
+        if args.kda_impl == "simt":
+            return "simt"
+        tc = w.dtype == "bf16" and w.K == 128 and w.V == 128 and tc_available()
+        return "tc" if tc else "simt"
+
+    clocks.start()
+    head = measure(args.workload, with_e2e=True, clocks_=clocks)
+    packed = measure(PACKED, with_e2e=False) if args.workload == HEADLINE else None
+    clk = clocks.stop()
+
+    w = head["workload"]
+    value = dist.world * head["tokens"] / (head["ms_max"] * 1e-3)
+    launches_per_step = 1 + (1 if head["has_seg"] else 0)
+    impl_used = kernel_impl(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_max"],
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / (w.B * w.T / (PAGES_TPU_FIXED_MS * 1e-3))
+                        if args.workload == HEADLINE else None),
+        "vs_baseline_ref": "pages' TPU v7x tokamax #19 fixed forward, 1.870 ms (other hardware; context)",
+        "dtype": "bf16" if impl_used == "tc" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
+                   "qkv_dtype": w.dtype, "chunk": CHUNK, "initial_state": w.init_state_std is not None,
+                   "output_final_state": True, "impl": impl_used,
+                   "l2": "flushed: 256 MiB write between timed steps",
+                   "ms_median": head["ms_median"], "ms_min": head["ms_min"]},
+        "roofline": roofline(head),
+        "e2e": head["e2e"],
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if packed is not None:
+        pw = packed["workload"]
+        line["packed"] = {"workload": pw.name, "ms_per_step": packed["ms_max"],
+                          "value": dist.world * packed["tokens"] / (packed["ms_max"] * 1e-3),
+                          "unit": "tokens/s", "roofline": roofline(packed),
+                          "vs_pages_tpu": (packed["tokens"] / (packed["ms_max"] * 1e-3))
+                          / (pw.B * pw.T / (PAGES_TPU_PACKED_MS * 1e-3)),
+                          "gpu_launches": 2 * args.steps}
+        line["gpu_launches"] += 2 * args.steps
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.seed, budget_s=args.cpu_seconds)
+    return line
+
+
+def tc_available() -> bool:
+    import gated_delta_rule_21_gb300 as kda
+    return kda.impl_available("tc", 1, 64, 1, 128, 128, torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(w, seed, heads):
+    """The first ``heads`` heads of the workload, as the oracle's fp64 input."""
+    import oracle
+    x = ki.make_inputs(w, seed=seed)
+    sl = slice(0, heads)
+    arrs = [oracle._f64(x[n][:, :, sl]) for n in ("q", "k", "v", "g", "beta")]
+    s0 = x["initial_state"]
+    s0 = None if s0 is None else oracle._f64(s0[:, sl])
+    seg = x["segment_ids"]
+    return arrs, s0, seg, x["scale"]
+
+
+def cpu_baseline(w, seed, budget_s=10.0):
+    import oracle
+    cores = oracle.default_threads()
+    heads = min(w.H, cores)
+    arrs, s0, seg, scale = oracle_sample(w, seed, heads)
+    runs, t_total = 0, 0.0
+    while t_total < budget_s and runs < 100:
+        t = time.perf_counter()
+        oracle.kda_forward(*arrs, scale, initial_state=s0, segment_ids=seg, threads=cores)
+        t_total += time.perf_counter() - t
+        runs += 1
+    per_run = t_total / runs
+    tokens_equiv = w.B * w.T * heads / w.H
+    return {"value": tokens_equiv / per_run, "unit": "tokens/s", "cores": min(cores, w.B * heads),
+            "kind": "oracle",
+            "sample": f"{heads} of {w.H} heads x {w.B * w.T} tokens (fp64 token recurrence), "
+                      f"{runs} runs, {t_total:.1f} s; tokens/s scaled by heads/H"}
+
+
+def run_reference(args, dist):
+    """The oracle as the reference program, on the host cores."""
+    import oracle
+    w = ki.WORKLOADS[args.workload]
+    cores = oracle.default_threads()
+    heads = min(w.H, cores)
+    arrs, s0, seg, scale = oracle_sample(w, args.seed, heads)
+    fn = lambda: oracle.kda_forward(*arrs, scale, initial_state=s0, segment_ids=seg,  # noqa: E731
+                                    threads=cores)
+    for _ in range(args.warmup):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t)
+    ms = statistics.mean(times) * 1e3
+    tokens_equiv = w.B * w.T * heads / w.H
+    value = tokens_equiv / (ms * 1e-3)
+    sample = (f"{heads} of {w.H} heads x {w.B * w.T} tokens per step (fp64 token "
+              f"recurrence); tokens/s scaled by heads/H")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, w.B * heads),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(ki.WORKLOADS))
+    ap.add_argument("--kda-impl", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--v-tile", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        dist = Dist.__new__(Dist)
+        dist.rank, dist.world, dist.local_rank, dist.pg = 0, int(os.environ.get("WORLD_SIZE", "1")), 0, None
+        print(json.dumps(run_reference(args, dist)))
+        return 0
+
+    dist = Dist()
+    try:
+        line = run_ours(args, dist)
+        if dist.rank == 0:
+            print(json.dumps(line))
+    finally:
+        dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,242 @@
+"""gated_delta_rule_21_gb300 -- Python binding of libkda, the GB300 (sm_103a)
+chunked Kimi Delta Attention forward.
+
+The binding only marshals arguments: it checks dtypes/shapes/devices of torch
+tensors, allocates outputs and the workspace with torch (device memory and
+streams are all torch is used for), and calls the C ABI declared in
+``include/kda.h`` through ctypes.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or eager fallback, and importing this
+package fails loudly when ``libkda.so`` has not been built.
+
+Entry points (same names as the C ABI, minus the ``kda_`` prefix):
+
+* :func:`chunk_fwd` -- the chunked KDA forward (``kda_chunk_fwd[_ex]``).
+* :func:`short_conv_silu` -- the causal conv + SiLU (+ L2) prologue.
+* :func:`workspace_size`, :func:`read_device_status`,
+  :func:`clear_device_status`, :func:`status_string`, :func:`version`.
+* :func:`lib` -- the raw ctypes library with typed signatures.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK = 0
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
+                3: "KDA_ERR_ALIGNMENT", 4: "KDA_ERR_WORKSPACE", 5: "KDA_ERR_CUDA",
+                6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_DEVICE"}
+IMPLS = {"auto": 0, "simt": 1, "tc": 2}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+CHUNK = 64
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status)})")
+
+
+class kda_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("K", ctypes.c_int), ("V", ctypes.c_int),
+                ("qkv_dtype", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """Load libkda.so (raising if it is missing) and return the typed CDLL."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"libkda.so is not built ({LIB_PATH}); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                "`python -m gated_delta_rule_21_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, u64, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        sp = ctypes.POINTER(kda_shape)
+        L.kda_chunk_fwd_workspace_size.argtypes = [sp, i]
+        L.kda_chunk_fwd_workspace_size.restype = u64
+        L.kda_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp,
+                                    vp, vp, u64, vp]
+        L.kda_chunk_fwd.restype = i
+        L.kda_chunk_fwd_ex.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp,
+                                       vp, vp, vp, u64, i, i, vp]
+        L.kda_chunk_fwd_ex.restype = i
+        L.kda_short_conv_silu.argtypes = [sp, vp, vp, vp, vp, vp, i, vp, vp,
+                                          vp, vp]
+        L.kda_short_conv_silu.restype = i
+        L.kda_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.kda_read_device_status.restype = i
+        L.kda_clear_device_status.argtypes = [vp, vp]
+        L.kda_clear_device_status.restype = i
+        L.kda_status_string.argtypes = [i]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_impl_available.argtypes = [i, sp, i]
+        L.kda_impl_available.restype = i
+        L.kda_version.argtypes = []
+        L.kda_version.restype = i
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().kda_version()
+
+
+def impl_available(impl, B, T, H, K, V, dtype=torch.bfloat16, v_tile=0) -> bool:
+    """Whether implementation ``impl`` ("auto"/"simt"/"tc") runs this shape."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return bool(lib().kda_impl_available(IMPLS[impl], ctypes.byref(s), int(v_tile)))
+
+
+def make_shape(B, T, H, K, V, dtype) -> kda_shape:
+    if dtype not in DTYPES:
+        raise TypeError(f"q/k/v dtype must be float32 or bfloat16, got {dtype}")
+    return kda_shape(int(B), int(T), int(H), int(K), int(V), DTYPES[dtype])
+
+
+def workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+
+
+def alloc_workspace(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
+                    device=None) -> torch.Tensor:
+    """Zero-filled workspace of the required size (uint8 device tensor)."""
+    n = workspace_size(B, T, H, K, V, dtype, has_segment_ids)
+    if n == 0:
+        raise KdaError(1, "workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None,
+              segment_ids=None, output_final_state=False, out=None,
+              final_state_out=None, workspace=None, impl="auto", v_tile=0,
+              stream=None):
+    """Chunked KDA forward on the GPU.
+
+    q, k: [B,T,H,K]; v: [B,T,H,V] (bf16 or fp32, same dtype); g: [B,T,H,K]
+    fp32 log-decay in [-5, 0]; beta: [B,T,H] fp32; initial_state: [B,H,K,V]
+    fp32 or None; segment_ids: [B,T] int32 (1-based, 0 = padding) or None.
+    ``scale`` None means K**-0.5.  Returns ``(o, final_state or None)``.
+    """
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("chunk_fwd needs CUDA tensors")
+    dt = q.dtype
+    _check(q, "q", (B, T, H, K), dt, dev)
+    _check(k, "k", (B, T, H, K), dt, dev)
+    _check(v, "v", (B, T, H, V), dt, dev)
+    _check(g, "g", (B, T, H, K), torch.float32, dev)
+    _check(beta, "beta", (B, T, H), torch.float32, dev)
+    _check(initial_state, "initial_state", (B, H, K, V), torch.float32, dev)
+    _check(segment_ids, "segment_ids", (B, T), torch.int32, dev)
+    if scale is None:
+        scale = K ** -0.5
+    o = out if out is not None else torch.empty(B, T, H, V, dtype=dt, device=dev)
+    _check(o, "out", (B, T, H, V), dt, dev)
+    fs = None
+    if output_final_state:
+        fs = final_state_out if final_state_out is not None else torch.empty(
+            B, H, K, V, dtype=torch.float32, device=dev)
+        _check(fs, "final_state_out", (B, H, K, V), torch.float32, dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, T, H, K, V, dt, segment_ids is not None, dev)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_fwd_ex(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        float(scale), int(chunk_size), _ptr(initial_state), _ptr(segment_ids),
+        _ptr(o), _ptr(fs), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        IMPLS[impl], int(v_tile), _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd")
+    return o, fs
+
+
+def short_conv_silu(x_q, x_k, x_v, w, segment_ids=None, l2norm_qk=True,
+                    stream=None):
+    """Segment-aware causal depthwise conv (width 4) + SiLU on q, k, v, then
+    optional L2 norm of q and k.  x_q, x_k: [B,T,H,K]; x_v: [B,T,H,V];
+    w: fp32 [3, H*K, 4] (q, k, v weight blocks; needs K == V) or a flat
+    tensor of 4*(2*H*K + H*V) floats.  Returns (q, k, v)."""
+    B, T, H, K = x_q.shape
+    V = x_v.shape[-1]
+    dev, dt = x_q.device, x_q.dtype
+    _check(x_q, "x_q", (B, T, H, K), dt, dev)
+    _check(x_k, "x_k", (B, T, H, K), dt, dev)
+    _check(x_v, "x_v", (B, T, H, V), dt, dev)
+    _check(segment_ids, "segment_ids", (B, T), torch.int32, dev)
+    if w.dtype != torch.float32 or w.device != dev or not w.is_contiguous() \
+            or w.numel() != 4 * (2 * H * K + H * V):
+        raise ValueError("w must be contiguous fp32 with 4*(2*H*K + H*V) elements")
+    q = torch.empty_like(x_q)
+    k = torch.empty_like(x_k)
+    v = torch.empty_like(x_v)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_short_conv_silu(
+        ctypes.byref(s), _ptr(x_q), _ptr(x_k), _ptr(x_v), _ptr(w),
+        _ptr(segment_ids), int(bool(l2norm_qk)), _ptr(q), _ptr(k), _ptr(v),
+        _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_short_conv_silu")
+    return q, k, v
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status bits (0 = clean)."""
+    bits = ctypes.c_uint32(0)
+    st = lib().kda_read_device_status(_ptr(workspace), _stream_ptr(stream, workspace.device),
+                                      ctypes.byref(bits))
+    if st not in (KDA_OK, 6, 7):
+        raise KdaError(st, "kda_read_device_status")
+    return int(bits.value)
+
+
+def clear_device_status(workspace, stream=None) -> None:
+    st = lib().kda_clear_device_status(_ptr(workspace), _stream_ptr(stream, workspace.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_clear_device_status")

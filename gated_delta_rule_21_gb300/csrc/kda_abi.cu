@@ -1,0 +1,219 @@
+// kda_abi.cu -- the extern "C" boundary of libkda (declared in include/kda.h).
+//
+// Every entry point validates its arguments on the host before enqueuing
+// anything, maps CUDA errors to kda_status, and never throws.  The forward
+// call builds the run list (packed segment ids) and then launches the chunk
+// kernel: the tcgen05/TMA tensor-core kernel for bf16 K = V = 128, the fp32
+// SIMT kernel otherwise.
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+      cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+kda_status check_shape(const kda_shape *s) {
+  if (!s) return KDA_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 1 || s->H < 1) return KDA_ERR_INVALID_ARG;
+  if (s->qkv_dtype != KDA_DTYPE_F32 && s->qkv_dtype != KDA_DTYPE_BF16)
+    return KDA_ERR_INVALID_ARG;
+  if (!supported_dim(s->K) || !supported_dim(s->V)) return KDA_ERR_UNSUPPORTED;
+  const long long d = s->K > s->V ? s->K : s->V;
+  if ((long long)s->B * s->T * s->H * d >= (1ll << 31)) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+kda_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return KDA_OK;
+  if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+  return KDA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char *kda_status_string(kda_status st) {
+  switch (st) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape, dtype or option";
+    case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_CUDA: return "CUDA runtime error";
+    case KDA_ERR_TIMEOUT: return "device: bounded wait timed out";
+    case KDA_ERR_DEVICE: return "device: error reported by a kernel";
+  }
+  return "unknown status";
+}
+
+int kda_version(void) { return KDA_VERSION; }
+
+size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids) {
+  if (check_shape(s) != KDA_OK) return 0;
+  return ws_bytes(s->B, s->T, has_segment_ids != 0);
+}
+
+kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            float scale, int chunk_size,
+                            const float *initial_state,
+                            const int32_t *segment_ids, void *o,
+                            float *final_state, void *workspace,
+                            size_t workspace_bytes, kda_impl impl, int v_tile,
+                            kda_stream_t stream) {
+  kda_status st = check_shape(s);
+  if (st != KDA_OK) return st;
+  if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+  if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (impl != KDA_IMPL_AUTO && impl != KDA_IMPL_SIMT && impl != KDA_IMPL_TC)
+    return KDA_ERR_INVALID_ARG;
+  if (v_tile < 0) return KDA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return KDA_ERR_INVALID_ARG;  // NaN scale
+  const void *ptrs[] = {q, k, v, g, beta, o, initial_state, final_state,
+                        segment_ids};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  const bool has_seg = segment_ids != nullptr;
+  if (!workspace || workspace_bytes < ws_bytes(s->B, s->T, has_seg))
+    return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+
+  const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
+  const bool tc_ok = fwd_tc_supported(s->K, s->V, bf16, v_tile);
+  bool use_tc;
+  if (impl == KDA_IMPL_TC) {
+    if (!tc_ok) return KDA_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else if (impl == KDA_IMPL_SIMT) {
+    use_tc = false;
+  } else {
+    use_tc = tc_ok;
+  }
+  if (!use_tc) {
+    if (v_tile == 0) v_tile = 32;
+    if (v_tile != 32 || s->V % v_tile) return KDA_ERR_UNSUPPORTED;
+  }
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;
+  p.v_tile = v_tile;
+  p.n_vtiles = v_tile > 0 ? s->V / v_tile : 0;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.scale = scale;
+  p.initial_state = initial_state;
+  p.o = o;
+  p.final_state = final_state;
+  char *ws = static_cast<char *>(workspace);
+  p.status = &reinterpret_cast<WsHeader *>(ws)->status;
+  if (has_seg) {
+    p.runs.row_offsets = reinterpret_cast<const int32_t *>(ws + sizeof(WsHeader));
+    p.runs.runs = reinterpret_cast<const int2 *>(ws + sizeof(WsHeader) +
+                                                 ws_row_offsets_bytes(s->B));
+    p.runs.total_runs = &reinterpret_cast<WsHeader *>(ws)->total_runs;
+  }
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (has_seg) {
+    e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, o,
+                            bf16 ? 1 : 0, initial_state, final_state,
+                            workspace, cs);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  e = use_tc ? launch_fwd_tc(p, cs) : launch_fwd_simt(p, bf16, cs);
+  return from_cuda(e);
+}
+
+int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile) {
+  if (check_shape(s) != KDA_OK || v_tile < 0) return 0;
+  const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
+  const bool simt_ok = (v_tile == 0 || v_tile == 32) && s->V % 32 == 0;
+  switch (impl) {
+    case KDA_IMPL_AUTO: return fwd_tc_supported(s->K, s->V, bf16, v_tile) || simt_ok;
+    case KDA_IMPL_SIMT: return simt_ok;
+    case KDA_IMPL_TC: return fwd_tc_supported(s->K, s->V, bf16, v_tile);
+  }
+  return 0;
+}
+
+kda_status kda_chunk_fwd(const kda_shape *s, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta,
+                         float scale, int chunk_size,
+                         const float *initial_state,
+                         const int32_t *segment_ids, void *o,
+                         float *final_state, void *workspace,
+                         size_t workspace_bytes, kda_stream_t stream) {
+  return kda_chunk_fwd_ex(s, q, k, v, g, beta, scale, chunk_size,
+                          initial_state, segment_ids, o, final_state,
+                          workspace, workspace_bytes, KDA_IMPL_AUTO, 0, stream);
+}
+
+kda_status kda_short_conv_silu(const kda_shape *s, const void *x_q,
+                               const void *x_k, const void *x_v,
+                               const float *w, const int32_t *segment_ids,
+                               int l2norm_qk, void *q, void *k, void *v,
+                               kda_stream_t stream) {
+  kda_status st = check_shape(s);
+  if (st != KDA_OK) return st;
+  if (!x_q || !x_k || !x_v || !w || !q || !k || !v) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {x_q, x_k, x_v, w, q, k, v, segment_ids};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  if (x_q == q || x_k == k || x_v == v) return KDA_ERR_INVALID_ARG;
+  if ((long long)s->B * ((s->T + 31) / 32) > 65535) return KDA_ERR_UNSUPPORTED;
+  ConvParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;
+  p.x[0] = x_q; p.x[1] = x_k; p.x[2] = x_v;
+  p.y[0] = q; p.y[1] = k; p.y[2] = v;
+  p.w = w;
+  p.segment_ids = segment_ids;
+  p.l2norm_qk = l2norm_qk != 0;
+  return from_cuda(launch_short_conv(p, s->qkv_dtype == KDA_DTYPE_BF16,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_read_device_status(const void *workspace, kda_stream_t stream,
+                                  uint32_t *device_bits) {
+  if (!workspace || !device_bits) return KDA_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return KDA_ERR_CUDA;
+  *device_bits = bits;
+  if (bits & KDA_DEVICE_TIMEOUT) return KDA_ERR_TIMEOUT;
+  if (bits) return KDA_ERR_DEVICE;
+  return KDA_OK;
+}
+
+kda_status kda_clear_device_status(void *workspace, kda_stream_t stream) {
+  if (!workspace) return KDA_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(uint32_t),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

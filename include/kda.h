@@ -1,0 +1,201 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) implementation of the chunked
+ * Kimi Delta Attention (KDA) forward pass.
+ *
+ * The operation (page "feat(kda): integrate KDA attention with tokamax backend
+ * and CP support", section "Delta Rule formulation"), per batch row b and head
+ * h, token by token, with a K x V state S indexed [key][value]:
+ *
+ *     S'       = S * exp(g_t)        g_t in R^K: per-key-channel log-decay
+ *     residual = v_t - k_t^T S'
+ *     S        = S' + beta_t * k_t (outer) residual
+ *     o_t      = scale * q_t^T S
+ *
+ * computed in chunks of 64 tokens (same page, section "Public API":
+ * chunk_kda(..., chunk_size=64, initial_state, output_final_state,
+ * segment_ids, ...)).  Packed variable-length sequences are given by 1-based
+ * segment ids [B, T] with 0 = padding (same section, decoder_segment_ids);
+ * the state restarts at every segment boundary.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major
+ *     buffers owned by the caller.  libkda allocates no device memory and
+ *     keeps no global state between calls (the status word lives in the
+ *     caller's workspace), so calls are reentrant; calls on different
+ *     streams must use different workspaces.
+ *   - Work is enqueued on `stream` and the call returns without
+ *     synchronising.  Argument errors are detected on the host before
+ *     anything is enqueued and are returned synchronously; nothing is
+ *     thrown across the ABI.
+ *   - Device-side conditions (a bounded wait that ran out, a debug-mode
+ *     bounds check) set bits in the status word at the start of the
+ *     workspace; read them with kda_read_device_status() after the work has
+ *     finished.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_VERSION 100 /* 1.0.0 */
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,  /* NULL required pointer, bad size, bad flag   */
+  KDA_ERR_UNSUPPORTED = 2,  /* shape / dtype / chunk size not implemented   */
+  KDA_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned             */
+  KDA_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required      */
+  KDA_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed         */
+  KDA_ERR_TIMEOUT = 6,      /* device status: a bounded wait ran out        */
+  KDA_ERR_DEVICE = 7        /* device status: another device-side error     */
+} kda_status;
+
+typedef enum kda_dtype {
+  KDA_DTYPE_F32 = 0,
+  KDA_DTYPE_BF16 = 1
+} kda_dtype;
+
+/* Problem shape.  q, k: [B,T,H,K]; v, o: [B,T,H,V], all of qkv_dtype.
+ * g: [B,T,H,K] float32; beta: [B,T,H] float32; states [B,H,K,V] float32.
+ * Supported: K, V in {32, 64, 128}; B, T, H >= 1; B*T*H*max(K,V) < 2^31. */
+typedef struct kda_shape {
+  int B, T, H, K, V;
+  kda_dtype qkv_dtype;
+} kda_shape;
+
+/* Implementation choice for kda_chunk_fwd_ex. */
+typedef enum kda_impl {
+  KDA_IMPL_AUTO = 0, /* tensor-core kernel where it applies, else SIMT      */
+  KDA_IMPL_SIMT = 1, /* fp32 CUDA-core kernel (every supported shape)       */
+  KDA_IMPL_TC = 2    /* tcgen05 / TMA kernel: bf16, K = V = 128             */
+} kda_impl;
+
+/* Device status bits OR-ed into the workspace status word. */
+#define KDA_DEVICE_TIMEOUT 0x1u    /* a bounded mbarrier / flag wait ran out */
+#define KDA_DEVICE_BAD_INPUT 0x2u  /* a debug-build input check failed       */
+
+/*
+ * Bytes of workspace kda_chunk_fwd needs for this shape.  The workspace
+ * holds the device status word and, when segment ids are given, the run
+ * list (one 8-byte record per run, at most B*T runs) and per-row counts.
+ * The workspace must be zero-filled once before its first use (for
+ * instance allocated with cudaMemset 0); libkda leaves it reusable.
+ * Returns 0 when `s` is NULL or invalid.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids);
+
+/*
+ * Chunked KDA forward (the operation above).
+ *   q, k, v       device, [B,T,H,K|V] of s->qkv_dtype, 16-byte aligned.
+ *   g             device float32 [B,T,H,K]: log-decay, already activated
+ *                 (use_gate_in_kernel=False on the pages).  Contract:
+ *                 g in [-5, 0] (the pages' safe-gate lower bound range);
+ *                 values below -5 may lose accuracy in the intra-chunk
+ *                 factors, values above 0 are growth and are not supported.
+ *   beta          device float32 [B,T,H].
+ *   scale         output scale (the pages leave its default open; callers
+ *                 usually pass K^-0.5).
+ *   chunk_size    must be 64.
+ *   initial_state device float32 [B,H,K,V] or NULL (zeros).  It seeds only
+ *                 the first run of each row; later runs start from zero.
+ *   segment_ids   device int32 [B,T], 1-based ids, 0 = padding, or NULL
+ *                 (every token has id 1).  A run is a maximal span of equal
+ *                 non-zero ids; padding tokens get o = 0, do not touch the
+ *                 state and end the current run.
+ *   o             device [B,T,H,V] of s->qkv_dtype (written for every token).
+ *   final_state   device float32 [B,H,K,V] or NULL (not requested): the state
+ *                 after each row's last non-padding token (initial_state or
+ *                 zeros for an all-padding row).
+ *   workspace     device, >= kda_chunk_fwd_workspace_size(s, segment_ids
+ *                 != NULL) bytes, 256-byte aligned, zero-filled before first
+ *                 use.
+ * Returns KDA_OK or an error code; on error nothing has been enqueued.
+ */
+KDA_API kda_status kda_chunk_fwd(const kda_shape *s, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta,
+                         float scale, int chunk_size,
+                         const float *initial_state,
+                         const int32_t *segment_ids, void *o,
+                         float *final_state, void *workspace,
+                         size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Same as kda_chunk_fwd with an explicit implementation and value-tile
+ * width (v_tile = columns of V one CTA owns; 0 = automatic; otherwise a
+ * divisor of V supported by the chosen kernel).  KDA_ERR_UNSUPPORTED when
+ * the choice does not apply to the shape.
+ */
+KDA_API kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            float scale, int chunk_size,
+                            const float *initial_state,
+                            const int32_t *segment_ids, void *o,
+                            float *final_state, void *workspace,
+                            size_t workspace_bytes, kda_impl impl, int v_tile,
+                            kda_stream_t stream);
+
+/*
+ * 1 when `impl` can run shape `s` (KDA_IMPL_AUTO: always, for a valid
+ * shape), else 0.  Pure host query.
+ */
+KDA_API int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile);
+
+/*
+ * Short-convolution prologue (page "feat(kda): ...", section "Layer
+ * architecture", step 1: causal depthwise 1-D conv of width 4 with SiLU on
+ * each of Q, K, V; optional step 5 / use_qk_l2norm_in_kernel: L2 norm of q
+ * and k per token and head).  Per channel c of each input:
+ *     y_t[c] = SiLU( sum_{i=0}^{3} w[c][3-i] * x_{t-i}[c] )
+ * with taps before t = 0 or before the start of t's run equal to zero, no
+ * bias, and y = 0 on padding tokens.  With l2norm_qk != 0, q and k are then
+ * scaled per (token, head) by 1 / sqrt(sum y^2 + 1e-6).  fp32 arithmetic.
+ *   x_q, x_k      device [B,T,H,K] of s->qkv_dtype; x_v [B,T,H,V].
+ *   w             device float32, three weight blocks back to back:
+ *                 w_q [H*K][4], w_k [H*K][4], w_v [H*V][4].
+ *   segment_ids   device int32 [B,T] or NULL.
+ *   q, k, v       device outputs, same shapes and dtype as the inputs; they
+ *                 must not alias the inputs.
+ */
+KDA_API kda_status kda_short_conv_silu(const kda_shape *s, const void *x_q,
+                               const void *x_k, const void *x_v,
+                               const float *w, const int32_t *segment_ids,
+                               int l2norm_qk, void *q, void *k, void *v,
+                               kda_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads the device status word at the start of
+ * `workspace` into *device_bits (KDA_DEVICE_* bits, 0 when clean).  Returns
+ * KDA_ERR_TIMEOUT when the timeout bit is set, KDA_ERR_DEVICE for any other
+ * bit, KDA_OK when clean, KDA_ERR_CUDA when the copy fails.
+ */
+KDA_API kda_status kda_read_device_status(const void *workspace, kda_stream_t stream,
+                                  uint32_t *device_bits);
+
+/* Enqueues a reset of the device status word to zero on `stream`. */
+KDA_API kda_status kda_clear_device_status(void *workspace, kda_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+KDA_API const char *kda_status_string(kda_status status);
+
+/* KDA_VERSION of the built library. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,124 @@
+"""The C-ABI library loads, exports every entry point include/kda.h declares,
+and rejects bad arguments on the host before touching the GPU.
+
+These run without a GPU: every call here fails validation before any CUDA
+call is made (the library links the CUDA runtime statically and reaches the
+driver only when it launches).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_delta_rule_21_gb300 as kda
+from gated_delta_rule_21_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kda.lib()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API[^;(]*?\b(kda_\w+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_symbols()
+    for must in ("kda_chunk_fwd", "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size",
+                 "kda_short_conv_silu", "kda_read_device_status",
+                 "kda_clear_device_status", "kda_status_string", "kda_version",
+                 "kda_impl_available"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), f"libkda.so does not export {name}"
+
+
+def test_header_compiles_as_c(tmp_path):
+    c = tmp_path / "t.c"
+    c.write_text('#include "kda.h"\nint main(void){return kda_version()==0;}\n')
+    import subprocess
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", str(c), "-I",
+                    os.path.join(ROOT, "include"), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_version_and_status_strings(L):
+    assert kda.version() == 100
+    for st in range(8):
+        assert kda.status_string(st)
+    assert kda.status_string(99) == "unknown status"
+
+
+def test_workspace_size_formula(L):
+    assert kda.workspace_size(1, 8192, 32, 128, 128) == 256
+    # header + row offsets (B+1 ints rounded to 256 B) + 8 B per possible run
+    assert kda.workspace_size(2, 1000, 4, 64, 64, has_segment_ids=True) == 256 + 256 + 8 * 2000
+    s = kda.kda_shape(1, 16, 1, 48, 128, 1)   # unsupported K
+    assert L.kda_chunk_fwd_workspace_size(ctypes.byref(s), 0) == 0
+
+
+FAKE = 0x10000  # a 256-byte aligned address; never dereferenced
+
+
+def call_fwd(L, shape=(1, 128, 2, 128, 128, 1), q=FAKE, k=FAKE, v=FAKE, g=FAKE,
+             beta=FAKE, chunk=64, s0=None, seg=None, o=FAKE, fs=None, ws=FAKE,
+             ws_bytes=1 << 20, impl=0, v_tile=0, scale=0.1):
+    s = kda.kda_shape(*shape)
+    vp = ctypes.c_void_p
+    return L.kda_chunk_fwd_ex(ctypes.byref(s), vp(q), vp(k), vp(v), vp(g), vp(beta),
+                              scale, chunk, vp(s0), vp(seg), vp(o), vp(fs), vp(ws),
+                              ws_bytes, impl, v_tile, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(beta=None), 1),
+    (dict(shape=(0, 128, 2, 128, 128, 1)), 1),
+    (dict(shape=(1, 128, 2, 128, 128, 7)), 1),
+    (dict(shape=(1, 128, 2, 96, 128, 1)), 2),
+    (dict(shape=(1, 128, 2, 128, 16, 1)), 2),
+    (dict(chunk=32), 2),
+    (dict(q=FAKE + 2), 3), (dict(g=FAKE + 4), 3), (dict(s0=FAKE + 8), 3),
+    (dict(ws=None), 4), (dict(ws_bytes=16), 4),
+    (dict(seg=FAKE, ws_bytes=300), 4),
+    (dict(ws=FAKE + 16), 3),
+    (dict(impl=9), 1), (dict(v_tile=-1), 1), (dict(scale=float("nan")), 1),
+    (dict(impl=1, v_tile=48), 2),
+    (dict(impl=2, shape=(1, 128, 2, 64, 64, 1)), 2),
+    (dict(impl=2, shape=(1, 128, 2, 128, 128, 0)), 2),
+])
+def test_forward_rejects_bad_arguments_without_launching(L, kw, expect):
+    assert call_fwd(L, **kw) == expect
+
+
+def test_conv_rejects_bad_arguments(L):
+    s = kda.kda_shape(1, 64, 2, 128, 128, 1)
+    vp = ctypes.c_void_p
+    f = lambda *a: L.kda_short_conv_silu(ctypes.byref(s), *[vp(x) for x in a[:5]], 1,
+                                         *[vp(x) for x in a[5:]], None)
+    assert f(FAKE, FAKE, FAKE, None, None, FAKE + 256, FAKE + 512, FAKE + 768) == 1
+    assert f(FAKE + 2, FAKE, FAKE, FAKE, None, FAKE + 256, FAKE + 512, FAKE + 768) == 3
+    assert f(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE + 512, FAKE + 768) == 1  # aliasing
+
+
+def test_impl_available_query(L):
+    assert kda.impl_available("simt", 1, 64, 1, 128, 128)
+    assert kda.impl_available("auto", 1, 64, 1, 64, 32, torch.float32)
+    assert not kda.impl_available("simt", 1, 64, 1, 128, 128, v_tile=48)
+    assert not kda.impl_available("tc", 1, 64, 1, 64, 64)
+    assert not kda.impl_available("tc", 1, 64, 1, 128, 128, torch.float32)
+
+
+def test_status_calls_reject_null(L):
+    bits = ctypes.c_uint32(0)
+    assert L.kda_read_device_status(None, None, ctypes.byref(bits)) == 1
+    assert L.kda_clear_device_status(None, None) == 1
