@@ -362,8 +362,9 @@ def run_ours(args, dist):
         return "tc" if tc else "simt"
 
     clocks.start()
-    head = measure(args.workload, with_e2e=True, clocks_=clocks)
-    packed = measure(PACKED, with_e2e=False) if args.workload == HEADLINE else None
+    head = measure(args.workload, with_e2e=not args.no_e2e, clocks_=clocks)
+    packed = (measure(PACKED, with_e2e=False)
+              if args.workload == HEADLINE and not args.no_packed else None)
     clk = clocks.stop()
 
     w = head["workload"]
@@ -385,7 +386,7 @@ def run_ours(args, dist):
                    "l2": "flushed: 256 MiB write between timed steps",
                    "ms_median": head["ms_median"], "ms_min": head["ms_min"]},
         "roofline": roofline(head),
-        "e2e": head["e2e"],
+        "e2e": head.get("e2e"),
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }
@@ -486,6 +487,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--no-packed", action="store_true", help="skip the packed N=25 leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
