@@ -156,6 +156,12 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def whole_job_value(world: int, tokens_per_rank: int, ms_max: float) -> float:
+    """tokens/s of the whole job: each rank processes its own replica, and the
+    job takes as long as its slowest rank."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
@@ -368,7 +374,7 @@ def run_ours(args, dist):
     clk = clocks.stop()
 
     w = head["workload"]
-    value = dist.world * head["tokens"] / (head["ms_max"] * 1e-3)
+    value = whole_job_value(dist.world, head["tokens"], head["ms_max"])
     launches_per_step = 1 + (1 if head["has_seg"] else 0)
     impl_used = kernel_impl(w)
     line = {
@@ -393,7 +399,7 @@ def run_ours(args, dist):
     if packed is not None:
         pw = packed["workload"]
         line["packed"] = {"workload": pw.name, "ms_per_step": packed["ms_max"],
-                          "value": dist.world * packed["tokens"] / (packed["ms_max"] * 1e-3),
+                          "value": whole_job_value(dist.world, packed["tokens"], packed["ms_max"]),
                           "unit": "tokens/s", "roofline": roofline(packed),
                           "vs_pages_tpu": (packed["tokens"] / (packed["ms_max"] * 1e-3))
                           / (pw.B * pw.T / (PAGES_TPU_PACKED_MS * 1e-3)),
