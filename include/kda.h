@@ -149,6 +149,35 @@ KDA_API kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const voi
                             kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd without a workspace argument, for callers that cannot
+ * allocate device memory (no counterpart on the pages: it exists only for
+ * such callers).  A plugin inside a host application may be handed nothing
+ * but the tensors it works on; other code runs under a memory budget held
+ * by another allocator, or on a path where allocating is not allowed.  The
+ * arguments and results are those of kda_chunk_fwd.  The scratch it needs
+ * lives in a fixed device array of KDA_NOALLOC_SCRATCH_BYTES bytes that the
+ * library defines; every GPU that loads the library keeps that memory until
+ * the process exits.  The call itself allocates nothing.
+ *   - Shapes whose scratch need, kda_chunk_fwd_workspace_size(s,
+ *     segment_ids != NULL), exceeds KDA_NOALLOC_SCRATCH_BYTES are rejected
+ *     with KDA_ERR_WORKSPACE (with segment ids about B*T > 130000 tokens).
+ *   - All calls share the array: calls whose work overlaps on the GPU race
+ *     and give wrong results.  Order them on one stream.
+ *   - The first call on each device looks up the array's address with that
+ *     device current and keeps it; make that first call before any stream
+ *     capture begins.
+ *   - Each call clears the array's header on `stream` before its kernels,
+ *     so the previous call's counters never carry over.  Device status
+ *     bits are not reported by this entry point.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (1u << 20)
+KDA_API kda_status kda_chunk_fwd_noalloc(
+    const kda_shape *s, const void *q, const void *k, const void *v,
+    const float *g, const float *beta, float scale, int chunk_size,
+    const float *initial_state, const int32_t *segment_ids, void *o,
+    float *final_state, kda_stream_t stream);
+
+/*
  * 1 when `impl` can run shape `s` (KDA_IMPL_AUTO: always, for a valid
  * shape), else 0.  Pure host query.
  */
