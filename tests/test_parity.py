@@ -12,7 +12,7 @@ from kda_testlib import (assert_parity, check_workload, errors, run_gpu, run_ora
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["auto", "simt"]
+IMPLS = ["auto", "simt"]   # auto = tensor-core kernel for bf16 K = V = 128
 NAMED = ["tiny_fp32_h2_t128_d32", "fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg",
          "fixed_bf16_h32_t8192", "packed_bf16_h32_t8192_25seg"]
 
@@ -28,10 +28,7 @@ def _built():
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("name", NAMED)
 def test_named_workload(name, impl):
-    w = ki.WORKLOADS[name]
-    if impl == "simt" and w.T >= 8192:
-        pytest.skip("the full-size SIMT run is covered by impl=auto until the TC path lands")
-    check_workload(w, impl=impl)
+    check_workload(ki.WORKLOADS[name], impl=impl)
 
 
 EDGE = {
