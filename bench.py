@@ -45,6 +45,10 @@ import torch  # noqa: E402
 import kda_inputs as ki  # noqa: E402
 
 METRIC = "KDA forward tokens/s (ms/fwd) at H=32 T=8192 K=V=128 bf16; % of roofline"
+# The kernels one forward launches, per implementation (the roofline covers
+# the whole forward: for the split path that is its two kernels together).
+KERNEL_NAMES = {"simt": "fwd_simt_kernel", "tc": "fwd_tc_kernel",
+                "split": "fwd_prep_kernel + fwd_rec_kernel"}
 HEADLINE = "fixed_bf16_h32_t8192"
 PACKED = "packed_bf16_h32_t8192_25seg"
 L2_FLUSH_BYTES = 256 << 20
@@ -97,7 +101,7 @@ def measured_peaks():
 
 
 def kernel_source_digest(impl_name: str) -> str:
-    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu"}[impl_name]
+    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu"}[impl_name]
     path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -298,7 +302,8 @@ def run_ours(args, dist):
         has_seg = d["segment_ids"] is not None
         o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
         fs = torch.empty(w.B, w.H, w.K, w.V, dtype=torch.float32, device=dev)
-        ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg, dev)
+        ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg, dev,
+                                 impl=args.kda_impl)
 
         def step():
             kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
@@ -350,22 +355,26 @@ def run_ours(args, dist):
         flops = algorithmic_flops(w)
         t = res["ms"] * 1e-3
         gbs = nbytes / t / 1e9
-        impl_name = "tc" if kernel_impl(w) == "tc" else "simt"
+        impl_name = kernel_impl(w)
         traffic = profiled_traffic(impl_name, w.name)
         return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(gbs / hbm_peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"
                 if peak_src == "measured" else "fallback 6.8 TB/s",
-                "kernel": f"fwd_{impl_name}_kernel", "algorithmic_bytes": nbytes,
+                "kernel": KERNEL_NAMES[impl_name], "algorithmic_bytes": nbytes,
                 "algorithmic_flops": flops,
                 "tensor_frac": round(flops / t / 1e12 / tc_peak, 4),
                 "roofline_ms": round(max(nbytes / (hbm_peak * 1e9), flops / (tc_peak * 1e12)) * 1e3, 4)}
 
     def kernel_impl(w):
-        if args.kda_impl == "simt":
-            return "simt"
-        tc = w.dtype == "bf16" and w.K == 128 and w.V == 128 and tc_available()
-        return "tc" if tc else "simt"
+        import gated_delta_rule_21_gb300 as kda
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        has_seg = w.segments is not None
+        if args.kda_impl in ("simt", "tc", "split"):
+            return args.kda_impl
+        if kda.workspace_size(w.B, w.T, w.H, w.K, w.V, dt, has_seg, impl="split") > 0:
+            return "split"
+        return "tc" if kda.impl_available("tc", w.B, w.T, w.H, w.K, w.V, dt) else "simt"
 
     clocks.start()
     head = measure(args.workload, with_e2e=not args.no_e2e, clocks_=clocks)
@@ -375,8 +384,8 @@ def run_ours(args, dist):
 
     w = head["workload"]
     value = whole_job_value(dist.world, head["tokens"], head["ms_max"])
-    launches_per_step = 1 + (1 if head["has_seg"] else 0)
     impl_used = kernel_impl(w)
+    launches_per_step = (2 if impl_used == "split" else 1) + (1 if head["has_seg"] else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_max"],
@@ -384,7 +393,7 @@ def run_ours(args, dist):
         "vs_baseline": (value / (w.B * w.T / (PAGES_TPU_FIXED_MS * 1e-3))
                         if args.workload == HEADLINE else None),
         "vs_baseline_ref": "pages' TPU v7x tokamax #19 fixed forward, 1.870 ms (other hardware; context)",
-        "dtype": "bf16" if impl_used == "tc" else "f32",
+        "dtype": "bf16" if impl_used in ("tc", "split") else "f32",
         "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
                    "qkv_dtype": w.dtype, "chunk": CHUNK, "initial_state": w.init_state_std is not None,
@@ -403,16 +412,11 @@ def run_ours(args, dist):
                           "unit": "tokens/s", "roofline": roofline(packed),
                           "vs_pages_tpu": (packed["tokens"] / (packed["ms_max"] * 1e-3))
                           / (pw.B * pw.T / (PAGES_TPU_PACKED_MS * 1e-3)),
-                          "gpu_launches": 2 * args.steps}
-        line["gpu_launches"] += 2 * args.steps
+                          "gpu_launches": (1 + (2 if kernel_impl(pw) == "split" else 1)) * args.steps}
+        line["gpu_launches"] += line["packed"]["gpu_launches"]
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, budget_s=args.cpu_seconds)
     return line
-
-
-def tc_available() -> bool:
-    import gated_delta_rule_21_gb300 as kda
-    return kda.impl_available("tc", 1, 64, 1, 128, 128, torch.bfloat16)
 
 
 # ----------------------------------------------------------------------------

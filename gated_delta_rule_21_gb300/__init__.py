@@ -31,7 +31,7 @@ KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
                 3: "KDA_ERR_ALIGNMENT", 4: "KDA_ERR_WORKSPACE", 5: "KDA_ERR_CUDA",
                 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_DEVICE"}
-IMPLS = {"auto": 0, "simt": 1, "tc": 2}
+IMPLS = {"auto": 0, "simt": 1, "tc": 2, "split": 3}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 CHUNK = 64
 
@@ -69,6 +69,8 @@ def lib():
         sp = ctypes.POINTER(kda_shape)
         L.kda_chunk_fwd_workspace_size.argtypes = [sp, i]
         L.kda_chunk_fwd_workspace_size.restype = u64
+        L.kda_chunk_fwd_workspace_size_for.argtypes = [sp, i, i]
+        L.kda_chunk_fwd_workspace_size_for.restype = u64
         L.kda_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp,
                                     vp, vp, u64, vp]
         L.kda_chunk_fwd.restype = i
@@ -112,15 +114,20 @@ def make_shape(B, T, H, K, V, dtype) -> kda_shape:
     return kda_shape(int(B), int(T), int(H), int(K), int(V), DTYPES[dtype])
 
 
-def workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
+def workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
+                   impl=None) -> int:
+    """Workspace bytes: the minimum (impl None) or what ``impl`` needs."""
     s = make_shape(B, T, H, K, V, dtype)
-    return int(lib().kda_chunk_fwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+    if impl is None:
+        return int(lib().kda_chunk_fwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+    return int(lib().kda_chunk_fwd_workspace_size_for(ctypes.byref(s), int(bool(has_segment_ids)),
+                                                      IMPLS[impl]))
 
 
 def alloc_workspace(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
-                    device=None) -> torch.Tensor:
-    """Zero-filled workspace of the required size (uint8 device tensor)."""
-    n = workspace_size(B, T, H, K, V, dtype, has_segment_ids)
+                    device=None, impl=None) -> torch.Tensor:
+    """Zero-filled workspace of the size ``impl`` needs (uint8 device tensor)."""
+    n = workspace_size(B, T, H, K, V, dtype, has_segment_ids, impl)
     if n == 0:
         raise KdaError(1, "workspace_size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
@@ -185,7 +192,7 @@ def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None
             B, H, K, V, dtype=torch.float32, device=dev)
         _check(fs, "final_state_out", (B, H, K, V), torch.float32, dev)
     if workspace is None:
-        workspace = alloc_workspace(B, T, H, K, V, dt, segment_ids is not None, dev)
+        workspace = alloc_workspace(B, T, H, K, V, dt, segment_ids is not None, dev, impl=impl)
     s = make_shape(B, T, H, K, V, dt)
     st = lib().kda_chunk_fwd_ex(
         ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),

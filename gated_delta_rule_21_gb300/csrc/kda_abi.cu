@@ -74,6 +74,26 @@ size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids) {
   return ws_bytes(s->B, s->T, has_segment_ids != 0);
 }
 
+size_t kda_chunk_fwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
+                                        kda_impl impl) {
+  if (check_shape(s) != KDA_OK) return 0;
+  const bool has_seg = has_segment_ids != 0;
+  const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
+  const size_t base = ws_bytes(s->B, s->T, has_seg);
+  const bool split_ok = fwd_split_supported(s->K, s->V, bf16, has_seg, 0);
+  switch (impl) {
+    case KDA_IMPL_SIMT:
+      return base;
+    case KDA_IMPL_TC:
+      return fwd_tc_supported(s->K, s->V, bf16, 0) ? base : 0;
+    case KDA_IMPL_SPLIT:
+      return split_ok ? split_workspace_bytes(s->B, s->T, s->H) : 0;
+    case KDA_IMPL_AUTO:
+      return split_ok ? split_workspace_bytes(s->B, s->T, s->H) : base;
+  }
+  return 0;
+}
+
 kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
                             const void *v, const float *g, const float *beta,
                             float scale, int chunk_size,
@@ -86,7 +106,8 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
   if (st != KDA_OK) return st;
   if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
   if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
-  if (impl != KDA_IMPL_AUTO && impl != KDA_IMPL_SIMT && impl != KDA_IMPL_TC)
+  if (impl != KDA_IMPL_AUTO && impl != KDA_IMPL_SIMT && impl != KDA_IMPL_TC &&
+      impl != KDA_IMPL_SPLIT)
     return KDA_ERR_INVALID_ARG;
   if (v_tile < 0) return KDA_ERR_INVALID_ARG;
   if (!(scale == scale)) return KDA_ERR_INVALID_ARG;  // NaN scale
@@ -101,16 +122,21 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
 
   const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
   const bool tc_ok = fwd_tc_supported(s->K, s->V, bf16, v_tile);
-  bool use_tc;
-  if (impl == KDA_IMPL_TC) {
+  const bool split_ok = fwd_split_supported(s->K, s->V, bf16, has_seg, v_tile);
+  const size_t split_need = split_ok ? split_workspace_bytes(s->B, s->T, s->H) : 0;
+  bool use_tc = false, use_split = false;
+  if (impl == KDA_IMPL_SPLIT) {
+    if (!split_ok) return KDA_ERR_UNSUPPORTED;
+    if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE;
+    use_split = true;
+  } else if (impl == KDA_IMPL_TC) {
     if (!tc_ok) return KDA_ERR_UNSUPPORTED;
     use_tc = true;
-  } else if (impl == KDA_IMPL_SIMT) {
-    use_tc = false;
-  } else {
-    use_tc = tc_ok;
+  } else if (impl == KDA_IMPL_AUTO) {
+    use_split = split_ok && workspace_bytes >= split_need;
+    use_tc = !use_split && tc_ok;
   }
-  if (!use_tc) {
+  if (!use_tc && !use_split) {
     if (v_tile == 0) v_tile = 32;
     if (v_tile != 32 || s->V % v_tile) return KDA_ERR_UNSUPPORTED;
   }
@@ -142,7 +168,9 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
                             workspace, cs);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  e = use_tc ? launch_fwd_tc(p, cs) : launch_fwd_simt(p, bf16, cs);
+  if (use_split) e = launch_fwd_split(p, workspace, cs);
+  else if (use_tc) e = launch_fwd_tc(p, cs);
+  else e = launch_fwd_simt(p, bf16, cs);
   return from_cuda(e);
 }
 
@@ -154,6 +182,7 @@ int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile) {
     case KDA_IMPL_AUTO: return fwd_tc_supported(s->K, s->V, bf16, v_tile) || simt_ok;
     case KDA_IMPL_SIMT: return simt_ok;
     case KDA_IMPL_TC: return fwd_tc_supported(s->K, s->V, bf16, v_tile);
+    case KDA_IMPL_SPLIT: return fwd_split_supported(s->K, s->V, bf16, false, v_tile);
   }
   return 0;
 }

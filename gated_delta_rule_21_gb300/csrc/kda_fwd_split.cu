@@ -1,0 +1,822 @@
+// kda_fwd_split.cu -- chunked KDA forward as two tensor-core kernels:
+//
+//   1. fwd_prep_kernel: every (row, chunk, head) item is independent of the
+//      recurrent state, so all of them run in parallel over the whole GPU.
+//      Per item (64 tokens of one head) it builds the gate cumsum and decay
+//      factors, the intra-chunk products A_kk / A_qk on tcgen05 (one MMA per
+//      16-row block), the triangular inverse T = (I + beta A_kk)^-1 (fp32,
+//      blocked), and [w | u] = T [beta K e^G | beta V] on tcgen05, and writes
+//      the operands the recurrence needs into the workspace, already in the
+//      shared-memory layouts the tensor cores read:
+//         [w ; Q e^G] (128 x 128 bf16), [T ; A_qk] (128 x 64 bf16),
+//         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 fp32), e^{G_C}.
+//   2. fwd_rec_kernel: one CTA per (row, head, 32-column value tile) walks
+//      the chunks in order with the fp32 state in registers; per chunk it
+//      bulk-copies the item (double-buffered) and runs only the
+//      state-dependent MMAs:  D1 = [w ; Q e^G] S,  U = u - w S,
+//      D1 += [T ; A_qk] U,  D2 = (K e^{G_C-G})^T U,  S <- e^{G_C} S + D2,
+//      o = scale * D1[64:128].
+//
+// The arithmetic is the same chunk form, sub-block factors and rounding
+// points as the fused kernel (kda_fwd_tc.cu); see there for the algebra.
+// This path needs a workspace of split_workspace_bytes() (about 97 KB per
+// chunk and head) and serves rows without segment ids.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_internal.cuh"
+#include "kda_tc_common.cuh"
+
+namespace kda {
+namespace {
+using namespace tc;
+
+constexpr int C = kChunk;
+constexpr int KD = 128;
+constexpr int VD = 128;
+constexpr int VT = 32;
+
+// ---- one workspace item (per row, chunk, head) ----------------------------
+constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: K-major, 128 rows, Kd 128
+constexpr uint32_t I_TAQ = 32768;     // [T ; A_qk]: K-major, 128 rows, Kd 64
+constexpr uint32_t I_KHT = 49152;     // (K e^{G_C-G})^T: MN-major, 128 x Kd 64
+constexpr uint32_t I_U = 65536;       // u fp32 [vt][r][32]
+constexpr uint32_t I_GAM = 98304;     // e^{G_C} fp32 [128]
+constexpr uint32_t ITEM_BYTES = 99328;     // 97 KiB, 1 KiB aligned
+constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
+
+// ---- prep kernel shared memory ----------------------------------------------
+constexpr int PT = 512;                       // threads
+constexpr uint32_t P_RAW_Q = 0, P_RAW_K = 16384, P_RAW_G = 32768;
+constexpr uint32_t P_RAW_V = 65536;           // 64 x 128 bf16, 256-byte rows
+constexpr uint32_t P_RAW_TX = 16384 * 2 + 32768 + 16384;
+constexpr uint32_t P_X = 81920;               // 128 x Kd 128
+constexpr uint32_t P_Y = P_X + 32768;         // Y_0..Y_3, 160 rows x Kd 128
+constexpr uint32_t P_RHST = P_Y + 40960;      // [beta K e^G | beta V]^T MN-major 256 x 64
+constexpr uint32_t P_MISC = P_RHST + 32768;
+constexpr uint32_t P_BETA = P_MISC;           // 64 fp32
+constexpr uint32_t P_DBLK = P_MISC + 256;     // 4 x 128 fp32
+constexpr uint32_t P_BSUM = P_DBLK + 2048;    // 4 x 128 fp32 block sums of g
+constexpr uint32_t P_BAR = P_BSUM + 2048;     // tma, mma
+constexpr uint32_t P_SLOT = P_BAR + 16;
+constexpr uint32_t P_ABORT = P_SLOT + 4;
+constexpr uint32_t P_SMEM = P_ABORT + 12;
+constexpr uint32_t P_ALLOC = P_SMEM + 1024;
+constexpr int LDF = C + 4;
+constexpr uint32_t P_AKK = P_X;                    // fp32 64 x 68
+constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68
+constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T bf16 K-major (128-row operand)
+constexpr uint32_t P_SCR = P_TB + 16384;           // 3 x 256 fp32
+static_assert(P_SCR + 3072 <= P_RHST, "prep aliases inside X / Y");
+static_assert(P_ALLOC <= 232448, "prep smem fits");
+constexpr uint32_t P_TM_TX = 256;  // TMEM: A blocks at 0/32/64/128, [w | u] at 256
+
+__device__ __forceinline__ uint32_t p_y_off(int b) {
+  return P_Y + 256u * (uint32_t)(8 * b * (b + 1));
+}
+__device__ __forceinline__ uint32_t tm_a(int b) {
+  return b == 0 ? 0u : b == 1 ? 32u : b == 2 ? 64u : 128u;
+}
+__device__ __forceinline__ int piece_count(int quad) { return (quad & 1) ? 7 : 3; }
+__device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
+  if ((quad & 1) == 0) {
+    b = i == 0 ? 0 : 1;
+    pp = i == 0 ? 0 : i - 1;
+  } else {
+    b = i < 3 ? 2 : 3;
+    pp = i < 3 ? i : i - 3;
+  }
+}
+
+__device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const float (&v)[8]) {
+  uint4 w;
+  w.x = pack_bf16(v[0], v[1]);
+  w.y = pack_bf16(v[2], v[3]);
+  w.z = pack_bf16(v[4], v[5]);
+  w.w = pack_bf16(v[6], v[7]);
+  *reinterpret_cast<uint4 *>(g + off) = w;
+}
+
+__global__ void __launch_bounds__(PT, 1)
+    fwd_prep_kernel(const FwdParams p, unsigned char *items, int n_chunks,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  float *sBeta = reinterpret_cast<float *>(smem + P_BETA);
+  float *sDblk = reinterpret_cast<float *>(smem + P_DBLK);
+  float *sBsum = reinterpret_cast<float *>(smem + P_BSUM);
+  float *sG = reinterpret_cast<float *>(smem + P_RAW_G);
+  float *sAkk = reinterpret_cast<float *>(smem + P_AKK);
+  float *sT = reinterpret_cast<float *>(smem + P_TF);
+  float *sScr = reinterpret_cast<float *>(smem + P_SCR);
+  volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + P_ABORT);
+  const uint32_t tma_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, sub = warp >> 2;  // 4 warps per TMEM lane quadrant
+  const int L = 32 * quad + lane;
+  const int H = p.H, T = p.T;
+
+  if (warp == 0) tmem_alloc(sb + P_SLOT, 512);
+  if (tid == 0) {
+    mbar_init(tma_bar, 1);
+    mbar_init(mma_bar, 1);
+    *sAbort = 0u;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P_SLOT);
+  const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
+  uint32_t tma_phase = 0, mma_phase = 0, tma_pending = 0, mma_pending = 0;
+  bool tma_inflight = false, mma_inflight = false;
+  auto abort_all = [&]() {
+    *sAbort = 1u;
+    set_status(p.status, KDA_DEVICE_TIMEOUT);
+  };
+
+  const uint32_t n_items = (uint32_t)p.B * n_chunks * H;
+  auto item_coords = [&](uint32_t it, int &b, int &c, int &h) {
+    h = (int)(it % (uint32_t)H);
+    const uint32_t bc = it / (uint32_t)H;
+    c = (int)(bc % (uint32_t)n_chunks);
+    b = (int)(bc / (uint32_t)n_chunks);
+  };
+  auto issue_tma = [&](uint32_t it) {
+    int b, c, h;
+    item_coords(it, b, c, h);
+    const int y = b * T + c * C;
+    mbar_expect_tx(tma_bar, P_RAW_TX);
+    tma_load_2d(sb + P_RAW_Q, &tm_q, h * KD, y, tma_bar);
+    tma_load_2d(sb + P_RAW_K, &tm_k, h * KD, y, tma_bar);
+    tma_load_2d(sb + P_RAW_G, &tm_g, h * KD, y, tma_bar);
+    tma_load_2d(sb + P_RAW_V, &tm_v, h * VD, y, tma_bar);
+  };
+  auto load_beta = [&](uint32_t it) -> float {
+    int b, c, h;
+    item_coords(it, b, c, h);
+    const int r = tid;
+    const int t = c * C + r;
+    return t < T ? p.beta[((size_t)b * T + t) * H + h] : 0.f;
+  };
+
+  uint32_t item = blockIdx.x;
+  float beta_next = 0.f;
+  if (item < n_items) {
+    if (tid == 0) issue_tma(item);
+    tma_inflight = true;
+    tma_pending = tma_phase;
+    if (tid < C) beta_next = load_beta(item);
+  }
+  for (; item < n_items; item += gridDim.x) {
+    int b_, c_, h_;
+    item_coords(item, b_, c_, h_);
+    const int n = min(C, T - c_ * C);
+    const uint32_t next = item + gridDim.x;
+    const bool has_next = next < n_items;
+    unsigned char *gi = items + (size_t)item * ITEM_BYTES;
+
+    if (tid < C) sBeta[tid] = beta_next;
+    if (!mbar_wait(tma_bar, tma_phase)) abort_all();
+    else tma_inflight = false;
+    tma_phase ^= 1u;
+    __syncthreads();
+    if (*sAbort) goto done;
+
+    // ---- gate cumsum: one thread per (channel, 16-row block) ----
+    {
+      const int c = tid & 127, q4 = tid >> 7;
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * q4 + i;
+        v[i] = r < n ? sG[r * KD + c] : 0.f;
+      }
+#pragma unroll
+      for (int i = 1; i < 16; ++i) v[i] += v[i - 1];
+      sBsum[q4 * KD + c] = v[15];
+      sDblk[q4 * KD + c] = ex2(v[15] * kLog2e);
+      __syncthreads();
+      float off = 0.f;
+      for (int i = 0; i < q4; ++i) off += sBsum[i * KD + c];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sG[(16 * q4 + i) * KD + c] = v[i] + off;
+    }
+    __syncthreads();
+
+    // ---- operands: X, Y_b, (beta K e^G)^T in smem; Q e^G, K e^{G_C-G} out ----
+    {
+      const int rl = tid & 7, cg = (tid >> 3) & 15, hi = (tid >> 7) & 1, bp = tid >> 8;
+      const int cc0 = cg * 8;
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int b = 2 * bp + i2;  // warp-uniform block of this row
+        const int r = kSub * b + 8 * hi + rl;
+        const bool valid = r < n;
+        const float br = sBeta[r];
+        float D[kNumSub][8], Pb[8], Eb[8], kk[8], qq[8], G[8];
+#pragma unroll
+        for (int i = 0; i < kNumSub; ++i) {
+          const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
+          const float4 d0 = dp[0], d1 = dp[1];
+          D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
+          D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
+        }
+        {
+          const float4 *ep = reinterpret_cast<const float4 *>(sG + (b * kSub + kSub - 1) * KD + cc0);
+          const float4 e0 = ep[0], e1v = ep[1];
+          Eb[0] = e0.x; Eb[1] = e0.y; Eb[2] = e0.z; Eb[3] = e0.w;
+          Eb[4] = e1v.x; Eb[5] = e1v.y; Eb[6] = e1v.z; Eb[7] = e1v.w;
+          const float4 *pq = reinterpret_cast<const float4 *>(sG + (b > 0 ? b * kSub - 1 : 0) * KD + cc0);
+          const float4 p0 = pq[0], p1 = pq[1];
+          const float z = b > 0 ? 1.f : 0.f;
+          Pb[0] = z * p0.x; Pb[1] = z * p0.y; Pb[2] = z * p0.z; Pb[3] = z * p0.w;
+          Pb[4] = z * p1.x; Pb[5] = z * p1.y; Pb[6] = z * p1.z; Pb[7] = z * p1.w;
+          const float4 *gp = reinterpret_cast<const float4 *>(sG + r * KD + cc0);
+          const float4 g0 = gp[0], g1 = gp[1];
+          G[0] = g0.x; G[1] = g0.y; G[2] = g0.z; G[3] = g0.w;
+          G[4] = g1.x; G[5] = g1.y; G[6] = g1.z; G[7] = g1.w;
+        }
+        ld_bf16x8(smem + P_RAW_K + r * 256 + cc0 * 2, kk);
+        ld_bf16x8(smem + P_RAW_Q + r * 256 + cc0 * 2, qq);
+        float xk[8], xq[8], qt[8], kb[8], kh[8], yd[8], y1[8], y2[8], y3[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float pre = 1.f, suf = 1.f, Db = 1.f, x2 = 1.f, x3 = 1.f;
+#pragma unroll
+          for (int i = 0; i < kNumSub; ++i) {
+            const float Di = D[i][j];
+            if (i < b) pre *= Di;
+            if (i > b) suf *= Di;
+            if (i == b) Db = Di;
+            if (i == b + 1) { x2 *= Di; x3 *= Di; }
+            if (i == b + 2) x3 *= Di;
+          }
+          const float gl = G[j] * kLog2e;
+          const float e1 = ex2(gl - Pb[j] * kLog2e);  // e^{G - P_b}
+          const float e2 = ex2(Eb[j] * kLog2e - gl);  // e^{E_b - G}
+          const float kv = valid ? kk[j] : 0.f;
+          const float qv = valid ? qq[j] : 0.f;
+          xk[j] = kv * e1;
+          xq[j] = qv * e1;
+          qt[j] = xq[j] * pre;
+          kb[j] = xk[j] * (br * pre);
+          const float ke2 = kv * e2;
+          kh[j] = ke2 * suf;
+          yd[j] = ke2 * __frcp_rn(Db);
+          y1[j] = ke2;
+          y2[j] = ke2 * x2;
+          y3[j] = ke2 * x3;
+        }
+        st_bf16x8(smem, P_X + op_off(r, cc0, KD), xk);
+        st_bf16x8(smem, P_X + op_off(64 + r, cc0, KD), xq);
+        st_bf16x8(smem, p_y_off(b) + op_off(r, cc0, KD), yd);
+        if (b + 1 < kNumSub) st_bf16x8(smem, p_y_off(b + 1) + op_off(r, cc0, KD), y1);
+        if (b + 2 < kNumSub) st_bf16x8(smem, p_y_off(b + 2) + op_off(r, cc0, KD), y2);
+        if (b + 3 < kNumSub) st_bf16x8(smem, p_y_off(b + 3) + op_off(r, cc0, KD), y3);
+        st_bf16x8(smem, P_RHST + mn_off(cc0, r, C), kb);
+        st_g16(gi, I_WQ + op_off(64 + r, cc0, KD), qt);
+        st_g16(gi, I_KHT + mn_off(cc0, r, C), kh);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {  // (beta V)^T
+        const int r = tid >> 3, vg = (tid & 7) + 8 * e;
+        float vv[8];
+        ld_bf16x8(smem + P_RAW_V + r * 256 + vg * 16, vv);
+        const float br = r < n ? sBeta[r] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vv[i] *= br;
+        st_bf16x8(smem, P_RHST + mn_off(KD + 8 * vg, r, C), vv);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- intra-chunk products on the tensor cores; next item's tiles ----
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int b = 0; b < kNumSub; ++b)
+        mma_group(tmem + tm_a(b), sb + P_X, sb + p_y_off(b), KD, 16 * (b + 1), false, 0, 0);
+      mma_commit(mma_bar);
+      if (has_next) issue_tma(next);
+    }
+    if (has_next) {
+      tma_inflight = true;
+      tma_pending = tma_phase;
+      if (tid < C) beta_next = load_beta(next);
+    }
+    mma_inflight = true;
+    mma_pending = mma_phase;
+    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+    else mma_inflight = false;
+    mma_phase ^= 1u;
+    __syncthreads();
+    if (*sAbort) goto done;
+    tc_fence_after();
+
+    // ---- beta A_kk (fp32, strict) to smem; A_qk (inclusive) to the item ----
+    {
+      const int r = L & 63;
+      const bool is_q = L >= 64;
+      const int bme = r >> 4;
+      const int np = piece_count(quad);
+      for (int pi = sub; pi < np; pi += 8) {
+        float v[2][16];
+        int bb[2], pp[2];
+        piece(quad, pi, bb[0], pp[0]);
+        const bool two = pi + 4 < np;
+        if (two) {
+          piece(quad, pi + 4, bb[1], pp[1]);
+          tmem_ld16x2(tq + tm_a(bb[0]) + 16 * pp[0], tq + tm_a(bb[1]) + 16 * pp[1], v[0], v[1]);
+        } else {
+          bb[1] = -1;
+          pp[1] = 0;
+          tmem_ld16(tq + tm_a(bb[0]) + 16 * pp[0], v[0]);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (bb[e] != bme) continue;
+          const int j0 = 16 * pp[e];
+          if (!is_q) {
+            const float br = sBeta[r];
+            float4 *dst = reinterpret_cast<float4 *>(sAkk + r * LDF + j0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float a[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                a[i] = (j0 + 4 * q4 + i < r) ? br * v[e][4 * q4 + i] : 0.f;
+              dst[q4] = make_float4(a[0], a[1], a[2], a[3]);
+            }
+          } else {
+            float a0[8], a1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              a0[i] = (j0 + i <= r) ? v[e][i] : 0.f;
+              a1[i] = (j0 + 8 + i <= r) ? v[e][8 + i] : 0.f;
+            }
+            st_g16(gi, I_TAQ + op_off(64 + r, j0, C), a0);
+            st_g16(gi, I_TAQ + op_off(64 + r, j0 + 8, C), a1);
+          }
+        }
+      }
+      if (is_q && sub == 0) {
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int jj = 16 * (bme + 1); jj < C; jj += 8) st_g16(gi, I_TAQ + op_off(64 + r, jj, C), z);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- T = (I + beta A_kk)^-1, blocked fp32 ----
+    if (tid < 64) {
+      const int i = tid >> 4, cc = tid & 15, base = 16 * i;
+      float x[16];
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) x[rr] = rr == cc ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m) {
+        const float xm = x[m];
+#pragma unroll
+        for (int rr = m + 1; rr < 16; ++rr)
+          x[rr] = fmaf(-sAkk[(base + rr) * LDF + base + m], xm, x[rr]);
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) sT[(base + rr) * LDF + base + cc] = x[rr];
+    }
+    __syncthreads();
+    for (int d = 1; d < kNumSub; ++d) {
+      const int nblk = kNumSub - d;
+      const int blk = tid >> 6, e = tid & 63, ra = 2 * (e >> 3), cb = 2 * (e & 7);
+      const bool act = blk < nblk;
+      const int i = d + blk, j = blk;
+      if (act) {
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        for (int m = j; m < i; ++m) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float l0 = sAkk[(16 * i + ra) * LDF + 16 * m + t];
+            const float l1 = sAkk[(16 * i + ra + 1) * LDF + 16 * m + t];
+            const float2 tv = *reinterpret_cast<const float2 *>(sT + (16 * m + t) * LDF + 16 * j + cb);
+            a00 = fmaf(l0, tv.x, a00); a01 = fmaf(l0, tv.y, a01);
+            a10 = fmaf(l1, tv.x, a10); a11 = fmaf(l1, tv.y, a11);
+          }
+        }
+        float *mm = sScr + blk * 256;
+        *reinterpret_cast<float2 *>(mm + ra * 16 + cb) = make_float2(a00, a01);
+        *reinterpret_cast<float2 *>(mm + (ra + 1) * 16 + cb) = make_float2(a10, a11);
+      }
+      __syncthreads();
+      if (act) {
+        const float *mm = sScr + blk * 256;
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float d0 = sT[(16 * i + ra) * LDF + 16 * i + t];
+          const float d1 = sT[(16 * i + ra + 1) * LDF + 16 * i + t];
+          const float2 mv = *reinterpret_cast<const float2 *>(mm + t * 16 + cb);
+          a00 = fmaf(d0, mv.x, a00); a01 = fmaf(d0, mv.y, a01);
+          a10 = fmaf(d1, mv.x, a10); a11 = fmaf(d1, mv.y, a11);
+        }
+        *reinterpret_cast<float2 *>(sT + (16 * i + ra) * LDF + 16 * j + cb) = make_float2(-a00, -a01);
+        *reinterpret_cast<float2 *>(sT + (16 * i + ra + 1) * LDF + 16 * j + cb) = make_float2(-a10, -a11);
+      }
+      __syncthreads();
+    }
+    {  // T -> bf16: smem operand (rows 0..63) and rows 0..63 of [T ; A_qk]
+      const int r = tid >> 3, j8 = (tid & 7) * 8;
+      const float4 *src = reinterpret_cast<const float4 *>(sT + r * LDF + j8);
+      const float4 a = src[0], b4 = src[1];
+      float t8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+      if ((j8 >> 4) > (r >> 4)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = 0.f;
+      }
+      st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
+      st_g16(gi, I_TAQ + op_off(r, j8, C), t8);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- [w | u] = T [beta K e^G | beta V] (N = 256) ----
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tmem + P_TM_TX, sb + P_TB, sb + P_RHST, C, KD + VD, false, 0, 1);
+      mma_commit(mma_bar);
+    }
+    mma_inflight = true;
+    mma_pending = mma_phase;
+    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+    else mma_inflight = false;
+    mma_phase ^= 1u;
+    __syncthreads();
+    if (*sAbort) goto done;
+    tc_fence_after();
+    if (quad < 2) {  // lanes 0..63: chunk rows; 4 warps share the 16 column pieces
+      const int r = L;
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int p0 = sub + 8 * k2, p1 = p0 + 4;  // pieces of 16 columns
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + P_TM_TX + 16 * p0, tq + P_TM_TX + 16 * p1, v0, v1);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pc = e ? p1 : p0;
+          const float *vv = e ? v1 : v0;
+          if (pc < 8) {  // w columns 16 pc .. 16 pc + 15
+            float a[8], c8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { a[i] = vv[i]; c8[i] = vv[8 + i]; }
+            st_g16(gi, I_WQ + op_off(r, 16 * pc, KD), a);
+            st_g16(gi, I_WQ + op_off(r, 16 * pc + 8, KD), c8);
+          } else {  // u columns 16 (pc - 8) ..
+            const int col = 16 * (pc - 8), vt = col >> 5, cv = col & 31;
+            float4 *dst = reinterpret_cast<float4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 4);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_float4(vv[4 * q4], vv[4 * q4 + 1], vv[4 * q4 + 2], vv[4 * q4 + 3]);
+          }
+        }
+      }
+    }
+    if (tid < KD) {
+      float gam = 1.f;
+#pragma unroll
+      for (int i = 0; i < kNumSub; ++i) gam *= sDblk[i * KD + tid];
+      reinterpret_cast<float *>(gi + I_GAM)[tid] = gam;
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+done:
+  if (tma_inflight) mbar_wait(tma_bar, tma_pending);
+  if (mma_inflight) mbar_wait(mma_bar, mma_pending);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---- recurrence kernel --------------------------------------------------------
+constexpr int RT = 128;
+// One stage: [w ; Q e^G] | [T ; A_qk] | K^T (one 64 KiB copy), this unit's
+// u tile (64 x 32 fp32), e^{G_C}.
+constexpr uint32_t S_U = 65536, S_GAM = S_U + 8192, S_BYTES = S_GAM + 512;
+constexpr uint32_t R_STAGE = 74752;            // S_BYTES rounded to 1 KiB
+constexpr uint32_t R_ST = 2 * R_STAGE;         // S^T MN-major 32 x Kd 128
+constexpr uint32_t R_UT = R_ST + 8192;         // U^T MN-major 32 x Kd 64
+constexpr uint32_t R_BAR = R_UT + 4096;        // stage0, stage1, mma
+constexpr uint32_t R_SLOT = R_BAR + 24;
+constexpr uint32_t R_ABORT = R_SLOT + 4;
+constexpr uint32_t R_SMEM = R_ABORT + 12;
+constexpr uint32_t R_ALLOC = R_SMEM + 1024;
+static_assert(S_BYTES <= R_STAGE && I_KHT + 16384 == S_U, "stage layout");
+static_assert(R_ALLOC <= 232448, "rec smem fits");
+
+__global__ void __launch_bounds__(RT, 1)
+    fwd_rec_kernel(const FwdParams p, const unsigned char *items, int n_chunks) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + R_ABORT);
+  const uint32_t bar0 = sb + R_BAR, mma_bar = sb + R_BAR + 16;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int L = tid;  // 4 warps = the 4 TMEM lane quadrants
+  const int H = p.H, T = p.T;
+
+  if (warp == 0) tmem_alloc(sb + R_SLOT, 64);
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    mbar_init(mma_bar, 1);
+    *sAbort = 0u;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + R_SLOT);
+  const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t TM_D1 = 0, TM_D2 = 32;
+  uint32_t st_phase[2] = {0u, 0u}, mma_phase = 0;
+  uint32_t st_issued = 0;  // per-stage bit: copy issued and not yet waited
+  bool mma_inflight = false;
+  uint32_t mma_pending = 0;
+  auto abort_all = [&]() {
+    *sAbort = 1u;
+    set_status(p.status, KDA_DEVICE_TIMEOUT);
+  };
+  auto issue_stage = [&](int s, const unsigned char *src, int vt) {
+    const uint32_t dst = sb + (uint32_t)s * R_STAGE;
+    const uint32_t bar = bar0 + 8u * (uint32_t)s;
+    mbar_expect_tx(bar, S_BYTES);
+    bulk_load(dst, src, S_U, bar);
+    bulk_load(dst + S_U, src + I_U + (size_t)vt * 8192, 8192, bar);
+    bulk_load(dst + S_GAM, src + I_GAM, 512, bar);
+  };
+
+  float S[VT];
+  const uint32_t n_units = (uint32_t)p.B * H * p.n_vtiles;
+  for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const int vt = (int)(unit % (uint32_t)p.n_vtiles);
+    const int h = (int)((unit / (uint32_t)p.n_vtiles) % (uint32_t)H);
+    const int b = (int)(unit / ((uint32_t)p.n_vtiles * H));
+    const int vc0 = vt * VT;
+    auto item_ptr = [&](int c) {
+      return items + ((size_t)((size_t)b * n_chunks + c) * H + h) * ITEM_BYTES;
+    };
+    {
+      const int c = tid;
+      if (p.initial_state) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.initial_state + (((size_t)b * H + h) * KD + c) * p.V + vc0);
+#pragma unroll
+        for (int q4 = 0; q4 < VT / 4; ++q4) {
+          const float4 x = src[q4];
+          S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < VT; ++i) S[i] = 0.f;
+      }
+#pragma unroll
+      for (int vg = 0; vg < VT / 8; ++vg) {
+        float t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
+        st_bf16x8(smem, R_ST + mn_off(8 * vg, c, KD), t8);
+      }
+    }
+    if (tid == 0) {
+      issue_stage(0, item_ptr(0), vt);
+      if (n_chunks > 1) issue_stage(1, item_ptr(1), vt);
+    }
+    st_issued = n_chunks > 1 ? 3u : 1u;
+    fence_proxy_async();
+    __syncthreads();
+
+    for (int c = 0; c < n_chunks; ++c) {
+      const int s = c & 1;
+      const int n = min(C, T - c * C);
+      const size_t tok0 = (size_t)b * T + (size_t)c * C;
+      const unsigned char *stg = smem + (uint32_t)s * R_STAGE;
+      const uint32_t sstg = sb + (uint32_t)s * R_STAGE;
+      if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
+      else st_issued &= ~(1u << s);
+      st_phase[s] ^= 1u;
+      __syncthreads();
+      if (*sAbort) goto done;
+
+      // D1 = [w ; Q e^G] S
+      if (tid == 0) {
+        tc_fence_after();
+        mma_group(tmem + TM_D1, sstg + I_WQ, sb + R_ST, KD, VT, false, 0, 1);
+        mma_commit(mma_bar);
+      }
+      mma_inflight = true;
+      mma_pending = mma_phase;
+      if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+      else mma_inflight = false;
+      mma_phase ^= 1u;
+      __syncthreads();
+      if (*sAbort) goto done;
+      tc_fence_after();
+
+      // U = u - w S  (lanes 0..63)
+      if (warp < 2) {
+        const int r = L;
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
+        const float4 *up = reinterpret_cast<const float4 *>(stg + S_U + (size_t)r * VT * 4);
+#pragma unroll
+        for (int vg = 0; vg < VT / 8; ++vg) {
+          const float4 u0 = up[2 * vg], u1 = up[2 * vg + 1];
+          const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = 8 * vg + i;
+            a[i] = uu[i] - (col < 16 ? v0[col & 15] : v1[col & 15]);
+          }
+          st_bf16x8(smem, R_UT + mn_off(8 * vg, r, C), a);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
+      if (tid == 0) {
+        tc_fence_after();
+        mma_group(tmem + TM_D1, sstg + I_TAQ, sb + R_UT, C, VT, true, 0, 1);
+        mma_group(tmem + TM_D2, sstg + I_KHT, sb + R_UT, C, VT, false, 1, 1);
+        mma_commit(mma_bar);
+      }
+      mma_inflight = true;
+      mma_pending = mma_phase;
+      if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+      else mma_inflight = false;
+      mma_phase ^= 1u;
+      __syncthreads();
+      if (*sAbort) goto done;
+      tc_fence_after();
+
+      // o rows (lanes 64..127); state update (all lanes = key rows)
+      if (warp >= 2) {
+        const int r = L - 64;
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
+        if (r < n) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0);
+#pragma unroll
+          for (int q4 = 0; q4 < VT / 8; ++q4) {
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int col = 8 * q4 + i;
+              o[i] = p.scale * (col < 16 ? v0[col & 15] : v1[col & 15]);
+            }
+            uint4 w;
+            w.x = pack_bf16(o[0], o[1]);
+            w.y = pack_bf16(o[2], o[3]);
+            w.z = pack_bf16(o[4], o[5]);
+            w.w = pack_bf16(o[6], o[7]);
+            dst[q4] = w;
+          }
+        }
+      }
+      {
+        const int cidx = L;
+        const float gam = reinterpret_cast<const float *>(stg + S_GAM)[cidx];
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + TM_D2, tq + TM_D2 + 16, v0, v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          S[i] = fmaf(gam, S[i], v0[i]);
+          S[16 + i] = fmaf(gam, S[16 + i], v1[i]);
+        }
+#pragma unroll
+        for (int vg = 0; vg < VT / 8; ++vg) {
+          float t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
+          st_bf16x8(smem, R_ST + mn_off(8 * vg, cidx, KD), t8);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (c + 2 < n_chunks) {  // stage s is free: its MMAs and reads are done
+        if (tid == 0) issue_stage(s, item_ptr(c + 2), vt);
+        st_issued |= 1u << s;
+      }
+    }
+    if (p.final_state) {
+      float4 *dst = reinterpret_cast<float4 *>(
+          p.final_state + (((size_t)b * H + h) * KD + tid) * p.V + vc0);
+#pragma unroll
+      for (int q4 = 0; q4 < VT / 4; ++q4)
+        dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+    }
+    __syncthreads();
+  }
+
+done:
+  for (int s = 0; s < 2; ++s)
+    if (st_issued & (1u << s)) mbar_wait(bar0 + 8u * s, st_phase[s]);
+  if (mma_inflight) mbar_wait(mma_bar, mma_pending);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+              uint64_t cols, uint64_t rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  const cuuint32_t box[2] = {box_cols, (cuuint32_t)C};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t split_workspace_bytes(int B, int T, int H) {
+  const size_t nc = ((size_t)T + C - 1) / C;
+  return WS_ITEMS_OFF + (size_t)B * nc * H * ITEM_BYTES;
+}
+
+bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile) {
+  return bf16 && !has_seg && K == KD && V == VD && (v_tile == 0 || v_tile == VT);
+}
+
+cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, cudaStream_t stream) {
+  if (!fwd_split_supported(p_in.K, p_in.V, true, p_in.runs.runs != nullptr, p_in.v_tile))
+    return cudaErrorNotSupported;
+  FwdParams p = p_in;
+  p.v_tile = VT;
+  p.n_vtiles = VD / VT;
+  const int n_chunks = (p.T + C - 1) / C;
+  unsigned char *items = static_cast<unsigned char *>(workspace) + WS_ITEMS_OFF;
+  const uint64_t rows = (uint64_t)p.B * p.T;
+  CUtensorMap mq, mk, mg, mv;
+  if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, KD) ||
+      !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, KD) ||
+      !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, KD) ||
+      !make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * VD, rows, VD))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_ALLOC);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fwd_rec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)R_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long sms = num_sms();
+  const long n_items = (long)p.B * n_chunks * p.H;
+  const int g1 = (int)(n_items < sms ? n_items : sms);
+  fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, n_chunks, mq, mk, mg, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long n_units = (long)p.B * p.H * p.n_vtiles;
+  const int g2 = (int)(n_units < sms ? n_units : sms);
+  fwd_rec_kernel<<<g2 > 0 ? g2 : 1, RT, R_ALLOC, stream>>>(p, items, n_chunks);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -40,9 +40,11 @@
 #include <mutex>
 
 #include "kda_internal.cuh"
+#include "kda_tc_common.cuh"
 
 namespace kda {
 namespace {
+using namespace tc;
 
 constexpr int kThreads = 256;
 constexpr int C = kChunk;  // 64
@@ -70,7 +72,7 @@ constexpr uint32_t ABORT_OFF = TMEMSLOT_OFF + 4;  // u32 abort flag
 constexpr uint32_t SMEM_BYTES = ABORT_OFF + 12;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for alignment
 // Reused after the intra-chunk MMAs are done with X and Y:
-constexpr int LDF = C + 1;                        // padded fp32 row stride
+constexpr int LDF = C + 4;                        // padded fp32 row stride
 constexpr uint32_t AKK_OFF = X_OFF;               // fp32 64 x 65: beta A_kk
 constexpr uint32_t TF_OFF = AKK_OFF + 64 * LDF * 4;  // fp32 64 x 65: T
 constexpr uint32_t TAQ_OFF = TF_OFF + 64 * LDF * 4;  // [T ; A_qk]: 128 x Kd 64
@@ -94,189 +96,6 @@ constexpr uint32_t TMEM_COLS = 512;
 static_assert(TM_D2 + 32 <= TMEM_COLS, "TMEM map fits");
 __device__ __forceinline__ uint32_t tm_a(int b) {
   return b == 0 ? TM_A0 : b == 1 ? TM_A1 : b == 2 ? TM_A2 : TM_A3;
-}
-
-// Byte offset of element (row, k) in a K-major no-swizzle operand with Kd
-// columns: 8x8 core matrices of 16-byte rows; core matrices along K are 128
-// bytes apart (LBO), groups of 8 rows are Kd*16 bytes apart (SBO).
-__device__ __forceinline__ uint32_t op_off(int row, int k, int Kd) {
-  return (uint32_t)((row & 7) * 16 + (row >> 3) * (Kd * 16) + (k >> 3) * 128 +
-                    (k & 7) * 2);
-}
-
-// ---- PTX wrappers -----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                   bar),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: gives up after about one second of SM clock.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (2ll << 30)) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
-                                            int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-  asm volatile(
-      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-          slot),
-      "r"(ncols)
-      : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
-                   : "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(
-                   taddr),
-               "r"(ncols)
-               : "memory");
-}
-
-// Shared-memory matrix descriptor: start address, LBO = 128 B (next core
-// matrix along K), SBO (next group of 8 rows), fixed field 0b001 at bit 46,
-// no swizzle, base offset 0.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
-  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                         uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accum)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
-          "r"(bar)
-      : "memory");
-}
-
-// D (M = 128) += A (128 x Kd) * B (N x Kd)^T, Kd / 16 instructions.
-__device__ __forceinline__ void mma_group(uint32_t d_tmem, uint32_t a_addr,
-                                          uint32_t b_addr, int Kd, int N,
-                                          bool accumulate) {
-  const uint32_t id = idesc_bf16(128, N);
-  const uint32_t sbo = (uint32_t)Kd * 16u;
-  for (int s = 0; s < Kd / 16; ++s) {
-    mma_bf16(d_tmem, smem_desc(a_addr + 256u * s, sbo),
-             smem_desc(b_addr + 256u * s, sbo), id,
-             (accumulate || s > 0) ? 1u : 0u);
-  }
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void st_bf16x8(unsigned char *smem, uint32_t off,
-                                          const float (&v)[8]) {
-  uint4 w;
-  w.x = pack_bf16(v[0], v[1]);
-  w.y = pack_bf16(v[2], v[3]);
-  w.z = pack_bf16(v[4], v[5]);
-  w.w = pack_bf16(v[6], v[7]);
-  *reinterpret_cast<uint4 *>(smem + off) = w;
-}
-
-__device__ __forceinline__ void st_bf16(unsigned char *smem, uint32_t off,
-                                        float v) {
-  *reinterpret_cast<__nv_bfloat16 *>(smem + off) = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ void ld_bf16x8(const unsigned char *p, float (&v)[8]) {
-  const uint4 w = *reinterpret_cast<const uint4 *>(p);
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&u[i]);
-    v[2 * i] = __low2float(h);
-    v[2 * i + 1] = __high2float(h);
-  }
 }
 
 // Which 16-column pieces of the intra-chunk products each TMEM lane quadrant
@@ -346,18 +165,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t n_units = total_units(p.runs, p.B, H, p.n_vtiles);
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
     const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
-    const int v0 = u.vt * VT;
+    const int vc0 = u.vt * VT;  // first value column of this unit
 
-    // ---- state entering the run; S^T operand ----
+    // ---- state entering the run; S^T operand (MN-major: v contiguous) ----
     if (tid < 128) {
       const int c = tid;
+      if (u.first && p.initial_state) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.initial_state + (((size_t)u.b * H + u.h) * KD + c) * p.V + vc0);
 #pragma unroll
-      for (int i = 0; i < VT; ++i) {
-        float s = 0.f;
-        if (u.first && p.initial_state)
-          s = p.initial_state[(((size_t)u.b * H + u.h) * KD + c) * p.V + v0 + i];
-        S[i] = s;
-        st_bf16(smem, ST_OFF + op_off(i, c, KD), s);
+        for (int q4 = 0; q4 < VT / 4; ++q4) {
+          const float4 x = src[q4];
+          S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < VT; ++i) S[i] = 0.f;
+      }
+#pragma unroll
+      for (int vg = 0; vg < VT / 8; ++vg) {
+        float t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
+        st_bf16x8(smem, ST_OFF + mn_off(8 * vg, c, KD), t8);
       }
     }
     float beta_next = 0.f;
@@ -372,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sb + RAW_Q, &tm_q, u.h * KD, y, tma_bar);
       tma_load_2d(sb + RAW_K, &tm_k, u.h * KD, y, tma_bar);
       tma_load_2d(sb + RAW_G, &tm_g, u.h * KD, y, tma_bar);
-      tma_load_2d(sb + RAW_V, &tm_v, u.h * p.V + v0, y, tma_bar);
+      tma_load_2d(sb + RAW_V, &tm_v, u.h * p.V + vc0, y, tma_bar);
     }
     tma_inflight = true;
     tma_pending = tma_phase;
@@ -389,113 +219,121 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (*sAbort) goto done;
 
-      // ---- P0: gate cumsum per channel, block decays ----
-      if (tid < 128) {
-        const int c = tid;
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-          acc += r < n ? sG[r * KD + c] : 0.f;
-          sG[r * KD + c] = acc;
-        }
-        float prev = 0.f;
+      // ---- P0: gate cumsum per channel (two halves of 32 rows), block decays ----
+      {
+        const int c = tid & 127, hf = tid >> 7;
+        float v[32];
 #pragma unroll
-        for (int b = 0; b < kNumSub; ++b) {
-          const float e = sG[(b * kSub + kSub - 1) * KD + c];
-          sDblk[b * KD + c] = __expf(e - prev);
-          prev = e;
+        for (int i = 0; i < 32; ++i) {
+          const int r = 32 * hf + i;
+          v[i] = r < n ? sG[r * KD + c] : 0.f;
+        }
+#pragma unroll
+        for (int i = 1; i < 32; ++i) v[i] += v[i - 1];
+        sDblk[(2 * hf) * KD + c] = ex2(v[15] * kLog2e);
+        sDblk[(2 * hf + 1) * KD + c] = ex2((v[31] - v[15]) * kLog2e);
+        if (hf == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sG[i * KD + c] = v[i];
+        }
+        __syncthreads();
+        if (hf == 1) {
+          const float base = sG[31 * KD + c];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sG[(32 + i) * KD + c] = v[i] + base;
         }
       }
       __syncthreads();
 
       // ---- P1: decay factors and bf16 MMA operands ----
+      // Thread -> 8 channels (cg) x 4 rows, one row per 16-row block; a warp
+      // covers 8 consecutive rows x 4 channel groups (conflict-free stores).
       {
-        const int rg = tid >> 4, cg = tid & 15;
-        const int r0 = rg * 4, c0c = cg * 8, b = rg >> 2;
-        float P[8], E[8], pre[8], suf[8], invD[8], cr1[8], cr2[8], cr3[8];
+        const int rl = tid & 7, cg = (tid >> 3) & 15, hi = tid >> 7;
+        const int cc0 = cg * 8;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = c0c + j;
-          P[j] = b > 0 ? sG[(b * kSub - 1) * KD + c] : 0.f;
-          E[j] = sG[(b * kSub + kSub - 1) * KD + c];
-          // pre = prod_{i<b} D_i, suf = prod_{i>b} D_i, Db = D_b, and the
-          // cross factors e^{P_b' - E_b} = prod_{i=b+1}^{b'-1} D_i for
-          // b' = b+1 (1), b+2 (D_{b+1}), b+3 (D_{b+1} D_{b+2}).
-          float a = 1.f, z = 1.f, Db = 1.f, x2 = 1.f, x3 = 1.f;
-#pragma unroll
-          for (int i = 0; i < kNumSub; ++i) {
-            const float Di = sDblk[i * KD + c];
-            if (i < b) a *= Di;
-            if (i > b) z *= Di;
-            if (i == b) Db = Di;
-            if (i == b + 1) { x2 *= Di; x3 *= Di; }
-            if (i == b + 2) x3 *= Di;
-          }
-          pre[j] = a;
-          suf[j] = z;
-          invD[j] = 1.f / Db;
-          cr1[j] = 1.f;
-          cr2[j] = x2;
-          cr3[j] = x3;
-        }
-        float kbT[8][4], khT[8][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = r0 + i;
+        for (int b = 0; b < kNumSub; ++b) {  // the thread's row in block b
+          const int r = kSub * b + 8 * hi + rl;
           const bool valid = r < n;
           const float br = sBeta[r];
-          float kk[8], qq[8];
-          ld_bf16x8(smem + RAW_K + r * 256 + c0c * 2, kk);
-          ld_bf16x8(smem + RAW_Q + r * 256 + c0c * 2, qq);
-          float xk[8], xq[8], qt[8], yd[8], y1[8], y2[8], y3[8];
+          // block decays of the 8 channels and G at the block boundaries
+          float D[kNumSub][8], Pb[8], Eb[8];
+#pragma unroll
+          for (int i = 0; i < kNumSub; ++i) {
+            const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
+            const float4 d0 = dp[0], d1 = dp[1];
+            D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
+            D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
+          }
+          {
+            const float4 *ep = reinterpret_cast<const float4 *>(sG + (b * kSub + kSub - 1) * KD + cc0);
+            const float4 e0 = ep[0], e1v = ep[1];
+            Eb[0] = e0.x; Eb[1] = e0.y; Eb[2] = e0.z; Eb[3] = e0.w;
+            Eb[4] = e1v.x; Eb[5] = e1v.y; Eb[6] = e1v.z; Eb[7] = e1v.w;
+            if (b > 0) {
+              const float4 *pp = reinterpret_cast<const float4 *>(sG + (b * kSub - 1) * KD + cc0);
+              const float4 p0 = pp[0], p1 = pp[1];
+              Pb[0] = p0.x; Pb[1] = p0.y; Pb[2] = p0.z; Pb[3] = p0.w;
+              Pb[4] = p1.x; Pb[5] = p1.y; Pb[6] = p1.z; Pb[7] = p1.w;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) Pb[j] = 0.f;
+            }
+          }
+          float kk[8], qq[8], G[8];
+          ld_bf16x8(smem + RAW_K + r * 256 + cc0 * 2, kk);
+          ld_bf16x8(smem + RAW_Q + r * 256 + cc0 * 2, qq);
+          {
+            const float4 *gp = reinterpret_cast<const float4 *>(sG + r * KD + cc0);
+            const float4 g0 = gp[0], g1 = gp[1];
+            G[0] = g0.x; G[1] = g0.y; G[2] = g0.z; G[3] = g0.w;
+            G[4] = g1.x; G[5] = g1.y; G[6] = g1.z; G[7] = g1.w;
+          }
+          float xk[8], xq[8], qt[8], kb[8], kh[8], yd[8], y1[8], y2[8], y3[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
+            float pre = 1.f, suf = 1.f;
+#pragma unroll
+            for (int i = 0; i < kNumSub; ++i) {
+              if (i < b) pre *= D[i][j];
+              if (i > b) suf *= D[i][j];
+            }
+            const float Pl = Pb[j] * kLog2e;
+            const float El = Eb[j] * kLog2e;
+            const float gl = G[j] * kLog2e;
+            const float e1 = ex2(gl - Pl);   // e^{G - P_b}
+            const float e2 = ex2(El - gl);   // e^{E_b - G}
             const float kv = valid ? kk[j] : 0.f;
             const float qv = valid ? qq[j] : 0.f;
-            const float G = sG[r * KD + c0c + j];
-            const float e1 = __expf(G - P[j]);
-            const float e2 = __expf(E[j] - G);
             xk[j] = kv * e1;
             xq[j] = qv * e1;
-            qt[j] = xq[j] * pre[j];
-            kbT[j][i] = br * xk[j] * pre[j];
+            qt[j] = xq[j] * pre;
+            kb[j] = xk[j] * (br * pre);
             const float ke2 = kv * e2;
-            khT[j][i] = ke2 * suf[j];
-            yd[j] = ke2 * invD[j];
-            y1[j] = ke2 * cr1[j];
-            y2[j] = ke2 * cr2[j];
-            y3[j] = ke2 * cr3[j];
+            kh[j] = ke2 * suf;
+            yd[j] = ke2 * __frcp_rn(D[b][j]);
+            y1[j] = ke2;
+            y2[j] = b + 2 < kNumSub ? ke2 * D[b + 2 < kNumSub ? b + 1 : 0][j] : 0.f;
+            y3[j] = b + 3 < kNumSub ? y2[j] * D[b + 3 < kNumSub ? b + 2 : 0][j] : 0.f;
           }
-          st_bf16x8(smem, X_OFF + op_off(r, c0c, KD), xk);
-          st_bf16x8(smem, X_OFF + op_off(64 + r, c0c, KD), xq);
-          st_bf16x8(smem, WQ_OFF + op_off(64 + r, c0c, KD), qt);
-          st_bf16x8(smem, y_off(b) + op_off(r, c0c, KD), yd);
-          if (b + 1 < kNumSub) st_bf16x8(smem, y_off(b + 1) + op_off(r, c0c, KD), y1);
-          if (b + 2 < kNumSub) st_bf16x8(smem, y_off(b + 2) + op_off(r, c0c, KD), y2);
-          if (b + 3 < kNumSub) st_bf16x8(smem, y_off(b + 3) + op_off(r, c0c, KD), y3);
+          st_bf16x8(smem, X_OFF + op_off(r, cc0, KD), xk);
+          st_bf16x8(smem, X_OFF + op_off(64 + r, cc0, KD), xq);
+          st_bf16x8(smem, WQ_OFF + op_off(64 + r, cc0, KD), qt);
+          st_bf16x8(smem, y_off(b) + op_off(r, cc0, KD), yd);
+          if (b + 1 < kNumSub) st_bf16x8(smem, y_off(b + 1) + op_off(r, cc0, KD), y1);
+          if (b + 2 < kNumSub) st_bf16x8(smem, y_off(b + 2) + op_off(r, cc0, KD), y2);
+          if (b + 3 < kNumSub) st_bf16x8(smem, y_off(b + 3) + op_off(r, cc0, KD), y3);
+          st_bf16x8(smem, KHT_OFF + mn_off(cc0, r, C), kh);   // (K e^{G_C-G})^T
+          st_bf16x8(smem, RHST_OFF + mn_off(cc0, r, C), kb);  // (beta K e^G)^T
         }
+        {  // (beta V)^T: thread -> row r, 8 value columns
+          const int r = tid >> 2, vg = tid & 3;
+          float vv[8];
+          ld_bf16x8(smem + RAW_V + r * 64 + vg * 16, vv);
+          const float br = r < n ? sBeta[r] : 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = c0c + j;
-          uint2 w;
-          w.x = pack_bf16(kbT[j][0], kbT[j][1]);
-          w.y = pack_bf16(kbT[j][2], kbT[j][3]);
-          *reinterpret_cast<uint2 *>(smem + RHST_OFF + op_off(c, r0, C)) = w;
-          w.x = pack_bf16(khT[j][0], khT[j][1]);
-          w.y = pack_bf16(khT[j][2], khT[j][3]);
-          *reinterpret_cast<uint2 *>(smem + KHT_OFF + op_off(c, r0, C)) = w;
-        }
-        // beta V^T rows 128..159 of the TX B operand
-        {
-          const int v = tid & 31, rr0 = (tid >> 5) * 8;
-          float vals[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = rr0 + i;
-            const float vv = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16 *>(smem + RAW_V + r * 64 + v * 2));
-            vals[i] = r < n ? sBeta[r] * vv : 0.f;
-          }
-          st_bf16x8(smem, RHST_OFF + op_off(128 + v, rr0, C), vals);
+          for (int i = 0; i < 8; ++i) vv[i] *= br;
+          st_bf16x8(smem, RHST_OFF + mn_off(KD + 8 * vg, r, C), vv);
         }
       }
       fence_proxy_async();
@@ -507,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int b = 0; b < kNumSub; ++b)
-          mma_group(tmem + tm_a(b), sb + X_OFF, sb + y_off(b), KD, 16 * (b + 1), false);
+          mma_group(tmem + tm_a(b), sb + X_OFF, sb + y_off(b), KD, 16 * (b + 1), false, 0, 0);
         mma_commit(mma_bar);
         if (has_next) {
           const int y = (int)(tok0 + C);
@@ -515,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sb + RAW_Q, &tm_q, u.h * KD, y, tma_bar);
           tma_load_2d(sb + RAW_K, &tm_k, u.h * KD, y, tma_bar);
           tma_load_2d(sb + RAW_G, &tm_g, u.h * KD, y, tma_bar);
-          tma_load_2d(sb + RAW_V, &tm_v, u.h * p.V + v0, y, tma_bar);
+          tma_load_2d(sb + RAW_V, &tm_v, u.h * p.V + vc0, y, tma_bar);
         }
       }
       if (has_next) {
@@ -542,28 +380,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool is_q = L >= 64;
         const int bme = r >> 4;
         const int np = piece_count(quad);
-        for (int pi = half; pi < np; pi += 2) {
-          int bb, pp;
-          piece(quad, pi, bb, pp);
-          float v[16];
-          tmem_ld16(tq + tm_a(bb) + 16 * pp, v);
-          if (bb == bme) {
+        for (int pi = half; pi < np; pi += 4) {
+          float v[2][16];
+          int bb[2], pp[2];
+          piece(quad, pi, bb[0], pp[0]);
+          const bool two = pi + 2 < np;
+          if (two) {
+            piece(quad, pi + 2, bb[1], pp[1]);
+            tmem_ld16x2(tq + tm_a(bb[0]) + 16 * pp[0], tq + tm_a(bb[1]) + 16 * pp[1], v[0], v[1]);
+          } else {
+            bb[1] = -1;
+            pp[1] = 0;
+            tmem_ld16(tq + tm_a(bb[0]) + 16 * pp[0], v[0]);
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (bb[e] != bme) continue;
+            const int j0 = 16 * pp[e];
             if (!is_q) {
               const float br = sBeta[r];
+              float4 *dst = reinterpret_cast<float4 *>(sAkk + r * LDF + j0);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int j = 16 * pp + i;
-                sAkk[r * LDF + j] = j < r ? br * v[i] : 0.f;
+              for (int q4 = 0; q4 < 4; ++q4) {
+                float a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  a[i] = (j0 + 4 * q4 + i < r) ? br * v[e][4 * q4 + i] : 0.f;
+                dst[q4] = make_float4(a[0], a[1], a[2], a[3]);
               }
             } else {
               float a0[8], a1[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                a0[i] = (16 * pp + i <= r) ? v[i] : 0.f;
-                a1[i] = (16 * pp + 8 + i <= r) ? v[8 + i] : 0.f;
+                a0[i] = (j0 + i <= r) ? v[e][i] : 0.f;
+                a1[i] = (j0 + 8 + i <= r) ? v[e][8 + i] : 0.f;
               }
-              st_bf16x8(smem, TAQ_OFF + op_off(64 + r, 16 * pp, C), a0);
-              st_bf16x8(smem, TAQ_OFF + op_off(64 + r, 16 * pp + 8, C), a1);
+              st_bf16x8(smem, TAQ_OFF + op_off(64 + r, j0, C), a0);
+              st_bf16x8(smem, TAQ_OFF + op_off(64 + r, j0 + 8, C), a1);
             }
           }
         }
@@ -577,55 +430,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
 
       // ---- P4: T = (I + L)^-1, blocked, fp32 ----
-      if (tid < 64) {  // diagonal 16 x 16 blocks by forward substitution
+      if (tid < 64) {  // diagonal 16 x 16 blocks: right-looking substitution
         const int i = tid >> 4, cc = tid & 15, base = 16 * i;
         float x[16];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          float acc = rr == cc ? 1.f : 0.f;
+        for (int rr = 0; rr < 16; ++rr) x[rr] = rr == cc ? 1.f : 0.f;
 #pragma unroll
-          for (int m = 0; m < rr; ++m)
-            acc = fmaf(-sAkk[(base + rr) * LDF + base + m], x[m], acc);
-          x[rr] = rr < cc ? 0.f : acc;
-          sT[(base + rr) * LDF + base + cc] = x[rr];
+        for (int m = 0; m < 15; ++m) {
+          const float xm = x[m];
+#pragma unroll
+          for (int rr = m + 1; rr < 16; ++rr)
+            x[rr] = fmaf(-sAkk[(base + rr) * LDF + base + m], xm, x[rr]);
         }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) sT[(base + rr) * LDF + base + cc] = x[rr];
       }
       __syncthreads();
       for (int d = 1; d < kNumSub; ++d) {
+        // Blocks (i, j = i - d): M = sum_{m=j}^{i-1} L_im T_mj, then
+        // T_ij = -T_ii M.  64 threads per block, 2 x 2 outputs each.
         const int nblk = kNumSub - d;
-        // M_ij = sum_{m=j}^{i-1} L_im T_mj for blocks (i, j = i - d)
-        for (int o = tid; o < nblk * 256; o += kThreads) {
-          const int blk = o >> 8, e = o & 255, rr = e >> 4, cc = e & 15;
-          const int i = d + blk, j = blk;
-          float acc = 0.f;
-          for (int m = j; m < i; ++m)
+        const int blk = tid >> 6, e = tid & 63, ra = 2 * (e >> 3), cb = 2 * (e & 7);
+        const bool act = blk < nblk;
+        const int i = d + blk, j = blk;
+        if (act) {
+          float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+          for (int m = j; m < i; ++m) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              acc = fmaf(sAkk[(16 * i + rr) * LDF + 16 * m + t],
-                         sT[(16 * m + t) * LDF + 16 * j + cc], acc);
-          sScr[o] = acc;
+            for (int t = 0; t < 16; ++t) {
+              const float l0 = sAkk[(16 * i + ra) * LDF + 16 * m + t];
+              const float l1 = sAkk[(16 * i + ra + 1) * LDF + 16 * m + t];
+              const float2 tv = *reinterpret_cast<const float2 *>(
+                  sT + (16 * m + t) * LDF + 16 * j + cb);
+              a00 = fmaf(l0, tv.x, a00); a01 = fmaf(l0, tv.y, a01);
+              a10 = fmaf(l1, tv.x, a10); a11 = fmaf(l1, tv.y, a11);
+            }
+          }
+          float *mm = sScr + blk * 256;
+          *reinterpret_cast<float2 *>(mm + ra * 16 + cb) = make_float2(a00, a01);
+          *reinterpret_cast<float2 *>(mm + (ra + 1) * 16 + cb) = make_float2(a10, a11);
         }
         __syncthreads();
-        // T_ij = -T_ii M_ij
-        for (int o = tid; o < nblk * 256; o += kThreads) {
-          const int blk = o >> 8, e = o & 255, rr = e >> 4, cc = e & 15;
-          const int i = d + blk, j = blk;
-          float acc = 0.f;
+        if (act) {
+          const float *mm = sScr + blk * 256;
+          float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            acc = fmaf(sT[(16 * i + rr) * LDF + 16 * i + t], sScr[(blk << 8) + t * 16 + cc], acc);
-          sT[(16 * i + rr) * LDF + 16 * j + cc] = -acc;
+          for (int t = 0; t < 16; ++t) {
+            const float d0 = sT[(16 * i + ra) * LDF + 16 * i + t];
+            const float d1 = sT[(16 * i + ra + 1) * LDF + 16 * i + t];
+            const float2 mv = *reinterpret_cast<const float2 *>(mm + t * 16 + cb);
+            a00 = fmaf(d0, mv.x, a00); a01 = fmaf(d0, mv.y, a01);
+            a10 = fmaf(d1, mv.x, a10); a11 = fmaf(d1, mv.y, a11);
+          }
+          *reinterpret_cast<float2 *>(sT + (16 * i + ra) * LDF + 16 * j + cb) = make_float2(-a00, -a01);
+          *reinterpret_cast<float2 *>(sT + (16 * i + ra + 1) * LDF + 16 * j + cb) = make_float2(-a10, -a11);
         }
         __syncthreads();
       }
       {  // T -> bf16 rows 0..63 of [T ; A_qk]
         const int r = tid >> 2, jq = (tid & 3) * 16;
+        const float4 *src = reinterpret_cast<const float4 *>(sT + r * LDF + jq);
         float t0[8], t1[8];
+        const bool zero = (jq >> 4) > (r >> 4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int j0 = jq + i, j1 = jq + 8 + i;
-          t0[i] = (j0 >> 4) > (r >> 4) ? 0.f : sT[r * LDF + j0];
-          t1[i] = (j1 >> 4) > (r >> 4) ? 0.f : sT[r * LDF + j1];
+        for (int q4 = 0; q4 < 2; ++q4) {
+          const float4 a = src[q4], b4 = src[2 + q4];
+          t0[4 * q4] = a.x; t0[4 * q4 + 1] = a.y; t0[4 * q4 + 2] = a.z; t0[4 * q4 + 3] = a.w;
+          t1[4 * q4] = b4.x; t1[4 * q4 + 1] = b4.y; t1[4 * q4 + 2] = b4.z; t1[4 * q4 + 3] = b4.w;
+        }
+        if (zero) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t0[i] = t1[i] = 0.f;
         }
         st_bf16x8(smem, TAQ_OFF + op_off(r, jq, C), t0);
         st_bf16x8(smem, TAQ_OFF + op_off(r, jq + 8, C), t1);
@@ -637,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P5: [w | u] = T [beta K e^G | beta V] ----
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + TM_TX, sb + TAQ_OFF, sb + RHST_OFF, C, KD + VT, false);
+        mma_group(tmem + TM_TX, sb + TAQ_OFF, sb + RHST_OFF, C, KD + VT, false, 0, 1);
         mma_commit(mma_bar);
       }
       mma_inflight = true;
@@ -651,25 +526,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quad < 2) {  // TMEM lanes 0..63 = chunk rows
         const int r = L;
         if (half == 0) {
-          float v[16];
-          tmem_ld16(tq + TM_TX + KD, v);
+          float v0[16], v1[16];
+          tmem_ld16x2(tq + TM_TX + KD, tq + TM_TX + KD + 16, v0, v1);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) u_reg[i] = v[i];
-          tmem_ld16(tq + TM_TX + KD + 16, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) u_reg[16 + i] = v[i];
-        }
-        for (int pc = half * 4; pc < half * 4 + 4; ++pc) {
-          float v[16];
-          tmem_ld16(tq + TM_TX + 16 * pc, v);
-          float a0[8], a1[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            a0[i] = v[i];
-            a1[i] = v[8 + i];
+          for (int i = 0; i < 16; ++i) {
+            u_reg[i] = v0[i];
+            u_reg[16 + i] = v1[i];
           }
-          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * pc, KD), a0);
-          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * pc + 8, KD), a1);
+        }
+#pragma unroll
+        for (int pc = 0; pc < 4; pc += 2) {
+          const int c16 = half * 4 + pc;
+          float v0[16], v1[16];
+          tmem_ld16x2(tq + TM_TX + 16 * c16, tq + TM_TX + 16 * (c16 + 1), v0, v1);
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = v0[i];
+          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * c16, KD), a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = v0[8 + i];
+          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * c16 + 8, KD), a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = v1[i];
+          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * c16 + 16, KD), a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = v1[8 + i];
+          st_bf16x8(smem, WQ_OFF + op_off(r, 16 * c16 + 24, KD), a);
         }
       }
       fence_proxy_async();
@@ -679,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P6: D1 = [w ; Q e^G] S0 ----
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + TM_D1, sb + WQ_OFF, sb + ST_OFF, KD, VT, false);
+        mma_group(tmem + TM_D1, sb + WQ_OFF, sb + ST_OFF, KD, VT, false, 0, 1);
         mma_commit(mma_bar);
       }
       mma_inflight = true;
@@ -691,16 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // ---- P7: U = u - w S0 -> U^T (bf16) ----
+      // ---- P7: U = u - w S0 -> U^T (bf16, MN-major) ----
       if (quad < 2 && half == 0) {
         const int r = L;
+        float v0[16], v1[16];
+        tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
 #pragma unroll
-        for (int h16 = 0; h16 < 2; ++h16) {
-          float v[16];
-          tmem_ld16(tq + TM_D1 + 16 * h16, v);
+        for (int vg = 0; vg < VT / 8; ++vg) {
+          float a[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            st_bf16(smem, UT_OFF + op_off(16 * h16 + i, r, C), u_reg[16 * h16 + i] - v[i]);
+          for (int i = 0; i < 8; ++i) {
+            const int col = 8 * vg + i;
+            a[i] = u_reg[col] - (col < 16 ? v0[col & 15] : v1[col & 15]);
+          }
+          st_bf16x8(smem, UT_OFF + mn_off(8 * vg, r, C), a);
         }
       }
       fence_proxy_async();
@@ -710,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P8: D1 += [T ; A_qk] U ; D2 = (K e^{G_C-G})^T U ----
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + TM_D1, sb + TAQ_OFF, sb + UT_OFF, C, VT, true);
-        mma_group(tmem + TM_D2, sb + KHT_OFF, sb + UT_OFF, C, VT, false);
+        mma_group(tmem + TM_D1, sb + TAQ_OFF, sb + UT_OFF, C, VT, true, 0, 1);
+        mma_group(tmem + TM_D2, sb + KHT_OFF, sb + UT_OFF, C, VT, false, 1, 1);
         mma_commit(mma_bar);
       }
       mma_inflight = true;
@@ -727,24 +613,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (half == 0) {
         if (quad >= 2) {
           const int r = L - 64;
-          float o[VT];
-#pragma unroll
-          for (int h16 = 0; h16 < 2; ++h16) {
-            float v[16];
-            tmem_ld16(tq + TM_D1 + 16 * h16, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[16 * h16 + i] = p.scale * v[i];
-          }
+          float v0[16], v1[16];
+          tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
           if (r < n) {
             uint4 *dst = reinterpret_cast<uint4 *>(
-                static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + u.h) * p.V + v0);
+                static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + u.h) * p.V + vc0);
 #pragma unroll
             for (int q4 = 0; q4 < VT / 8; ++q4) {
+              float o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int col = 8 * q4 + i;
+                o[i] = p.scale * (col < 16 ? v0[col & 15] : v1[col & 15]);
+              }
               uint4 w;
-              w.x = pack_bf16(o[8 * q4 + 0], o[8 * q4 + 1]);
-              w.y = pack_bf16(o[8 * q4 + 2], o[8 * q4 + 3]);
-              w.z = pack_bf16(o[8 * q4 + 4], o[8 * q4 + 5]);
-              w.w = pack_bf16(o[8 * q4 + 6], o[8 * q4 + 7]);
+              w.x = pack_bf16(o[0], o[1]);
+              w.y = pack_bf16(o[2], o[3]);
+              w.z = pack_bf16(o[4], o[5]);
+              w.w = pack_bf16(o[6], o[7]);
               dst[q4] = w;
             }
           }
@@ -754,16 +640,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           float gam = 1.f;
 #pragma unroll
           for (int i = 0; i < kNumSub; ++i) gam *= sDblk[i * KD + c];
+          float v0[16], v1[16];
+          tmem_ld16x2(tq + TM_D2, tq + TM_D2 + 16, v0, v1);
 #pragma unroll
-          for (int h16 = 0; h16 < 2; ++h16) {
-            float v[16];
-            tmem_ld16(tq + TM_D2 + 16 * h16, v);
+          for (int i = 0; i < 16; ++i) {
+            S[i] = fmaf(gam, S[i], v0[i]);
+            S[16 + i] = fmaf(gam, S[16 + i], v1[i]);
+          }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float s = fmaf(gam, S[16 * h16 + i], v[i]);
-              S[16 * h16 + i] = s;
-              st_bf16(smem, ST_OFF + op_off(16 * h16 + i, c, KD), s);
-            }
+          for (int vg = 0; vg < VT / 8; ++vg) {
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
+            st_bf16x8(smem, ST_OFF + mn_off(8 * vg, c, KD), t8);
           }
         }
       }
@@ -774,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (u.last && p.final_state && tid < 128) {
       float4 *dst = reinterpret_cast<float4 *>(
-          p.final_state + (((size_t)u.b * H + u.h) * KD + tid) * p.V + v0);
+          p.final_state + (((size_t)u.b * H + u.h) * KD + tid) * p.V + vc0);
 #pragma unroll
       for (int q4 = 0; q4 < VT / 4; ++q4)
         dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);

@@ -84,6 +84,12 @@ cudaError_t launch_fwd_simt(const FwdParams &p, bool bf16, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);
 bool fwd_tc_supported(int K, int V, bool bf16, int v_tile);
 
+// Split tensor-core path (parallel prep kernel + recurrence kernel), bf16,
+// K = V = 128, no segment ids; needs split_workspace_bytes() of workspace.
+size_t split_workspace_bytes(int B, int T, int H);
+bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile);
+cudaError_t launch_fwd_split(const FwdParams &p, void *workspace, cudaStream_t stream);
+
 cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
                               cudaStream_t stream);
 

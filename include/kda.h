@@ -79,9 +79,14 @@ typedef struct kda_shape {
 
 /* Implementation choice for kda_chunk_fwd_ex. */
 typedef enum kda_impl {
-  KDA_IMPL_AUTO = 0, /* tensor-core kernel where it applies, else SIMT      */
-  KDA_IMPL_SIMT = 1, /* fp32 CUDA-core kernel (every supported shape)       */
-  KDA_IMPL_TC = 2    /* tcgen05 / TMA kernel: bf16, K = V = 128             */
+  KDA_IMPL_AUTO = 0,  /* fastest that applies: SPLIT when the workspace is
+                         large enough, else TC, else SIMT                   */
+  KDA_IMPL_SIMT = 1,  /* fp32 CUDA-core kernel (every supported shape)      */
+  KDA_IMPL_TC = 2,    /* fused tcgen05 / TMA kernel: bf16, K = V = 128      */
+  KDA_IMPL_SPLIT = 3  /* tcgen05 in two kernels (parallel per-chunk prep,
+                         then the state recurrence): bf16, K = V = 128, no
+                         segment ids; needs the larger workspace reported by
+                         kda_chunk_fwd_workspace_size_for(.., KDA_IMPL_SPLIT) */
 } kda_impl;
 
 /* Device status bits OR-ed into the workspace status word. */
@@ -97,6 +102,17 @@ typedef enum kda_impl {
  * Returns 0 when `s` is NULL or invalid.
  */
 KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids);
+
+/*
+ * Workspace bytes implementation `impl` needs (same zero-fill rule).  For
+ * KDA_IMPL_SPLIT this holds the per-chunk operands the recurrence kernel
+ * reads: about 97 KB per (row, 64-token chunk, head).  For KDA_IMPL_AUTO it
+ * is the size that lets AUTO pick its fastest kernel for the shape.
+ * Returns 0 when the shape or the choice is invalid or does not apply.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size_for(const kda_shape *s,
+                                                int has_segment_ids,
+                                                kda_impl impl);
 
 /*
  * Chunked KDA forward (the operation above).

@@ -61,7 +61,23 @@ def assert_parity(got, ref, bf16, what):
     return mx, rel
 
 
+def skip_unless_supported(w, impl):
+    """Skip a test whose implementation does not serve the shape (the ABI
+    rejects it with KDA_ERR_UNSUPPORTED, which test_abi covers)."""
+    import pytest
+    import gated_delta_rule_21_gb300 as kda
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    if impl == "split":
+        ok = kda.workspace_size(w.B, w.T, w.H, w.K, w.V, dt, w.segments is not None,
+                                impl="split") > 0
+    else:
+        ok = kda.impl_available(impl, w.B, w.T, w.H, w.K, w.V, dt)
+    if not ok:
+        pytest.skip(f"{impl} does not serve {w.name}")
+
+
 def check_workload(w, seed=0, impl="auto", v_tile=0):
+    skip_unless_supported(w, impl)
     x = ki.make_inputs(w, seed=seed)
     o, fs = run_gpu(x, impl=impl, v_tile=v_tile)
     o_ref, fs_ref = run_oracle(x)

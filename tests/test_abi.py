@@ -35,7 +35,7 @@ def test_header_declares_expected_entry_points():
     for must in ("kda_chunk_fwd", "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size",
                  "kda_short_conv_silu", "kda_read_device_status",
                  "kda_clear_device_status", "kda_status_string", "kda_version",
-                 "kda_impl_available"):
+                 "kda_impl_available", "kda_chunk_fwd_workspace_size_for"):
         assert must in names
 
 
@@ -116,6 +116,23 @@ def test_impl_available_query(L):
     assert not kda.impl_available("simt", 1, 64, 1, 128, 128, v_tile=48)
     assert not kda.impl_available("tc", 1, 64, 1, 64, 64)
     assert not kda.impl_available("tc", 1, 64, 1, 128, 128, torch.float32)
+
+
+def test_workspace_size_for_each_impl(L):
+    base = kda.workspace_size(1, 8192, 32, 128, 128)
+    split = kda.workspace_size(1, 8192, 32, 128, 128, impl="split")
+    assert split == 1024 + 128 * 32 * 99328          # one 97 KiB item per chunk-head
+    assert kda.workspace_size(1, 8192, 32, 128, 128, impl="auto") == split
+    assert kda.workspace_size(1, 8192, 32, 128, 128, impl="tc") == base
+    assert kda.workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="split") == 0
+    assert kda.workspace_size(1, 100, 2, 64, 64, impl="split") == 0
+    assert kda.workspace_size(1, 100, 2, 128, 128, torch.float32, impl="auto") == \
+        kda.workspace_size(1, 100, 2, 128, 128, torch.float32)
+
+
+def test_split_rejects_small_workspace(L):
+    assert call_fwd(L, impl=3, ws_bytes=4096) == 4
+    assert call_fwd(L, impl=3, seg=FAKE) == 2
 
 
 def test_status_calls_reject_null(L):

@@ -8,11 +8,13 @@ import torch
 
 import kda_inputs as ki
 from kda_testlib import (assert_parity, check_workload, errors, run_gpu, run_oracle,
-                         to_dev)
+                         skip_unless_supported, to_dev)
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["auto", "simt"]   # auto = tensor-core kernel for bf16 K = V = 128
+# auto = the split tensor-core path for bf16 K = V = 128 without segment ids
+# (its workspace is allocated by the binding), the fused one with them.
+IMPLS = ["auto", "tc", "simt"]
 NAMED = ["tiny_fp32_h2_t128_d32", "fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg",
          "fixed_bf16_h32_t8192", "packed_bf16_h32_t8192_25seg"]
 
@@ -59,6 +61,7 @@ EDGE = {
 @pytest.mark.parametrize("case", sorted(EDGE))
 def test_edge_case(case, impl):
     w = ki.custom_workload(name=case, **EDGE[case])
+    skip_unless_supported(w, impl)
     x = ki.make_inputs(w, seed=1)
     if case == "repeated_id_after_pad":
         seg = x["segment_ids"]
