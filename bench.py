@@ -302,8 +302,11 @@ def run_ours(args, dist):
         has_seg = d["segment_ids"] is not None
         o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
         fs = torch.empty(w.B, w.H, w.K, w.V, dtype=torch.float32, device=dev)
+        # packed inputs: the split path's items are sized for the workload's
+        # runs per row (the pages' bound on segments per row)
+        max_runs = len(w.segments) if w.segments is not None else None
         ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg, dev,
-                                 impl=args.kda_impl)
+                                 impl=args.kda_impl, max_runs_per_row=max_runs)
 
         def step():
             kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
@@ -372,7 +375,7 @@ def run_ours(args, dist):
         has_seg = w.segments is not None
         if args.kda_impl in ("simt", "tc", "split"):
             return args.kda_impl
-        if kda.workspace_size(w.B, w.T, w.H, w.K, w.V, dt, has_seg, impl="split") > 0:
+        if kda.impl_available("split", w.B, w.T, w.H, w.K, w.V, dt):
             return "split"
         return "tc" if kda.impl_available("tc", w.B, w.T, w.H, w.K, w.V, dt) else "simt"
 

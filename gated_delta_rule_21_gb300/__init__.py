@@ -71,6 +71,8 @@ def lib():
         L.kda_chunk_fwd_workspace_size.restype = u64
         L.kda_chunk_fwd_workspace_size_for.argtypes = [sp, i, i]
         L.kda_chunk_fwd_workspace_size_for.restype = u64
+        L.kda_chunk_fwd_workspace_size_packed.argtypes = [sp, i]
+        L.kda_chunk_fwd_workspace_size_packed.restype = u64
         L.kda_chunk_fwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp,
                                     vp, vp, u64, vp]
         L.kda_chunk_fwd.restype = i
@@ -124,10 +126,22 @@ def workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
                                                       IMPLS[impl]))
 
 
+def workspace_size_packed(B, T, H, K, V, max_runs_per_row, dtype=torch.bfloat16) -> int:
+    """Split-path workspace for packed inputs with at most ``max_runs_per_row``
+    runs per row."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_workspace_size_packed(ctypes.byref(s), int(max_runs_per_row)))
+
+
 def alloc_workspace(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
-                    device=None, impl=None) -> torch.Tensor:
-    """Zero-filled workspace of the size ``impl`` needs (uint8 device tensor)."""
-    n = workspace_size(B, T, H, K, V, dtype, has_segment_ids, impl)
+                    device=None, impl=None, max_runs_per_row=None) -> torch.Tensor:
+    """Zero-filled workspace of the size ``impl`` needs (uint8 device tensor);
+    with ``max_runs_per_row`` the split path's packed bound is used."""
+    n = 0
+    if max_runs_per_row is not None and has_segment_ids and impl in ("auto", "split"):
+        n = workspace_size_packed(B, T, H, K, V, max_runs_per_row, dtype)
+    if n == 0:
+        n = workspace_size(B, T, H, K, V, dtype, has_segment_ids, impl)
     if n == 0:
         raise KdaError(1, "workspace_size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
@@ -161,13 +175,15 @@ def _check(t, name, shape, dtype, device):
 def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None,
               segment_ids=None, output_final_state=False, out=None,
               final_state_out=None, workspace=None, impl="auto", v_tile=0,
-              stream=None):
+              stream=None, max_runs_per_row=None):
     """Chunked KDA forward on the GPU.
 
     q, k: [B,T,H,K]; v: [B,T,H,V] (bf16 or fp32, same dtype); g: [B,T,H,K]
     fp32 log-decay in [-5, 0]; beta: [B,T,H] fp32; initial_state: [B,H,K,V]
     fp32 or None; segment_ids: [B,T] int32 (1-based, 0 = padding) or None.
-    ``scale`` None means K**-0.5.  Returns ``(o, final_state or None)``.
+    ``scale`` None means K**-0.5.  ``max_runs_per_row`` bounds the runs
+    per row when the workspace is allocated here for packed inputs.
+    Returns ``(o, final_state or None)``.
     """
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -192,7 +208,8 @@ def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None
             B, H, K, V, dtype=torch.float32, device=dev)
         _check(fs, "final_state_out", (B, H, K, V), torch.float32, dev)
     if workspace is None:
-        workspace = alloc_workspace(B, T, H, K, V, dt, segment_ids is not None, dev, impl=impl)
+        workspace = alloc_workspace(B, T, H, K, V, dt, segment_ids is not None, dev, impl=impl,
+                                    max_runs_per_row=max_runs_per_row)
     s = make_shape(B, T, H, K, V, dt)
     st = lib().kda_chunk_fwd_ex(
         ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
@@ -238,7 +255,7 @@ def read_device_status(workspace, stream=None) -> int:
     bits = ctypes.c_uint32(0)
     st = lib().kda_read_device_status(_ptr(workspace), _stream_ptr(stream, workspace.device),
                                       ctypes.byref(bits))
-    if st not in (KDA_OK, 6, 7):
+    if st not in (KDA_OK, 4, 6, 7):
         raise KdaError(st, "kda_read_device_status")
     return int(bits.value)
 

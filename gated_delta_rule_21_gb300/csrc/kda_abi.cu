@@ -40,6 +40,10 @@ kda_status check_shape(const kda_shape *s) {
   return KDA_OK;
 }
 
+// Runs per row the default split workspace is sized for (runs of 64 tokens
+// on average).
+int default_runs_bound(int T) { return (T + kChunk - 1) / kChunk; }
+
 kda_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return KDA_OK;
   if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
@@ -81,17 +85,26 @@ size_t kda_chunk_fwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
   const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
   const size_t base = ws_bytes(s->B, s->T, has_seg);
   const bool split_ok = fwd_split_supported(s->K, s->V, bf16, has_seg, 0);
+  const size_t split = split_ok ? split_workspace_bytes(s->B, s->T, s->H, has_seg,
+                                                        default_runs_bound(s->T))
+                                : 0;
   switch (impl) {
     case KDA_IMPL_SIMT:
       return base;
     case KDA_IMPL_TC:
       return fwd_tc_supported(s->K, s->V, bf16, 0) ? base : 0;
     case KDA_IMPL_SPLIT:
-      return split_ok ? split_workspace_bytes(s->B, s->T, s->H) : 0;
+      return split;
     case KDA_IMPL_AUTO:
-      return split_ok ? split_workspace_bytes(s->B, s->T, s->H) : base;
+      return split_ok ? split : base;
   }
   return 0;
+}
+
+size_t kda_chunk_fwd_workspace_size_packed(const kda_shape *s, int max_runs_per_row) {
+  if (check_shape(s) != KDA_OK || max_runs_per_row < 1) return 0;
+  if (!fwd_split_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16, true, 0)) return 0;
+  return split_workspace_bytes(s->B, s->T, s->H, true, max_runs_per_row);
 }
 
 kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
@@ -123,17 +136,26 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
   const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;
   const bool tc_ok = fwd_tc_supported(s->K, s->V, bf16, v_tile);
   const bool split_ok = fwd_split_supported(s->K, s->V, bf16, has_seg, v_tile);
-  const size_t split_need = split_ok ? split_workspace_bytes(s->B, s->T, s->H) : 0;
+  // AUTO takes the split path when the workspace has the default room; with
+  // segment ids it also enqueues the fused kernel, which runs only when the
+  // runs of this call overflow the split items.  An explicit SPLIT needs
+  // room for ceil(T/64) chunks per row at least and reports an overflow in
+  // the status word.
+  const size_t split_need =
+      split_ok ? split_workspace_bytes(s->B, s->T, s->H, has_seg, default_runs_bound(s->T)) : 0;
+  const size_t split_min = split_ok ? split_workspace_bytes(s->B, s->T, s->H, has_seg, 0) : 0;
   bool use_tc = false, use_split = false;
   if (impl == KDA_IMPL_SPLIT) {
     if (!split_ok) return KDA_ERR_UNSUPPORTED;
-    if (workspace_bytes < split_need) return KDA_ERR_WORKSPACE;
+    if (workspace_bytes < split_min) return KDA_ERR_WORKSPACE;
     use_split = true;
   } else if (impl == KDA_IMPL_TC) {
     if (!tc_ok) return KDA_ERR_UNSUPPORTED;
     use_tc = true;
   } else if (impl == KDA_IMPL_AUTO) {
-    use_split = split_ok && workspace_bytes >= split_need;
+    // Without segment ids every chunk item must fit; with them the fused
+    // fallback covers any overflow, so the minimum split workspace suffices.
+    use_split = split_ok && workspace_bytes >= (has_seg && tc_ok ? split_min : split_need);
     use_tc = !use_split && tc_ok;
   }
   if (!use_tc && !use_split) {
@@ -165,10 +187,11 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
   if (has_seg) {
     e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, o,
                             bf16 ? 1 : 0, initial_state, final_state,
-                            workspace, cs);
+                            workspace, cs, use_split);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  if (use_split) e = launch_fwd_split(p, workspace, cs);
+  if (use_split) e = launch_fwd_split(p, workspace, workspace_bytes, cs,
+                                      impl == KDA_IMPL_AUTO && tc_ok);
   else if (use_tc) e = launch_fwd_tc(p, cs);
   else e = launch_fwd_simt(p, bf16, cs);
   return from_cuda(e);
@@ -182,7 +205,7 @@ int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile) {
     case KDA_IMPL_AUTO: return fwd_tc_supported(s->K, s->V, bf16, v_tile) || simt_ok;
     case KDA_IMPL_SIMT: return simt_ok;
     case KDA_IMPL_TC: return fwd_tc_supported(s->K, s->V, bf16, v_tile);
-    case KDA_IMPL_SPLIT: return fwd_split_supported(s->K, s->V, bf16, false, v_tile);
+    case KDA_IMPL_SPLIT: return fwd_split_supported(s->K, s->V, bf16, true, v_tile);
   }
   return 0;
 }
@@ -235,6 +258,7 @@ kda_status kda_read_device_status(const void *workspace, kda_stream_t stream,
     return KDA_ERR_CUDA;
   *device_bits = bits;
   if (bits & KDA_DEVICE_TIMEOUT) return KDA_ERR_TIMEOUT;
+  if (bits & KDA_DEVICE_WORKSPACE) return KDA_ERR_WORKSPACE;
   if (bits) return KDA_ERR_DEVICE;
   return KDA_OK;
 }

@@ -20,7 +20,10 @@
 // The arithmetic is the same chunk form, sub-block factors and rounding
 // points as the fused kernel (kda_fwd_tc.cu); see there for the algebra.
 // This path needs a workspace of split_workspace_bytes() (about 97 KB per
-// chunk and head) and serves rows without segment ids.
+// chunk and head).  With segment ids the chunks are those of each run (a
+// run's last chunk may be short), sized for a caller bound on runs per row;
+// the kernels check the real chunk count and report KDA_DEVICE_WORKSPACE
+// (doing nothing else) when it does not fit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -88,6 +91,49 @@ __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
   }
 }
 
+// Chunk items: with segment ids, chunk k of the concatenated runs of all rows
+// (run i of row b owns chunks chunk_row_offsets[b] + run_chunk_base[b*T+i] ..);
+// without them, row b owns chunks b*n_chunks ... (b+1)*n_chunks - 1.
+struct ChunkTable {
+  const int32_t *run_chunk_base;     // [B*T] or nullptr (no segment ids)
+  const int32_t *chunk_row_offsets;  // [B+1]
+  const uint32_t *total_chunks;      // device count
+  uint32_t capacity;                 // chunk items the workspace holds
+  int n_chunks_row;                  // chunks per row without segment ids
+  int report_overflow;               // set KDA_DEVICE_WORKSPACE on overflow
+};
+
+__device__ __forceinline__ uint32_t total_chunk_count(const ChunkTable &ct, int B) {
+  return ct.run_chunk_base ? *ct.total_chunks : (uint32_t)B * ct.n_chunks_row;
+}
+
+// First token and end of chunk k, and its row.
+__device__ __forceinline__ void chunk_of(const ChunkTable &ct, const RunTable &rt, int B,
+                                         int T, uint32_t k, int &b, int &t0, int &end) {
+  if (!ct.run_chunk_base) {
+    b = (int)(k / (uint32_t)ct.n_chunks_row);
+    t0 = (int)(k % (uint32_t)ct.n_chunks_row) * C;
+    end = T;
+    return;
+  }
+  int lo = 0, hi = B;  // chunk_row_offsets[lo] <= k < chunk_row_offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)ct.chunk_row_offsets[mid] <= k) lo = mid; else hi = mid;
+  }
+  b = lo;
+  const int kk = (int)k - ct.chunk_row_offsets[lo];
+  const int32_t *base = ct.run_chunk_base + (size_t)lo * T;
+  int rl = 0, rh = rt.row_offsets[lo + 1] - rt.row_offsets[lo];  // runs of row
+  while (rh - rl > 1) {
+    const int mid = (rl + rh) >> 1;
+    if (base[mid] <= kk) rl = mid; else rh = mid;
+  }
+  const int2 run = rt.runs[(size_t)lo * T + rl];
+  t0 = run.x + (kk - base[rl]) * C;
+  end = run.y;
+}
+
 __device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const float (&v)[8]) {
   uint4 w;
   w.x = pack_bf16(v[0], v[1]);
@@ -98,7 +144,7 @@ __device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const flo
 }
 
 __global__ void __launch_bounds__(PT, 1)
-    fwd_prep_kernel(const FwdParams p, unsigned char *items, int n_chunks,
+    fwd_prep_kernel(const FwdParams p, unsigned char *items, const ChunkTable ct,
                     const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_g,
@@ -140,17 +186,18 @@ __global__ void __launch_bounds__(PT, 1)
     set_status(p.status, KDA_DEVICE_TIMEOUT);
   };
 
-  const uint32_t n_items = (uint32_t)p.B * n_chunks * H;
-  auto item_coords = [&](uint32_t it, int &b, int &c, int &h) {
+  const uint32_t n_chunk_items = total_chunk_count(ct, p.B);
+  if (n_chunk_items > ct.capacity && ct.report_overflow && tid == 0 && blockIdx.x == 0)
+    set_status(p.status, KDA_DEVICE_WORKSPACE);  // the items cannot hold every chunk
+  const uint32_t n_items = n_chunk_items > ct.capacity ? 0u : n_chunk_items * (uint32_t)H;
+  auto item_coords = [&](uint32_t it, int &b, int &t0, int &end, int &h) {
     h = (int)(it % (uint32_t)H);
-    const uint32_t bc = it / (uint32_t)H;
-    c = (int)(bc % (uint32_t)n_chunks);
-    b = (int)(bc / (uint32_t)n_chunks);
+    chunk_of(ct, p.runs, p.B, T, it / (uint32_t)H, b, t0, end);
   };
   auto issue_tma = [&](uint32_t it) {
-    int b, c, h;
-    item_coords(it, b, c, h);
-    const int y = b * T + c * C;
+    int b, t0, end, h;
+    item_coords(it, b, t0, end, h);
+    const int y = b * T + t0;
     mbar_expect_tx(tma_bar, P_RAW_TX);
     tma_load_2d(sb + P_RAW_Q, &tm_q, h * KD, y, tma_bar);
     tma_load_2d(sb + P_RAW_K, &tm_k, h * KD, y, tma_bar);
@@ -158,11 +205,10 @@ __global__ void __launch_bounds__(PT, 1)
     tma_load_2d(sb + P_RAW_V, &tm_v, h * VD, y, tma_bar);
   };
   auto load_beta = [&](uint32_t it) -> float {
-    int b, c, h;
-    item_coords(it, b, c, h);
-    const int r = tid;
-    const int t = c * C + r;
-    return t < T ? p.beta[((size_t)b * T + t) * H + h] : 0.f;
+    int b, t0, end, h;
+    item_coords(it, b, t0, end, h);
+    const int t = t0 + tid;
+    return t < end ? p.beta[((size_t)b * T + t) * H + h] : 0.f;
   };
 
   uint32_t item = blockIdx.x;
@@ -174,9 +220,9 @@ __global__ void __launch_bounds__(PT, 1)
     if (tid < C) beta_next = load_beta(item);
   }
   for (; item < n_items; item += gridDim.x) {
-    int b_, c_, h_;
-    item_coords(item, b_, c_, h_);
-    const int n = min(C, T - c_ * C);
+    int b_, t0_, end_, h_;
+    item_coords(item, b_, t0_, end_, h_);
+    const int n = min(C, end_ - t0_);
     const uint32_t next = item + gridDim.x;
     const bool has_next = next < n_items;
     unsigned char *gi = items + (size_t)item * ITEM_BYTES;
@@ -188,7 +234,7 @@ __global__ void __launch_bounds__(PT, 1)
     __syncthreads();
     if (*sAbort) goto done;
 
-    // ---- gate cumsum: one thread per (channel, 16-row block) ----
+    // ---- P0: gate cumsum, one thread per (channel, 16-row block) ----
     {
       const int c = tid & 127, q4 = tid >> 7;
       float v[16];
@@ -209,7 +255,7 @@ __global__ void __launch_bounds__(PT, 1)
     }
     __syncthreads();
 
-    // ---- operands: X, Y_b, (beta K e^G)^T in smem; Q e^G, K e^{G_C-G} out ----
+    // ---- P1: operands: X, Y_b, (beta K e^G)^T in smem; Q e^G, K e^{G_C-G} out ----
     {
       const int rl = tid & 7, cg = (tid >> 3) & 15, hi = (tid >> 7) & 1, bp = tid >> 8;
       const int cc0 = cg * 8;
@@ -298,7 +344,7 @@ __global__ void __launch_bounds__(PT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- intra-chunk products on the tensor cores; next item's tiles ----
+    // ---- P2: intra-chunk products on the tensor cores; next item's tiles ----
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -321,7 +367,7 @@ __global__ void __launch_bounds__(PT, 1)
     if (*sAbort) goto done;
     tc_fence_after();
 
-    // ---- beta A_kk (fp32, strict) to smem; A_qk (inclusive) to the item ----
+    // ---- P3: beta A_kk (fp32, strict) to smem; A_qk (inclusive) to the item ----
     {
       const int r = L & 63;
       const bool is_q = L >= 64;
@@ -375,7 +421,7 @@ __global__ void __launch_bounds__(PT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- T = (I + beta A_kk)^-1, blocked fp32 ----
+    // ---- P4: T = (I + beta A_kk)^-1, blocked fp32 ----
     if (tid < 64) {
       const int i = tid >> 4, cc = tid & 15, base = 16 * i;
       float x[16];
@@ -446,7 +492,7 @@ __global__ void __launch_bounds__(PT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- [w | u] = T [beta K e^G | beta V] (N = 256) ----
+    // ---- P5: [w | u] = T [beta K e^G | beta V] (N = 256) ----
     if (tid == 0) {
       tc_fence_after();
       mma_group(tmem + P_TM_TX, sb + P_TB, sb + P_RHST, C, KD + VD, false, 0, 1);
@@ -525,7 +571,7 @@ static_assert(S_BYTES <= R_STAGE && I_KHT + 16384 == S_U, "stage layout");
 static_assert(R_ALLOC <= 232448, "rec smem fits");
 
 __global__ void __launch_bounds__(RT, 1)
-    fwd_rec_kernel(const FwdParams p, const unsigned char *items, int n_chunks) {
+    fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -568,18 +614,22 @@ __global__ void __launch_bounds__(RT, 1)
   };
 
   float S[VT];
-  const uint32_t n_units = (uint32_t)p.B * H * p.n_vtiles;
+  const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
+  const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const int vt = (int)(unit % (uint32_t)p.n_vtiles);
-    const int h = (int)((unit / (uint32_t)p.n_vtiles) % (uint32_t)H);
-    const int b = (int)(unit / ((uint32_t)p.n_vtiles * H));
+    const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
+    const int vt = u.vt, h = u.h, b = u.b;
     const int vc0 = vt * VT;
+    const int n_chunks = (u.end - u.start + C - 1) / C;
+    const uint32_t cbase = ct.run_chunk_base
+        ? (uint32_t)(ct.chunk_row_offsets[b] + ct.run_chunk_base[(size_t)b * T + u.run_in_row])
+        : (uint32_t)b * ct.n_chunks_row;
     auto item_ptr = [&](int c) {
-      return items + ((size_t)((size_t)b * n_chunks + c) * H + h) * ITEM_BYTES;
+      return items + ((size_t)(cbase + c) * H + h) * ITEM_BYTES;
     };
     {
       const int c = tid;
-      if (p.initial_state) {
+      if (u.first && p.initial_state) {
         const float4 *src = reinterpret_cast<const float4 *>(
             p.initial_state + (((size_t)b * H + h) * KD + c) * p.V + vc0);
 #pragma unroll
@@ -609,17 +659,19 @@ __global__ void __launch_bounds__(RT, 1)
 
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
-      const int n = min(C, T - c * C);
-      const size_t tok0 = (size_t)b * T + (size_t)c * C;
+      const int t0 = u.start + c * C;
+      const int n = min(C, u.end - t0);
+      const size_t tok0 = (size_t)b * T + t0;
       const unsigned char *stg = smem + (uint32_t)s * R_STAGE;
       const uint32_t sstg = sb + (uint32_t)s * R_STAGE;
+      // ---- P10: wait for the stage
       if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
       else st_issued &= ~(1u << s);
       st_phase[s] ^= 1u;
       __syncthreads();
       if (*sAbort) goto done;
 
-      // D1 = [w ; Q e^G] S
+      // ---- P11: D1 = [w ; Q e^G] S
       if (tid == 0) {
         tc_fence_after();
         mma_group(tmem + TM_D1, sstg + I_WQ, sb + R_ST, KD, VT, false, 0, 1);
@@ -634,7 +686,7 @@ __global__ void __launch_bounds__(RT, 1)
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // U = u - w S  (lanes 0..63)
+      // ---- P12: U = u - w S  (lanes 0..63)
       if (warp < 2) {
         const int r = L;
         float v0[16], v1[16];
@@ -657,7 +709,7 @@ __global__ void __launch_bounds__(RT, 1)
       tc_fence_before();
       __syncthreads();
 
-      // D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
+      // ---- P13: D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
       if (tid == 0) {
         tc_fence_after();
         mma_group(tmem + TM_D1, sstg + I_TAQ, sb + R_UT, C, VT, true, 0, 1);
@@ -673,7 +725,7 @@ __global__ void __launch_bounds__(RT, 1)
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // o rows (lanes 64..127); state update (all lanes = key rows)
+      // ---- P14: o rows (lanes 64..127); state update (all lanes = key rows)
       if (warp >= 2) {
         const int r = L - 64;
         float v0[16], v1[16];
@@ -724,7 +776,7 @@ __global__ void __launch_bounds__(RT, 1)
         st_issued |= 1u << s;
       }
     }
-    if (p.final_state) {
+    if (u.last && p.final_state) {
       float4 *dst = reinterpret_cast<float4 *>(
           p.final_state + (((size_t)b * H + h) * KD + tid) * p.V + vc0);
 #pragma unroll
@@ -777,23 +829,52 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
 
 }  // namespace
 
-size_t split_workspace_bytes(int B, int T, int H) {
+namespace {
+// Byte offset of the first item: after the header (no segment ids) or after
+// the run list and the chunk tables (segment ids).
+size_t items_offset(int B, int T, bool has_seg) {
+  return has_seg ? align_up(ws_bytes(B, T, true) + ws_chunk_tables_bytes(B, T), 1024)
+                 : WS_ITEMS_OFF;
+}
+}  // namespace
+
+size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row) {
   const size_t nc = ((size_t)T + C - 1) / C;
-  return WS_ITEMS_OFF + (size_t)B * nc * H * ITEM_BYTES;
+  const size_t chunks = has_seg ? (size_t)B * (nc + (size_t)(max_runs_per_row > 0 ? max_runs_per_row : 0))
+                                : (size_t)B * nc;
+  return items_offset(B, T, has_seg) + chunks * H * ITEM_BYTES;
 }
 
-bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile) {
-  return bf16 && !has_seg && K == KD && V == VD && (v_tile == 0 || v_tile == VT);
+bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
+  return bf16 && K == KD && V == VD && (v_tile == 0 || v_tile == VT);
 }
 
-cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, cudaStream_t stream) {
-  if (!fwd_split_supported(p_in.K, p_in.V, true, p_in.runs.runs != nullptr, p_in.v_tile))
+cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, bool with_fallback) {
+  const bool has_seg = p_in.runs.runs != nullptr;
+  if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, p_in.v_tile))
     return cudaErrorNotSupported;
   FwdParams p = p_in;
   p.v_tile = VT;
   p.n_vtiles = VD / VT;
-  const int n_chunks = (p.T + C - 1) / C;
-  unsigned char *items = static_cast<unsigned char *>(workspace) + WS_ITEMS_OFF;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  const size_t ioff = items_offset(p.B, p.T, has_seg);
+  if (workspace_bytes < ioff + (size_t)p.H * ITEM_BYTES) return cudaErrorInvalidValue;
+  unsigned char *items = ws + ioff;
+  ChunkTable ct;
+  ct.report_overflow = with_fallback ? 0 : 1;
+  ct.n_chunks_row = (p.T + C - 1) / C;
+  ct.capacity = (uint32_t)((workspace_bytes - ioff) / ((size_t)p.H * ITEM_BYTES));
+  if (has_seg) {
+    ct.run_chunk_base = reinterpret_cast<const int32_t *>(ws + ws_bytes(p.B, p.T, true));
+    ct.chunk_row_offsets = reinterpret_cast<const int32_t *>(
+        ws + ws_bytes(p.B, p.T, true) + align_up(sizeof(int32_t) * (size_t)p.B * p.T, 256));
+    ct.total_chunks = &reinterpret_cast<const WsHeader *>(ws)->total_chunks;
+  } else {
+    ct.run_chunk_base = nullptr;
+    ct.chunk_row_offsets = nullptr;
+    ct.total_chunks = nullptr;
+  }
   const uint64_t rows = (uint64_t)p.B * p.T;
   CUtensorMap mq, mk, mg, mv;
   if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, KD) ||
@@ -808,15 +889,23 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, cudaStream_
                            (int)R_ALLOC);
   if (e != cudaSuccess) return e;
   const long sms = num_sms();
-  const long n_items = (long)p.B * n_chunks * p.H;
+  const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
   const int g1 = (int)(n_items < sms ? n_items : sms);
-  fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, n_chunks, mq, mk, mg, mv);
+  fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long n_units = (long)p.B * p.H * p.n_vtiles;
+  const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
+                               : (long)p.B * p.H * p.n_vtiles;
   const int g2 = (int)(n_units < sms ? n_units : sms);
-  fwd_rec_kernel<<<g2 > 0 ? g2 : 1, RT, R_ALLOC, stream>>>(p, items, n_chunks);
-  return cudaGetLastError();
+  fwd_rec_kernel<<<g2 > 0 ? g2 : 1, RT, R_ALLOC, stream>>>(p, items, ct);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !with_fallback || !has_seg) return e;
+  // The fused kernel covers calls whose runs overflow the items (it exits
+  // at once when they fit).
+  FwdParams pf = p_in;
+  pf.gate_chunks = ct.total_chunks;
+  pf.gate_capacity = ct.capacity;
+  return launch_fwd_tc(pf, stream);
 }
 
 }  // namespace kda

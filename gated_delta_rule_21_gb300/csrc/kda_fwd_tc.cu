@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = 32 * quad + lane;  // this thread's TMEM lane
   const int H = p.H, T = p.T;
 
+  // Fallback gate: nothing to do when the split path served this call.
+  if (p.gate_chunks && *p.gate_chunks <= p.gate_capacity) return;
   if (warp == 0) tmem_alloc(sb + TMEMSLOT_OFF, TMEM_COLS);
   if (tid == 0) {
     mbar_init(tma_bar, 1);

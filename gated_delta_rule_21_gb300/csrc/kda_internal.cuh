@@ -23,10 +23,11 @@ constexpr int kNumSub = kChunk / kSub;
 //                       runs[b*T + i]
 // ---------------------------------------------------------------------------
 struct WsHeader {
-  uint32_t status;      // KDA_DEVICE_* bits, sticky until cleared
-  uint32_t rows_done;   // run-builder completion counter (returns to 0)
-  uint32_t total_runs;  // number of runs over all rows (run-builder output)
-  uint32_t reserved[61];
+  uint32_t status;        // KDA_DEVICE_* bits, sticky until cleared
+  uint32_t rows_done;     // run-builder completion counter (returns to 0)
+  uint32_t total_runs;    // number of runs over all rows (run-builder output)
+  uint32_t total_chunks;  // 64-token chunks over all runs (split path only)
+  uint32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -39,6 +40,14 @@ inline size_t ws_bytes(int B, int T, bool has_seg) {
   size_t n = sizeof(WsHeader);
   if (has_seg) n += ws_row_offsets_bytes(B) + sizeof(int2) * (size_t)B * T;
   return n;
+}
+
+// The split path with segment ids appends, after ws_bytes(B, T, true):
+//   int32 run_chunk_base[B*T] (first chunk of run i of row b, within the row),
+//   int32 chunk_row_offsets[B+1] (prefix of chunk counts over rows),
+// then its per-chunk items.
+inline size_t ws_chunk_tables_bytes(int B, int T) {
+  return align_up(sizeof(int32_t) * (size_t)B * T, 256) + ws_row_offsets_bytes(B);
 }
 
 // Where one unit of work lives: a run of one row, for one head, for one
@@ -60,6 +69,11 @@ struct FwdParams {
   float *final_state;
   RunTable runs;
   uint32_t *status;
+  // Fallback gate (AUTO with segment ids): when set, the fused kernel runs
+  // only if *gate_chunks > gate_capacity, i.e. when the split path's items
+  // could not hold the runs of this call; the split kernels then do nothing.
+  const uint32_t *gate_chunks;
+  uint32_t gate_capacity;
 };
 
 struct ConvParams {
@@ -76,7 +90,7 @@ cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
                                 const int32_t *segment_ids, void *o,
                                 int o_is_bf16, const float *initial_state,
                                 float *final_state, void *workspace,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool with_chunks = false);
 
 cudaError_t launch_fwd_simt(const FwdParams &p, bool bf16, cudaStream_t stream);
 // Tensor-core path (bf16, K = V = 128).  Returns cudaErrorNotSupported when
@@ -86,9 +100,15 @@ bool fwd_tc_supported(int K, int V, bool bf16, int v_tile);
 
 // Split tensor-core path (parallel prep kernel + recurrence kernel), bf16,
 // K = V = 128, no segment ids; needs split_workspace_bytes() of workspace.
-size_t split_workspace_bytes(int B, int T, int H);
+// With segment ids, the items are sized for at most max_runs_per_row runs
+// per row; the kernels check the real count and report overflow.
+size_t split_workspace_bytes(int B, int T, int H, bool has_seg = false,
+                             int max_runs_per_row = 0);
 bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile);
-cudaError_t launch_fwd_split(const FwdParams &p, void *workspace, cudaStream_t stream);
+// with_fallback (AUTO): with segment ids, also enqueue the fused kernel,
+// gated to run only when the runs overflow the split items.
+cudaError_t launch_fwd_split(const FwdParams &p, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, bool with_fallback = false);
 
 cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
                               cudaStream_t stream);
@@ -116,6 +136,7 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
 // Decode unit index -> (row b, run [start, end), first/last flags, h, vt).
 struct Unit {
   int b, start, end, h, vt;
+  int run_in_row;  // index of the run within its row
   bool first, last;
 };
 
@@ -137,6 +158,7 @@ __device__ __forceinline__ Unit decode_unit(const RunTable &rt, uint32_t u,
     x.b = run;
     x.start = 0;
     x.end = T;
+    x.run_in_row = 0;
     x.first = x.last = true;
     return x;
   }
@@ -152,6 +174,7 @@ __device__ __forceinline__ Unit decode_unit(const RunTable &rt, uint32_t u,
   const int2 r = rt.runs[(size_t)lo * T + i];
   x.start = r.x;
   x.end = r.y;
+  x.run_in_row = i;
   x.first = (i == 0);
   x.last = (i == n - 1);
   return x;

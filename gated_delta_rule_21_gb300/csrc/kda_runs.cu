@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kThreads)
                         const int32_t *__restrict__ seg, char *o,
                         int o_elem_bytes, const float *initial_state,
                         float *final_state, WsHeader *hdr,
-                        int32_t *row_offsets, int2 *runs) {
+                        int32_t *row_offsets, int2 *runs,
+                        int32_t *run_chunk_base, int32_t *chunk_row_offsets) {
   __shared__ unsigned long long sm_scan[32];
   __shared__ int sm_pad[kTile];
   __shared__ int sm_is_last;
@@ -135,8 +136,29 @@ __global__ void __launch_bounds__(kThreads)
       dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
+  // Chunks of 64 tokens per run and their prefix inside the row (for the
+  // split path, whose work items are (run, chunk, head)).
+  int n_chunks_row = 0;
+  if (run_chunk_base) {
+    __syncthreads();  // this row's run records are written
+    for (int base = 0; base < n_runs; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      int cnt = 0;
+      if (i < n_runs) {
+        const int2 r = rrow[i];
+        cnt = (r.y - r.x + kChunk - 1) / kChunk;
+      }
+      unsigned long long tot;
+      const unsigned long long ex =
+          block_excl_scan64((unsigned long long)cnt, &tot, sm_scan);
+      if (i < n_runs) run_chunk_base[(size_t)b * T + i] = n_chunks_row + (int)ex;
+      n_chunks_row += (int)tot;
+    }
+  }
+
   if (threadIdx.x == 0) {
     row_offsets[b + 1] = n_runs;
+    if (chunk_row_offsets) chunk_row_offsets[b + 1] = n_chunks_row;
     __threadfence();
     const unsigned prev = atomicAdd(&hdr->rows_done, 1u);
     __threadfence();
@@ -156,9 +178,25 @@ __global__ void __launch_bounds__(kThreads)
     if (i < B) row_offsets[i + 1] = carry + (int)ex + c;
     carry += (int)tot;
   }
+  int chunk_carry = 0;
+  if (chunk_row_offsets) {
+    for (int base = 0; base < B; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const int c = i < B ? __ldcg(chunk_row_offsets + i + 1) : 0;
+      unsigned long long tot;
+      const unsigned long long ex =
+          block_excl_scan64((unsigned long long)c, &tot, sm_scan);
+      if (i < B) chunk_row_offsets[i + 1] = chunk_carry + (int)ex + c;
+      chunk_carry += (int)tot;
+    }
+  }
   if (threadIdx.x == 0) {
     row_offsets[0] = 0;
     hdr->total_runs = (uint32_t)carry;
+    if (chunk_row_offsets) {
+      chunk_row_offsets[0] = 0;
+      hdr->total_chunks = (uint32_t)chunk_carry;
+    }
     hdr->rows_done = 0u;
   }
 }
@@ -169,15 +207,21 @@ cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
                                 const int32_t *segment_ids, void *o,
                                 int o_is_bf16, const float *initial_state,
                                 float *final_state, void *workspace,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool with_chunks) {
   char *ws = static_cast<char *>(workspace);
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
   int32_t *row_offsets = reinterpret_cast<int32_t *>(ws + sizeof(WsHeader));
   int2 *runs =
       reinterpret_cast<int2 *>(ws + sizeof(WsHeader) + ws_row_offsets_bytes(B));
+  int32_t *chunk_base = nullptr, *chunk_rows = nullptr;
+  if (with_chunks) {
+    chunk_base = reinterpret_cast<int32_t *>(ws + ws_bytes(B, T, true));
+    chunk_rows = reinterpret_cast<int32_t *>(ws + ws_bytes(B, T, true) +
+                                             align_up(sizeof(int32_t) * (size_t)B * T, 256));
+  }
   segment_runs_kernel<<<B, kThreads, 0, stream>>>(
       B, T, H, K, V, segment_ids, static_cast<char *>(o), o_is_bf16 ? 2 : 4,
-      initial_state, final_state, hdr, row_offsets, runs);
+      initial_state, final_state, hdr, row_offsets, runs, chunk_base, chunk_rows);
   return cudaGetLastError();
 }
 

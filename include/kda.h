@@ -80,7 +80,10 @@ typedef struct kda_shape {
 /* Implementation choice for kda_chunk_fwd_ex. */
 typedef enum kda_impl {
   KDA_IMPL_AUTO = 0,  /* fastest that applies: SPLIT when the workspace is
-                         large enough, else TC, else SIMT                   */
+                         large enough, else TC, else SIMT.  With segment
+                         ids and the split path it always computes the
+                         result: runs that overflow the split workspace are
+                         served by the fused TC kernel on the device.       */
   KDA_IMPL_SIMT = 1,  /* fp32 CUDA-core kernel (every supported shape)      */
   KDA_IMPL_TC = 2,    /* fused tcgen05 / TMA kernel: bf16, K = V = 128      */
   KDA_IMPL_SPLIT = 3  /* tcgen05 in two kernels (parallel per-chunk prep,
@@ -92,6 +95,8 @@ typedef enum kda_impl {
 /* Device status bits OR-ed into the workspace status word. */
 #define KDA_DEVICE_TIMEOUT 0x1u    /* a bounded mbarrier / flag wait ran out */
 #define KDA_DEVICE_BAD_INPUT 0x2u  /* a debug-build input check failed       */
+#define KDA_DEVICE_WORKSPACE 0x4u  /* the runs need more chunk items than the
+                                      workspace was sized for (split path) */
 
 /*
  * Bytes of workspace kda_chunk_fwd needs for this shape.  The workspace
@@ -106,13 +111,28 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_
 /*
  * Workspace bytes implementation `impl` needs (same zero-fill rule).  For
  * KDA_IMPL_SPLIT this holds the per-chunk operands the recurrence kernel
- * reads: about 97 KB per (row, 64-token chunk, head).  For KDA_IMPL_AUTO it
- * is the size that lets AUTO pick its fastest kernel for the shape.
+ * reads: about 97 KB per (row, 64-token chunk, head).  With segment ids the
+ * chunks are those of each run, so their number depends on the runs: the
+ * size returned here assumes at most ceil(T/64) runs per row (see
+ * kda_chunk_fwd_workspace_size_packed for another bound).  For
+ * KDA_IMPL_AUTO it is the size that lets AUTO pick its fastest kernel.
  * Returns 0 when the shape or the choice is invalid or does not apply.
  */
 KDA_API size_t kda_chunk_fwd_workspace_size_for(const kda_shape *s,
                                                 int has_segment_ids,
                                                 kda_impl impl);
+
+/*
+ * Split-path workspace for packed inputs with at most max_runs_per_row runs
+ * in any row (the pages' bound on segments per row, max_segments_per_seq):
+ * room for B * (ceil(T/64) + max_runs_per_row) chunk items.  When the runs
+ * of a call need more chunk items than its workspace holds, the split path
+ * computes nothing and sets KDA_DEVICE_WORKSPACE in the status word
+ * (kda_read_device_status then returns KDA_ERR_WORKSPACE).  Returns 0 for an
+ * invalid shape, a shape the split path does not serve, or a bound < 1.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size_packed(const kda_shape *s,
+                                                   int max_runs_per_row);
 
 /*
  * Chunked KDA forward (the operation above).
@@ -224,8 +244,9 @@ KDA_API kda_status kda_short_conv_silu(const kda_shape *s, const void *x_q,
 /*
  * Waits for `stream`, then reads the device status word at the start of
  * `workspace` into *device_bits (KDA_DEVICE_* bits, 0 when clean).  Returns
- * KDA_ERR_TIMEOUT when the timeout bit is set, KDA_ERR_DEVICE for any other
- * bit, KDA_OK when clean, KDA_ERR_CUDA when the copy fails.
+ * KDA_ERR_TIMEOUT when the timeout bit is set, KDA_ERR_WORKSPACE for the
+ * workspace bit, KDA_ERR_DEVICE for any other bit, KDA_OK when clean,
+ * KDA_ERR_CUDA when the copy fails.
  */
 KDA_API kda_status kda_read_device_status(const void *workspace, kda_stream_t stream,
                                   uint32_t *device_bits);

@@ -35,7 +35,8 @@ def test_header_declares_expected_entry_points():
     for must in ("kda_chunk_fwd", "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size",
                  "kda_short_conv_silu", "kda_read_device_status",
                  "kda_clear_device_status", "kda_status_string", "kda_version",
-                 "kda_impl_available", "kda_chunk_fwd_workspace_size_for"):
+                 "kda_impl_available", "kda_chunk_fwd_workspace_size_for",
+                 "kda_chunk_fwd_workspace_size_packed"):
         assert must in names
 
 
@@ -124,7 +125,13 @@ def test_workspace_size_for_each_impl(L):
     assert split == 1024 + 128 * 32 * 99328          # one 97 KiB item per chunk-head
     assert kda.workspace_size(1, 8192, 32, 128, 128, impl="auto") == split
     assert kda.workspace_size(1, 8192, 32, 128, 128, impl="tc") == base
-    assert kda.workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="split") == 0
+    # packed: header + run list + chunk tables, then B*(ceil(T/64) + runs bound) items
+    packed = kda.workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="split")
+    assert packed == kda.workspace_size_packed(1, 100, 2, 128, 128, 2)
+    assert kda.workspace_size_packed(1, 100, 2, 128, 128, 5) - \
+        kda.workspace_size_packed(1, 100, 2, 128, 128, 2) == 3 * 2 * 99328
+    assert kda.workspace_size_packed(1, 100, 2, 128, 128, 0) == 0
+    assert kda.workspace_size_packed(1, 100, 2, 64, 64, 3) == 0
     assert kda.workspace_size(1, 100, 2, 64, 64, impl="split") == 0
     assert kda.workspace_size(1, 100, 2, 128, 128, torch.float32, impl="auto") == \
         kda.workspace_size(1, 100, 2, 128, 128, torch.float32)
@@ -132,7 +139,7 @@ def test_workspace_size_for_each_impl(L):
 
 def test_split_rejects_small_workspace(L):
     assert call_fwd(L, impl=3, ws_bytes=4096) == 4
-    assert call_fwd(L, impl=3, seg=FAKE) == 2
+    assert call_fwd(L, impl=3, seg=FAKE, ws_bytes=8192) == 4
 
 
 def test_status_calls_reject_null(L):

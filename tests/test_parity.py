@@ -144,6 +144,39 @@ def test_device_status_clean_and_workspace_reuse():
     assert_parity(o, o_ref, True, "o after workspace reuse")
 
 
+def test_split_packed_with_explicit_runs_bound():
+    """Packed input on the split path with a workspace sized for exactly the
+    runs present (four per row)."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.WORKLOADS["packed_bf16_h8_t1024_4seg"]
+    x = ki.make_inputs(w, seed=5)
+    ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, torch.bfloat16, True, impl="split",
+                             max_runs_per_row=4)
+    o, fs = run_gpu(x, impl="split", workspace=ws)
+    assert kda.read_device_status(ws) == 0
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, "o")
+    assert_parity(fs, fs_ref, True, "final_state")
+
+
+def test_split_packed_overflow_is_reported_not_computed():
+    """More runs than the workspace was sized for: the split path reports
+    KDA_DEVICE_WORKSPACE in the status word instead of writing garbage past
+    its items, and the context stays usable."""
+    import gated_delta_rule_21_gb300 as kda
+    lens = [1] * 120 + [8]          # 121 runs in one row of 128 tokens
+    w = ki.custom_workload(1, 128, 2, 128, 128, segments=lens)
+    x = ki.make_inputs(w, seed=6)
+    ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, torch.bfloat16, True, impl="split",
+                             max_runs_per_row=1)
+    run_gpu(x, impl="split", workspace=ws)
+    assert kda.read_device_status(ws) & 0x4
+    kda.clear_device_status(ws)
+    o, fs = run_gpu(x, impl="tc")      # the same inputs on the fused path
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, "o")
+
+
 def test_misaligned_pointer_rejected_on_gpu():
     import gated_delta_rule_21_gb300 as kda
     w = ki.custom_workload(1, 64, 1, 128, 128)
