@@ -9,7 +9,7 @@
 //      the operands the recurrence needs into the workspace, already in the
 //      shared-memory layouts the tensor cores read:
 //         [w ; Q e^G] (128 x 128 bf16), [T ; A_qk] (128 x 64 bf16),
-//         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 fp32), e^{G_C}.
+//         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 bf16), e^{G_C}.
 //   2. fwd_rec_kernel: one CTA per (row, head, 32-column value tile) walks
 //      the chunks in order with the fp32 state in registers; per chunk it
 //      bulk-copies the item (double-buffered) and runs only the
@@ -19,7 +19,7 @@
 //
 // The arithmetic is the same chunk form, sub-block factors and rounding
 // points as the fused kernel (kda_fwd_tc.cu); see there for the algebra.
-// This path needs a workspace of split_workspace_bytes() (about 97 KB per
+// This path needs a workspace of split_workspace_bytes() (about 81 KB per
 // chunk and head).  With segment ids the chunks are those of each run (a
 // run's last chunk may be short), sized for a caller bound on runs per row;
 // the kernels check the real chunk count and report KDA_DEVICE_WORKSPACE
@@ -43,9 +43,9 @@ constexpr int VT = 32;
 constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: K-major, 128 rows, Kd 128
 constexpr uint32_t I_TAQ = 32768;     // [T ; A_qk]: K-major, 128 rows, Kd 64
 constexpr uint32_t I_KHT = 49152;     // (K e^{G_C-G})^T: MN-major, 128 x Kd 64
-constexpr uint32_t I_U = 65536;       // u fp32 [vt][r][32]
-constexpr uint32_t I_GAM = 98304;     // e^{G_C} fp32 [128]
-constexpr uint32_t ITEM_BYTES = 99328;     // 97 KiB, 1 KiB aligned
+constexpr uint32_t I_U = 65536;       // u bf16 [vt][r][32]
+constexpr uint32_t I_GAM = 81920;     // e^{G_C} fp32 [128]
+constexpr uint32_t ITEM_BYTES = 82944;     // 81 KiB, 1 KiB aligned
 constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
 
 // ---- prep kernel shared memory ----------------------------------------------
@@ -72,14 +72,15 @@ constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T bf16 K-major (128-row op
 constexpr uint32_t P_SCR = P_TB + 16384;           // 3 x 256 fp32
 static_assert(P_SCR + 3072 <= P_RHST, "prep aliases inside X / Y");
 static_assert(P_ALLOC <= 232448, "prep smem fits");
-constexpr uint32_t P_TM_TX = 256;  // TMEM: A blocks at 0/32/64/128, [w | u] at 256
+constexpr uint32_t P_TM_TX = 256;  // TMEM: X Y^T at 0..159, [w | u] at 256
 
 __device__ __forceinline__ uint32_t p_y_off(int b) {
   return P_Y + 256u * (uint32_t)(8 * b * (b + 1));
 }
-__device__ __forceinline__ uint32_t tm_a(int b) {
-  return b == 0 ? 0u : b == 1 ? 32u : b == 2 ? 64u : 128u;
-}
+// Y_0..Y_3 are stored back to back (row groups of 8), so together they form
+// one 160-row B operand: a single N = 160 MMA gives X Y_b^T for every b at
+// TMEM columns 8 b (b + 1) ... 8 b (b + 1) + 16 (b + 1) - 1.
+__device__ __forceinline__ uint32_t tm_a(int b) { return 8u * (uint32_t)(b * (b + 1)); }
 __device__ __forceinline__ int piece_count(int quad) { return (quad & 1) ? 7 : 3; }
 __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
   if ((quad & 1) == 0) {
@@ -255,17 +256,16 @@ __global__ void __launch_bounds__(PT, 1)
     }
     __syncthreads();
 
-    // ---- P1: operands: X, Y_b, (beta K e^G)^T in smem; Q e^G, K e^{G_C-G} out ----
+    // ---- P1: operands X, Y_b (the intra-chunk MMA inputs) first ----
+    // Thread -> 8 channels of 2 rows of one 16-row block (warp-uniform
+    // block), so the per-channel block factors are built once per thread.
+    uint32_t kbp[2][4], qtp[2][4], khp[2][4];  // bf16 pairs stored after the MMA issue
+    const int rl = tid & 7, cg = (tid >> 3) & 15, b = tid >> 7;
+    const int cc0 = cg * 8;
     {
-      const int rl = tid & 7, cg = (tid >> 3) & 15, hi = (tid >> 7) & 1, bp = tid >> 8;
-      const int cc0 = cg * 8;
-#pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int b = 2 * bp + i2;  // warp-uniform block of this row
-        const int r = kSub * b + 8 * hi + rl;
-        const bool valid = r < n;
-        const float br = sBeta[r];
-        float D[kNumSub][8], Pb[8], Eb[8], kk[8], qq[8], G[8];
+      float pre[8], suf[8], rD[8], x2[8], x3[8], Pl[8], El[8];
+      {
+        float D[kNumSub][8], Eb[8], Pb[8];
 #pragma unroll
         for (int i = 0; i < kNumSub; ++i) {
           const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
@@ -273,51 +273,64 @@ __global__ void __launch_bounds__(PT, 1)
           D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
           D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
         }
+        const float4 *ep = reinterpret_cast<const float4 *>(sG + (b * kSub + kSub - 1) * KD + cc0);
+        const float4 e0 = ep[0], e1v = ep[1];
+        Eb[0] = e0.x; Eb[1] = e0.y; Eb[2] = e0.z; Eb[3] = e0.w;
+        Eb[4] = e1v.x; Eb[5] = e1v.y; Eb[6] = e1v.z; Eb[7] = e1v.w;
+        const float4 *pq = reinterpret_cast<const float4 *>(sG + (b > 0 ? b * kSub - 1 : 0) * KD + cc0);
+        const float4 p0 = pq[0], p1 = pq[1];
+        const float z = b > 0 ? 1.f : 0.f;
+        Pb[0] = z * p0.x; Pb[1] = z * p0.y; Pb[2] = z * p0.z; Pb[3] = z * p0.w;
+        Pb[4] = z * p1.x; Pb[5] = z * p1.y; Pb[6] = z * p1.z; Pb[7] = z * p1.w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float a = 1.f, zz = 1.f, Db = 1.f, c2 = 1.f, c3 = 1.f;
+#pragma unroll
+          for (int i = 0; i < kNumSub; ++i) {
+            const float Di = D[i][j];
+            if (i < b) a *= Di;
+            if (i > b) zz *= Di;
+            if (i == b) Db = Di;
+            if (i == b + 1) { c2 *= Di; c3 *= Di; }
+            if (i == b + 2) c3 *= Di;
+          }
+          pre[j] = a; suf[j] = zz; rD[j] = __frcp_rn(Db); x2[j] = c2; x3[j] = c3;
+          Pl[j] = Pb[j] * kLog2e;
+          El[j] = Eb[j] * kLog2e;
+        }
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int r = kSub * b + 8 * i2 + rl;
+        const bool valid = r < n;
+        const float br = sBeta[r];
+        float kk[8], qq[8], G[8];
+        ld_bf16x8(smem + P_RAW_K + r * 256 + cc0 * 2, kk);
+        ld_bf16x8(smem + P_RAW_Q + r * 256 + cc0 * 2, qq);
         {
-          const float4 *ep = reinterpret_cast<const float4 *>(sG + (b * kSub + kSub - 1) * KD + cc0);
-          const float4 e0 = ep[0], e1v = ep[1];
-          Eb[0] = e0.x; Eb[1] = e0.y; Eb[2] = e0.z; Eb[3] = e0.w;
-          Eb[4] = e1v.x; Eb[5] = e1v.y; Eb[6] = e1v.z; Eb[7] = e1v.w;
-          const float4 *pq = reinterpret_cast<const float4 *>(sG + (b > 0 ? b * kSub - 1 : 0) * KD + cc0);
-          const float4 p0 = pq[0], p1 = pq[1];
-          const float z = b > 0 ? 1.f : 0.f;
-          Pb[0] = z * p0.x; Pb[1] = z * p0.y; Pb[2] = z * p0.z; Pb[3] = z * p0.w;
-          Pb[4] = z * p1.x; Pb[5] = z * p1.y; Pb[6] = z * p1.z; Pb[7] = z * p1.w;
           const float4 *gp = reinterpret_cast<const float4 *>(sG + r * KD + cc0);
           const float4 g0 = gp[0], g1 = gp[1];
           G[0] = g0.x; G[1] = g0.y; G[2] = g0.z; G[3] = g0.w;
           G[4] = g1.x; G[5] = g1.y; G[6] = g1.z; G[7] = g1.w;
         }
-        ld_bf16x8(smem + P_RAW_K + r * 256 + cc0 * 2, kk);
-        ld_bf16x8(smem + P_RAW_Q + r * 256 + cc0 * 2, qq);
-        float xk[8], xq[8], qt[8], kb[8], kh[8], yd[8], y1[8], y2[8], y3[8];
+        float xk[8], xq[8], yd[8], y1[8], y2[8], y3[8], qt[8], kb[8], kh[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float pre = 1.f, suf = 1.f, Db = 1.f, x2 = 1.f, x3 = 1.f;
-#pragma unroll
-          for (int i = 0; i < kNumSub; ++i) {
-            const float Di = D[i][j];
-            if (i < b) pre *= Di;
-            if (i > b) suf *= Di;
-            if (i == b) Db = Di;
-            if (i == b + 1) { x2 *= Di; x3 *= Di; }
-            if (i == b + 2) x3 *= Di;
-          }
           const float gl = G[j] * kLog2e;
-          const float e1 = ex2(gl - Pb[j] * kLog2e);  // e^{G - P_b}
-          const float e2 = ex2(Eb[j] * kLog2e - gl);  // e^{E_b - G}
+          const float e1 = ex2(gl - Pl[j]);  // e^{G - P_b}
+          const float e2 = ex2(El[j] - gl);  // e^{E_b - G}
           const float kv = valid ? kk[j] : 0.f;
           const float qv = valid ? qq[j] : 0.f;
           xk[j] = kv * e1;
           xq[j] = qv * e1;
-          qt[j] = xq[j] * pre;
-          kb[j] = xk[j] * (br * pre);
+          qt[j] = xq[j] * pre[j];
+          kb[j] = xk[j] * (br * pre[j]);
           const float ke2 = kv * e2;
-          kh[j] = ke2 * suf;
-          yd[j] = ke2 * __frcp_rn(Db);
+          kh[j] = ke2 * suf[j];
+          yd[j] = ke2 * rD[j];
           y1[j] = ke2;
-          y2[j] = ke2 * x2;
-          y3[j] = ke2 * x3;
+          y2[j] = ke2 * x2[j];
+          y3[j] = ke2 * x3[j];
         }
         st_bf16x8(smem, P_X + op_off(r, cc0, KD), xk);
         st_bf16x8(smem, P_X + op_off(64 + r, cc0, KD), xq);
@@ -325,12 +338,15 @@ __global__ void __launch_bounds__(PT, 1)
         if (b + 1 < kNumSub) st_bf16x8(smem, p_y_off(b + 1) + op_off(r, cc0, KD), y1);
         if (b + 2 < kNumSub) st_bf16x8(smem, p_y_off(b + 2) + op_off(r, cc0, KD), y2);
         if (b + 3 < kNumSub) st_bf16x8(smem, p_y_off(b + 3) + op_off(r, cc0, KD), y3);
-        st_bf16x8(smem, P_RHST + mn_off(cc0, r, C), kb);
-        st_g16(gi, I_WQ + op_off(64 + r, cc0, KD), qt);
-        st_g16(gi, I_KHT + mn_off(cc0, r, C), kh);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          kbp[i2][q2] = pack_bf16(kb[2 * q2], kb[2 * q2 + 1]);
+          qtp[i2][q2] = pack_bf16(qt[2 * q2], qt[2 * q2 + 1]);
+          khp[i2][q2] = pack_bf16(kh[2 * q2], kh[2 * q2 + 1]);
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {  // (beta V)^T
+      for (int e = 0; e < 2; ++e) {  // (beta V)^T, read before the next tiles land
         const int r = tid >> 3, vg = (tid & 7) + 8 * e;
         float vv[8];
         ld_bf16x8(smem + P_RAW_V + r * 256 + vg * 16, vv);
@@ -344,15 +360,25 @@ __global__ void __launch_bounds__(PT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- P2: intra-chunk products on the tensor cores; next item's tiles ----
+    // ---- P2: intra-chunk products on the tensor cores; next item's tiles;
+    //      the remaining operands are stored while the MMAs run ----
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll
-      for (int b = 0; b < kNumSub; ++b)
-        mma_group(tmem + tm_a(b), sb + P_X, sb + p_y_off(b), KD, 16 * (b + 1), false, 0, 0);
+      mma_group(tmem, sb + P_X, sb + P_Y, KD, 160, false, 0, 0);
       mma_commit(mma_bar);
       if (has_next) issue_tma(next);
     }
+#pragma unroll
+    for (int i2 = 0; i2 < 2; ++i2) {
+      const int r = kSub * b + 8 * i2 + rl;
+      *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(cc0, r, C)) =
+          make_uint4(kbp[i2][0], kbp[i2][1], kbp[i2][2], kbp[i2][3]);
+      *reinterpret_cast<uint4 *>(gi + I_WQ + op_off(64 + r, cc0, KD)) =
+          make_uint4(qtp[i2][0], qtp[i2][1], qtp[i2][2], qtp[i2][3]);
+      *reinterpret_cast<uint4 *>(gi + I_KHT + mn_off(cc0, r, C)) =
+          make_uint4(khp[i2][0], khp[i2][1], khp[i2][2], khp[i2][3]);
+    }
+    fence_proxy_async();
     if (has_next) {
       tma_inflight = true;
       tma_pending = tma_phase;
@@ -523,12 +549,13 @@ __global__ void __launch_bounds__(PT, 1)
             for (int i = 0; i < 8; ++i) { a[i] = vv[i]; c8[i] = vv[8 + i]; }
             st_g16(gi, I_WQ + op_off(r, 16 * pc, KD), a);
             st_g16(gi, I_WQ + op_off(r, 16 * pc + 8, KD), c8);
-          } else {  // u columns 16 (pc - 8) ..
+          } else {  // u columns 16 (pc - 8) .., bf16
             const int col = 16 * (pc - 8), vt = col >> 5, cv = col & 31;
-            float4 *dst = reinterpret_cast<float4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 4);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_float4(vv[4 * q4], vv[4 * q4 + 1], vv[4 * q4 + 2], vv[4 * q4 + 3]);
+            uint4 *dst = reinterpret_cast<uint4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 2);
+            dst[0] = make_uint4(pack_bf16(vv[0], vv[1]), pack_bf16(vv[2], vv[3]),
+                                pack_bf16(vv[4], vv[5]), pack_bf16(vv[6], vv[7]));
+            dst[1] = make_uint4(pack_bf16(vv[8], vv[9]), pack_bf16(vv[10], vv[11]),
+                                pack_bf16(vv[12], vv[13]), pack_bf16(vv[14], vv[15]));
           }
         }
       }
@@ -558,8 +585,8 @@ done:
 constexpr int RT = 128;
 // One stage: [w ; Q e^G] | [T ; A_qk] | K^T (one 64 KiB copy), this unit's
 // u tile (64 x 32 fp32), e^{G_C}.
-constexpr uint32_t S_U = 65536, S_GAM = S_U + 8192, S_BYTES = S_GAM + 512;
-constexpr uint32_t R_STAGE = 74752;            // S_BYTES rounded to 1 KiB
+constexpr uint32_t S_U = 65536, S_GAM = S_U + 4096, S_BYTES = S_GAM + 512;
+constexpr uint32_t R_STAGE = 70656;            // S_BYTES rounded to 1 KiB
 constexpr uint32_t R_ST = 2 * R_STAGE;         // S^T MN-major 32 x Kd 128
 constexpr uint32_t R_UT = R_ST + 8192;         // U^T MN-major 32 x Kd 64
 constexpr uint32_t R_BAR = R_UT + 4096;        // stage0, stage1, mma
@@ -609,7 +636,7 @@ __global__ void __launch_bounds__(RT, 1)
     const uint32_t bar = bar0 + 8u * (uint32_t)s;
     mbar_expect_tx(bar, S_BYTES);
     bulk_load(dst, src, S_U, bar);
-    bulk_load(dst + S_U, src + I_U + (size_t)vt * 8192, 8192, bar);
+    bulk_load(dst + S_U, src + I_U + (size_t)vt * 4096, 4096, bar);
     bulk_load(dst + S_GAM, src + I_GAM, 512, bar);
   };
 
@@ -691,11 +718,10 @@ __global__ void __launch_bounds__(RT, 1)
         const int r = L;
         float v0[16], v1[16];
         tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
-        const float4 *up = reinterpret_cast<const float4 *>(stg + S_U + (size_t)r * VT * 4);
 #pragma unroll
         for (int vg = 0; vg < VT / 8; ++vg) {
-          const float4 u0 = up[2 * vg], u1 = up[2 * vg + 1];
-          const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          float uu[8];
+          ld_bf16x8(stg + S_U + (size_t)r * VT * 2 + vg * 16, uu);
           float a[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {

@@ -10,7 +10,8 @@
 //   G      = cumsum of g (per channel); block decays D_b = e^{E_b - P_b}
 //   X      = [K e1 ; Q e1]                       (128 x 128, A operand)
 //   Y_b    = K_{0..16b+15} * e^{P_b - G}         (B operands, one per block)
-//   D_b    = X Y_b^T  -> rows of block b: A_kk (k rows), A_qk (q rows)
+//   D      = X [Y_0 ; Y_1 ; Y_2 ; Y_3]^T (one MMA, N = 160) -> rows of block
+//            b against Y_b: A_kk (k rows), A_qk (q rows)
 //   T      = (I + beta * strict(A_kk))^-1        (fp32, blocked, CUDA cores)
 //   [w|u]  = [T ; A_qk] [beta K e^{G} | beta V]  (one MMA, N = 160)
 //   D1     = [w ; Q e^{G}] S0                    (M = 128: w S0 and Q e^G S0)
@@ -88,15 +89,15 @@ __device__ __forceinline__ uint32_t y_off(int b) {
 }
 
 // ---- TMEM column map (512 columns allocated) ------------------------------
-constexpr uint32_t TM_A0 = 0, TM_A1 = 32, TM_A2 = 64, TM_A3 = 128;
 constexpr uint32_t TM_TX = 192;  // 160 columns: [w | u]
 constexpr uint32_t TM_D1 = 352;  // 32 columns
 constexpr uint32_t TM_D2 = 384;  // 32 columns
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(TM_D2 + 32 <= TMEM_COLS, "TMEM map fits");
-__device__ __forceinline__ uint32_t tm_a(int b) {
-  return b == 0 ? TM_A0 : b == 1 ? TM_A1 : b == 2 ? TM_A2 : TM_A3;
-}
+// Y_0..Y_3 are stored back to back, so together they form one 160-row B
+// operand: a single N = 160 MMA gives X Y_b^T for every b, block b at TMEM
+// columns 8 b (b + 1) ... 8 b (b + 1) + 16 (b + 1) - 1 (below TM_TX).
+__device__ __forceinline__ uint32_t tm_a(int b) { return 8u * (uint32_t)(b * (b + 1)); }
 
 // Which 16-column pieces of the intra-chunk products each TMEM lane quadrant
 // reads: quadrants 0/2 hold rows 0..31 (blocks 0, 1), 1/3 rows 32..63.
@@ -345,9 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P2: intra-chunk products on the tensor cores; next TMA ----
       if (tid == 0) {
         tc_fence_after();
-#pragma unroll
-        for (int b = 0; b < kNumSub; ++b)
-          mma_group(tmem + tm_a(b), sb + X_OFF, sb + y_off(b), KD, 16 * (b + 1), false, 0, 0);
+        mma_group(tmem, sb + X_OFF, sb + Y_OFF, KD, 160, false, 0, 0);
         mma_commit(mma_bar);
         if (has_next) {
           const int y = (int)(tok0 + C);
