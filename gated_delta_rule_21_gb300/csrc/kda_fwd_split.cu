@@ -582,9 +582,11 @@ done:
 }
 
 // ---- recurrence kernel --------------------------------------------------------
-constexpr int RT = 128;
+// 256 threads: two warps per TMEM lane quadrant, each owning 16 of the 32
+// value columns (warp w: quadrant w % 4, columns 16 (w / 4) ..).
+constexpr int RT = 256;
 // One stage: [w ; Q e^G] | [T ; A_qk] | K^T (one 64 KiB copy), this unit's
-// u tile (64 x 32 fp32), e^{G_C}.
+// u tile (64 x 32 bf16), e^{G_C}.
 constexpr uint32_t S_U = 65536, S_GAM = S_U + 4096, S_BYTES = S_GAM + 512;
 constexpr uint32_t R_STAGE = 70656;            // S_BYTES rounded to 1 KiB
 constexpr uint32_t R_ST = 2 * R_STAGE;         // S^T MN-major 32 x Kd 128
@@ -596,6 +598,9 @@ constexpr uint32_t R_SMEM = R_ABORT + 12;
 constexpr uint32_t R_ALLOC = R_SMEM + 1024;
 static_assert(S_BYTES <= R_STAGE && I_KHT + 16384 == S_U, "stage layout");
 static_assert(R_ALLOC <= 232448, "rec smem fits");
+// TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
+// while the first MMA of chunk n + 1 runs; D2 single.
+constexpr uint32_t R_TM_D1 = 0, R_TM_D2 = 64, R_TM_COLS = 128;
 
 __global__ void __launch_bounds__(RT, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
@@ -605,11 +610,13 @@ __global__ void __launch_bounds__(RT, 1)
   const uint32_t sb = smem_u32(smem);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + R_ABORT);
   const uint32_t bar0 = sb + R_BAR, mma_bar = sb + R_BAR + 16;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int L = tid;  // 4 warps = the 4 TMEM lane quadrants
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int L = 32 * quad + lane;   // TMEM lane: chunk row (0..63) / o row / key row
+  const int col0 = 16 * half;       // this thread's 16 value columns within the tile
   const int H = p.H, T = p.T;
 
-  if (warp == 0) tmem_alloc(sb + R_SLOT, 64);
+  if (warp == 0) tmem_alloc(sb + R_SLOT, R_TM_COLS);
   if (tid == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8, 1);
@@ -621,8 +628,7 @@ __global__ void __launch_bounds__(RT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + R_SLOT);
-  const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
-  const uint32_t TM_D1 = 0, TM_D2 = 32;
+  const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
   uint32_t st_phase[2] = {0u, 0u}, mma_phase = 0;
   uint32_t st_issued = 0;  // per-stage bit: copy issued and not yet waited
   bool mma_inflight = false;
@@ -639,8 +645,20 @@ __global__ void __launch_bounds__(RT, 1)
     bulk_load(dst + S_U, src + I_U + (size_t)vt * 4096, 4096, bar);
     bulk_load(dst + S_GAM, src + I_GAM, 512, bar);
   };
+  auto wait_stage = [&](int s) {
+    if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
+    else st_issued &= ~(1u << s);
+    st_phase[s] ^= 1u;
+  };
+  auto wait_mma = [&]() {
+    mma_inflight = true;
+    mma_pending = mma_phase;
+    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+    else mma_inflight = false;
+    mma_phase ^= 1u;
+  };
 
-  float S[VT];
+  float S[16];  // S[key row L][col0 .. col0 + 15], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
   const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
@@ -654,26 +672,26 @@ __global__ void __launch_bounds__(RT, 1)
     auto item_ptr = [&](int c) {
       return items + ((size_t)(cbase + c) * H + h) * ITEM_BYTES;
     };
-    {
-      const int c = tid;
+    {  // state entering the run; S^T operand (MN-major: v contiguous)
+      const int c = L;
       if (u.first && p.initial_state) {
         const float4 *src = reinterpret_cast<const float4 *>(
-            p.initial_state + (((size_t)b * H + h) * KD + c) * p.V + vc0);
+            p.initial_state + (((size_t)b * H + h) * KD + c) * p.V + vc0 + col0);
 #pragma unroll
-        for (int q4 = 0; q4 < VT / 4; ++q4) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           const float4 x = src[q4];
           S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < VT; ++i) S[i] = 0.f;
+        for (int i = 0; i < 16; ++i) S[i] = 0.f;
       }
 #pragma unroll
-      for (int vg = 0; vg < VT / 8; ++vg) {
+      for (int e = 0; e < 2; ++e) {
         float t8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
-        st_bf16x8(smem, R_ST + mn_off(8 * vg, c, KD), t8);
+        for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
+        st_bf16x8(smem, R_ST + mn_off(col0 + 8 * e, c, KD), t8);
       }
     }
     if (tid == 0) {
@@ -682,7 +700,16 @@ __global__ void __launch_bounds__(RT, 1)
     }
     st_issued = n_chunks > 1 ? 3u : 1u;
     fence_proxy_async();
+    wait_stage(0);
+    tc_fence_before();
     __syncthreads();
+    if (*sAbort) goto done;
+    // ---- P11: D1[0] = [w ; Q e^G] S for chunk 0
+    if (tid == 0) {
+      tc_fence_after();
+      mma_group(tmem + R_TM_D1, sb + I_WQ, sb + R_ST, KD, VT, false, 0, 1);
+      mma_commit(mma_bar);
+    }
 
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c & 1;
@@ -691,44 +718,25 @@ __global__ void __launch_bounds__(RT, 1)
       const size_t tok0 = (size_t)b * T + t0;
       const unsigned char *stg = smem + (uint32_t)s * R_STAGE;
       const uint32_t sstg = sb + (uint32_t)s * R_STAGE;
-      // ---- P10: wait for the stage
-      if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
-      else st_issued &= ~(1u << s);
-      st_phase[s] ^= 1u;
-      __syncthreads();
-      if (*sAbort) goto done;
-
-      // ---- P11: D1 = [w ; Q e^G] S
-      if (tid == 0) {
-        tc_fence_after();
-        mma_group(tmem + TM_D1, sstg + I_WQ, sb + R_ST, KD, VT, false, 0, 1);
-        mma_commit(mma_bar);
-      }
-      mma_inflight = true;
-      mma_pending = mma_phase;
-      if (!mbar_wait(mma_bar, mma_phase)) abort_all();
-      else mma_inflight = false;
-      mma_phase ^= 1u;
+      const uint32_t d1 = R_TM_D1 + 32u * (uint32_t)s;
+      // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk
+      wait_mma();
       __syncthreads();
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // ---- P12: U = u - w S  (lanes 0..63)
-      if (warp < 2) {
+      // ---- P12: U = u - w S (lanes 0..63), 16 columns per thread
+      if (quad < 2) {
         const int r = L;
-        float v0[16], v1[16];
-        tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
+        float v[16];
+        tmem_ld16(tq + d1 + col0, v);
 #pragma unroll
-        for (int vg = 0; vg < VT / 8; ++vg) {
-          float uu[8];
-          ld_bf16x8(stg + S_U + (size_t)r * VT * 2 + vg * 16, uu);
-          float a[8];
+        for (int e = 0; e < 2; ++e) {
+          float uu[8], a[8];
+          ld_bf16x8(stg + S_U + (size_t)r * VT * 2 + (col0 + 8 * e) * 2, uu);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = 8 * vg + i;
-            a[i] = uu[i] - (col < 16 ? v0[col & 15] : v1[col & 15]);
-          }
-          st_bf16x8(smem, R_UT + mn_off(8 * vg, r, C), a);
+          for (int i = 0; i < 8; ++i) a[i] = uu[i] - v[8 * e + i];
+          st_bf16x8(smem, R_UT + mn_off(col0 + 8 * e, r, C), a);
         }
       }
       fence_proxy_async();
@@ -738,60 +746,29 @@ __global__ void __launch_bounds__(RT, 1)
       // ---- P13: D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + TM_D1, sstg + I_TAQ, sb + R_UT, C, VT, true, 0, 1);
-        mma_group(tmem + TM_D2, sstg + I_KHT, sb + R_UT, C, VT, false, 1, 1);
+        mma_group(tmem + d1, sstg + I_TAQ, sb + R_UT, C, VT, true, 0, 1);
+        mma_group(tmem + R_TM_D2, sstg + I_KHT, sb + R_UT, C, VT, false, 1, 1);
         mma_commit(mma_bar);
       }
-      mma_inflight = true;
-      mma_pending = mma_phase;
-      if (!mbar_wait(mma_bar, mma_phase)) abort_all();
-      else mma_inflight = false;
-      mma_phase ^= 1u;
+      wait_mma();
       __syncthreads();
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // ---- P14: o rows (lanes 64..127); state update (all lanes = key rows)
-      if (warp >= 2) {
-        const int r = L - 64;
-        float v0[16], v1[16];
-        tmem_ld16x2(tq + TM_D1, tq + TM_D1 + 16, v0, v1);
-        if (r < n) {
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0);
-#pragma unroll
-          for (int q4 = 0; q4 < VT / 8; ++q4) {
-            float o[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int col = 8 * q4 + i;
-              o[i] = p.scale * (col < 16 ? v0[col & 15] : v1[col & 15]);
-            }
-            uint4 w;
-            w.x = pack_bf16(o[0], o[1]);
-            w.y = pack_bf16(o[2], o[3]);
-            w.z = pack_bf16(o[4], o[5]);
-            w.w = pack_bf16(o[6], o[7]);
-            dst[q4] = w;
-          }
-        }
-      }
+      // ---- P14: state update (all lanes = key rows), next chunk's first MMA
       {
         const int cidx = L;
         const float gam = reinterpret_cast<const float *>(stg + S_GAM)[cidx];
-        float v0[16], v1[16];
-        tmem_ld16x2(tq + TM_D2, tq + TM_D2 + 16, v0, v1);
+        float v[16];
+        tmem_ld16(tq + R_TM_D2 + col0, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          S[i] = fmaf(gam, S[i], v0[i]);
-          S[16 + i] = fmaf(gam, S[16 + i], v1[i]);
-        }
+        for (int i = 0; i < 16; ++i) S[i] = fmaf(gam, S[i], v[i]);
 #pragma unroll
-        for (int vg = 0; vg < VT / 8; ++vg) {
+        for (int e = 0; e < 2; ++e) {
           float t8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t8[i] = S[8 * vg + i];
-          st_bf16x8(smem, R_ST + mn_off(8 * vg, cidx, KD), t8);
+          for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
+          st_bf16x8(smem, R_ST + mn_off(col0 + 8 * e, cidx, KD), t8);
         }
       }
       fence_proxy_async();
@@ -801,12 +778,41 @@ __global__ void __launch_bounds__(RT, 1)
         if (tid == 0) issue_stage(s, item_ptr(c + 2), vt);
         st_issued |= 1u << s;
       }
+      if (c + 1 < n_chunks) {
+        wait_stage(s ^ 1);
+        if (tid == 0) {
+          tc_fence_after();
+          mma_group(tmem + R_TM_D1 + 32u * (uint32_t)(s ^ 1), sb + (uint32_t)(s ^ 1) * R_STAGE + I_WQ,
+                    sb + R_ST, KD, VT, false, 0, 1);
+          mma_commit(mma_bar);
+        }
+      }
+      // o rows of this chunk (lanes 64..127) while the next MMA runs
+      if (quad >= 2) {
+        const int r = L - 64;
+        float v[16];
+        tmem_ld16(tq + d1 + col0, v);
+        if (r < n) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0 + col0);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint4 w;
+            w.x = pack_bf16(p.scale * v[8 * e + 0], p.scale * v[8 * e + 1]);
+            w.y = pack_bf16(p.scale * v[8 * e + 2], p.scale * v[8 * e + 3]);
+            w.z = pack_bf16(p.scale * v[8 * e + 4], p.scale * v[8 * e + 5]);
+            w.w = pack_bf16(p.scale * v[8 * e + 6], p.scale * v[8 * e + 7]);
+            dst[e] = w;
+          }
+        }
+      }
+      tc_fence_before();
     }
     if (u.last && p.final_state) {
       float4 *dst = reinterpret_cast<float4 *>(
-          p.final_state + (((size_t)b * H + h) * KD + tid) * p.V + vc0);
+          p.final_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0);
 #pragma unroll
-      for (int q4 = 0; q4 < VT / 4; ++q4)
+      for (int q4 = 0; q4 < 4; ++q4)
         dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
     }
     __syncthreads();
@@ -820,7 +826,7 @@ done:
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, R_TM_COLS);
   }
 }
 
