@@ -5,27 +5,29 @@
 //      Per item (64 tokens of one head) it builds the gate cumsum and decay
 //      factors, the intra-chunk products A_kk / A_qk on tcgen05 (one MMA per
 //      16-row block), the triangular inverse T = (I + beta A_kk)^-1 (fp32,
-//      blocked), and [w | u] = T [beta K e^G | beta V] on tcgen05, and writes
-//      the operands the recurrence needs into the workspace, already in the
-//      shared-memory layouts the tensor cores read:
-//         [w ; Q e^G] (128 x 128 bf16), [T ; A_qk] (128 x 64 bf16),
+//      blocked), and [w | u] = T diag(beta) [K e^G | V] on tcgen05, and
+//      writes the operands the recurrence needs into the workspace, already
+//      in the shared-memory layouts the tensor cores read:
+//         [w ; Q e^G] (128 x 128 bf16), A_qk (64 x 64 bf16),
 //         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 bf16), e^{G_C}.
 //   2. fwd_rec_kernel: one CTA per (row, head, 32-column value tile) walks
 //      the chunks in order with the fp32 state in registers; per chunk it
 //      bulk-copies the item (double-buffered) and runs only the
 //      state-dependent MMAs:  D1 = [w ; Q e^G] S,  U = u - w S,
-//      D1 += [T ; A_qk] U,  D2 = (K e^{G_C-G})^T U,  S <- e^{G_C} S + D2,
+//      D1 += [0 ; A_qk] U,  D2 = (K e^{G_C-G})^T U,  S <- e^{G_C} S + D2,
 //      o = scale * D1[64:128].
 //
 // The arithmetic is the same chunk form, sub-block factors and rounding
 // points as the fused kernel (kda_fwd_tc.cu); see there for the algebra.
-// This path needs a workspace of split_workspace_bytes() (about 81 KB per
+// This path needs a workspace of split_workspace_bytes() (about 73 KB per
 // chunk and head).  With segment ids the chunks are those of each run (a
 // run's last chunk may be short), sized for a caller bound on runs per row;
 // the kernels check the real chunk count and report KDA_DEVICE_WORKSPACE
 // (doing nothing else) when it does not fit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "kda_internal.cuh"
 #include "kda_tc_common.cuh"
@@ -41,27 +43,31 @@ constexpr int VT = 32;
 
 // ---- one workspace item (per row, chunk, head) ----------------------------
 constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: K-major, 128 rows, Kd 128
-constexpr uint32_t I_TAQ = 32768;     // [T ; A_qk]: K-major, 128 rows, Kd 64
-constexpr uint32_t I_KHT = 49152;     // (K e^{G_C-G})^T: MN-major, 128 x Kd 64
-constexpr uint32_t I_U = 65536;       // u bf16 [vt][r][32]
-constexpr uint32_t I_GAM = 81920;     // e^{G_C} fp32 [128]
-constexpr uint32_t ITEM_BYTES = 82944;     // 81 KiB, 1 KiB aligned
+constexpr uint32_t I_AQK = 32768;     // A_qk: K-major, 64 rows, Kd 64
+constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: MN-major, 128 x Kd 64
+constexpr uint32_t I_U = 57344;       // u bf16 [vt][r][32]
+constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
+constexpr uint32_t ITEM_BYTES = 74240;     // 72.5 KiB, 256-byte aligned
 constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
 
 // ---- prep kernel shared memory ----------------------------------------------
 constexpr int PT = 512;                       // threads
+// Raw q / k tiles: two 64-column halves, g: four 32-column quarters, each
+// 64 rows of 128 bytes with the TMA 128-byte swizzle (16-byte unit u of row
+// r stored at unit u ^ (r % 8)), so that row- and column-wise reads are both
+// free of bank conflicts.  v goes straight into the V part of RHST.
 constexpr uint32_t P_RAW_Q = 0, P_RAW_K = 16384, P_RAW_G = 32768;
-constexpr uint32_t P_RAW_V = 65536;           // 64 x 128 bf16, 256-byte rows
-constexpr uint32_t P_RAW_TX = 16384 * 2 + 32768 + 16384;
-constexpr uint32_t P_X = 81920;               // 128 x Kd 128
+constexpr uint32_t P_RAW_TX = 16384 * 2 + 32768;
+constexpr uint32_t P_V_TX = 16384;
+constexpr uint32_t P_X = 65536;               // 128 x Kd 128
 constexpr uint32_t P_Y = P_X + 32768;         // Y_0..Y_3, 160 rows x Kd 128
 constexpr uint32_t P_RHST = P_Y + 40960;      // [beta K e^G | beta V]^T MN-major 256 x 64
 constexpr uint32_t P_MISC = P_RHST + 32768;
 constexpr uint32_t P_BETA = P_MISC;           // 64 fp32
 constexpr uint32_t P_DBLK = P_MISC + 256;     // 4 x 128 fp32
 constexpr uint32_t P_BSUM = P_DBLK + 2048;    // 4 x 128 fp32 block sums of g
-constexpr uint32_t P_BAR = P_BSUM + 2048;     // tma, mma
-constexpr uint32_t P_SLOT = P_BAR + 16;
+constexpr uint32_t P_BAR = P_BSUM + 2048;     // tma, mma, v
+constexpr uint32_t P_SLOT = P_BAR + 24;
 constexpr uint32_t P_ABORT = P_SLOT + 4;
 constexpr uint32_t P_SMEM = P_ABORT + 12;
 constexpr uint32_t P_ALLOC = P_SMEM + 1024;
@@ -69,10 +75,25 @@ constexpr int LDF = C + 4;
 constexpr uint32_t P_AKK = P_X;                    // fp32 64 x 68
 constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68
 constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T bf16 K-major (128-row operand)
-constexpr uint32_t P_SCR = P_TB + 16384;           // 3 x 256 fp32
-static_assert(P_SCR + 3072 <= P_RHST, "prep aliases inside X / Y");
+constexpr uint32_t P_SCR = P_TB + 16384;           // 10 blocks of 16 x LDS fp32
+constexpr int LDS = 20;                            // padded: conflict-free rows
+static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_RHST, "prep aliases inside X / Y");
 static_assert(P_ALLOC <= 232448, "prep smem fits");
 constexpr uint32_t P_TM_TX = 256;  // TMEM: X Y^T at 0..159, [w | u] at 256
+
+// Byte offsets of element (row r, column c) in the swizzled raw tiles.
+__device__ __forceinline__ uint32_t kq_off(int r, int c) {
+  return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+__device__ __forceinline__ uint32_t g_off(int r, int c) {
+  return (uint32_t)((c >> 5) * 8192 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
+}
+__device__ __forceinline__ void ld_f32x8(const unsigned char *tile, int r, int c8, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(tile + g_off(r, c8));
+  const float4 b = *reinterpret_cast<const float4 *>(tile + g_off(r, c8 + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
 __device__ __forceinline__ uint32_t p_y_off(int b) {
   return P_Y + 256u * (uint32_t)(8 * b * (b + 1));
@@ -144,6 +165,33 @@ __device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const flo
   *reinterpret_cast<uint4 *>(g + off) = w;
 }
 
+// One 16 x 16 block product on the CUDA cores, 64 threads (e = 0..63, one
+// row and four columns each): dst = sgn X Y + add_sgn add  (add optional).
+__device__ __forceinline__ void blk_prod(float *dst, int ldd, const float *X, int ldx,
+                                         const float *Y, int ldy, float sgn, const float *add,
+                                         int lda, int e, float add_sgn = -1.f) {
+  const int r = e >> 2, c4 = (e & 3) * 4;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const float x = X[r * ldx + t];
+    const float4 y = *reinterpret_cast<const float4 *>(Y + t * ldy + c4);
+    a0 = fmaf(x, y.x, a0);
+    a1 = fmaf(x, y.y, a1);
+    a2 = fmaf(x, y.z, a2);
+    a3 = fmaf(x, y.w, a3);
+  }
+  float4 o = make_float4(sgn * a0, sgn * a1, sgn * a2, sgn * a3);
+  if (add) {
+    const float4 z = *reinterpret_cast<const float4 *>(add + r * lda + c4);
+    o.x = fmaf(add_sgn, z.x, o.x);
+    o.y = fmaf(add_sgn, z.y, o.y);
+    o.z = fmaf(add_sgn, z.z, o.z);
+    o.w = fmaf(add_sgn, z.w, o.w);
+  }
+  *reinterpret_cast<float4 *>(dst + r * ldd + c4) = o;
+}
+
 __global__ void __launch_bounds__(PT, 1)
     fwd_prep_kernel(const FwdParams p, unsigned char *items, const ChunkTable ct,
                     const __grid_constant__ CUtensorMap tm_q,
@@ -157,12 +205,11 @@ __global__ void __launch_bounds__(PT, 1)
   float *sBeta = reinterpret_cast<float *>(smem + P_BETA);
   float *sDblk = reinterpret_cast<float *>(smem + P_DBLK);
   float *sBsum = reinterpret_cast<float *>(smem + P_BSUM);
-  float *sG = reinterpret_cast<float *>(smem + P_RAW_G);
   float *sAkk = reinterpret_cast<float *>(smem + P_AKK);
   float *sT = reinterpret_cast<float *>(smem + P_TF);
   float *sScr = reinterpret_cast<float *>(smem + P_SCR);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + P_ABORT);
-  const uint32_t tma_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8;
+  const uint32_t tma_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8, v_bar = sb + P_BAR + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, sub = warp >> 2;  // 4 warps per TMEM lane quadrant
   const int L = 32 * quad + lane;
@@ -172,6 +219,7 @@ __global__ void __launch_bounds__(PT, 1)
   if (tid == 0) {
     mbar_init(tma_bar, 1);
     mbar_init(mma_bar, 1);
+    mbar_init(v_bar, 1);
     *sAbort = 0u;
     fence_mbar_init();
   }
@@ -180,8 +228,9 @@ __global__ void __launch_bounds__(PT, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P_SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
-  uint32_t tma_phase = 0, mma_phase = 0, tma_pending = 0, mma_pending = 0;
-  bool tma_inflight = false, mma_inflight = false;
+  uint32_t tma_phase = 0, mma_phase = 0, v_phase = 0, tma_pending = 0, mma_pending = 0,
+           v_pending = 0;
+  bool tma_inflight = false, mma_inflight = false, v_inflight = false;
   auto abort_all = [&]() {
     *sAbort = 1u;
     set_status(p.status, KDA_DEVICE_TIMEOUT);
@@ -195,15 +244,31 @@ __global__ void __launch_bounds__(PT, 1)
     h = (int)(it % (uint32_t)H);
     chunk_of(ct, p.runs, p.B, T, it / (uint32_t)H, b, t0, end);
   };
+  // Both issue functions are called by all 32 lanes of one warp: lane 0
+  // arms the barrier, then one box per lane.
   auto issue_tma = [&](uint32_t it) {
     int b, t0, end, h;
     item_coords(it, b, t0, end, h);
     const int y = b * T + t0;
-    mbar_expect_tx(tma_bar, P_RAW_TX);
-    tma_load_2d(sb + P_RAW_Q, &tm_q, h * KD, y, tma_bar);
-    tma_load_2d(sb + P_RAW_K, &tm_k, h * KD, y, tma_bar);
-    tma_load_2d(sb + P_RAW_G, &tm_g, h * KD, y, tma_bar);
-    tma_load_2d(sb + P_RAW_V, &tm_v, h * VD, y, tma_bar);
+    if (lane == 0) mbar_expect_tx(tma_bar, P_RAW_TX);
+    __syncwarp();
+    if (lane < 2)
+      tma_load_2d(sb + P_RAW_Q + 8192 * lane, &tm_q, h * KD + 64 * lane, y, tma_bar);
+    else if (lane < 4)
+      tma_load_2d(sb + P_RAW_K + 8192 * (lane - 2), &tm_k, h * KD + 64 * (lane - 2), y, tma_bar);
+    else if (lane < 8)
+      tma_load_2d(sb + P_RAW_G + 8192 * (lane - 4), &tm_g, h * KD + 32 * (lane - 4), y, tma_bar);
+  };
+  // v as 16 column groups of 8, each 64 rows x 16 bytes: the MN-major layout
+  // of the V part of RHST (read by the [w | u] MMA).
+  auto issue_v = [&](uint32_t it) {
+    int b, t0, end, h;
+    item_coords(it, b, t0, end, h);
+    const int y = b * T + t0;
+    if (lane == 0) mbar_expect_tx(v_bar, P_V_TX);
+    __syncwarp();
+    if (lane < VD / 8)
+      tma_load_2d(sb + P_RHST + mn_off(KD + 8 * lane, 0, C), &tm_v, h * VD + 8 * lane, y, v_bar);
   };
   auto load_beta = [&](uint32_t it) -> float {
     int b, t0, end, h;
@@ -215,9 +280,11 @@ __global__ void __launch_bounds__(PT, 1)
   uint32_t item = blockIdx.x;
   float beta_next = 0.f;
   if (item < n_items) {
-    if (tid == 0) issue_tma(item);
-    tma_inflight = true;
+    if (warp == 0) issue_tma(item);
+    if (warp == 1) issue_v(item);
+    tma_inflight = v_inflight = true;
     tma_pending = tma_phase;
+    v_pending = v_phase;
     if (tid < C) beta_next = load_beta(item);
   }
   for (; item < n_items; item += gridDim.x) {
@@ -238,11 +305,12 @@ __global__ void __launch_bounds__(PT, 1)
     // ---- P0: gate cumsum, one thread per (channel, 16-row block) ----
     {
       const int c = tid & 127, q4 = tid >> 7;
+      unsigned char *graw = smem + P_RAW_G;
       float v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = 16 * q4 + i;
-        v[i] = r < n ? sG[r * KD + c] : 0.f;
+        v[i] = r < n ? *reinterpret_cast<const float *>(graw + g_off(r, c)) : 0.f;
       }
 #pragma unroll
       for (int i = 1; i < 16; ++i) v[i] += v[i - 1];
@@ -252,108 +320,109 @@ __global__ void __launch_bounds__(PT, 1)
       float off = 0.f;
       for (int i = 0; i < q4; ++i) off += sBsum[i * KD + c];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sG[(16 * q4 + i) * KD + c] = v[i] + off;
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float *>(graw + g_off(16 * q4 + i, c)) = v[i] + off;
     }
     __syncthreads();
 
     // ---- P1: operands X, Y_b (the intra-chunk MMA inputs) first ----
-    // Thread -> 8 channels of 2 rows of one 16-row block (warp-uniform
-    // block), so the per-channel block factors are built once per thread.
+    // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform,
+    // and a compile-time constant inside build_rows), so the per-channel
+    // block factors are built once per thread and only those block b needs.
     uint32_t kbp[2][4], qtp[2][4], khp[2][4];  // bf16 pairs stored after the MMA issue
     const int rl = tid & 7, cg = (tid >> 3) & 15, b = tid >> 7;
     const int cc0 = cg * 8;
     {
-      float pre[8], suf[8], rD[8], x2[8], x3[8], Pl[8], El[8];
-      {
-        float D[kNumSub][8], Eb[8], Pb[8];
-#pragma unroll
-        for (int i = 0; i < kNumSub; ++i) {
-          const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
-          const float4 d0 = dp[0], d1 = dp[1];
-          D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
-          D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
-        }
-        const float4 *ep = reinterpret_cast<const float4 *>(sG + (b * kSub + kSub - 1) * KD + cc0);
-        const float4 e0 = ep[0], e1v = ep[1];
-        Eb[0] = e0.x; Eb[1] = e0.y; Eb[2] = e0.z; Eb[3] = e0.w;
-        Eb[4] = e1v.x; Eb[5] = e1v.y; Eb[6] = e1v.z; Eb[7] = e1v.w;
-        const float4 *pq = reinterpret_cast<const float4 *>(sG + (b > 0 ? b * kSub - 1 : 0) * KD + cc0);
-        const float4 p0 = pq[0], p1 = pq[1];
-        const float z = b > 0 ? 1.f : 0.f;
-        Pb[0] = z * p0.x; Pb[1] = z * p0.y; Pb[2] = z * p0.z; Pb[3] = z * p0.w;
-        Pb[4] = z * p1.x; Pb[5] = z * p1.y; Pb[6] = z * p1.z; Pb[7] = z * p1.w;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float a = 1.f, zz = 1.f, Db = 1.f, c2 = 1.f, c3 = 1.f;
+      auto build_rows = [&](auto bconst) {
+        constexpr int BB = decltype(bconst)::value;
+        float pre[8], suf[8], rD[8], x2[8], x3[8], Pl[8], El[8];
+        {
+          float D[kNumSub][8];
 #pragma unroll
           for (int i = 0; i < kNumSub; ++i) {
-            const float Di = D[i][j];
-            if (i < b) a *= Di;
-            if (i > b) zz *= Di;
-            if (i == b) Db = Di;
-            if (i == b + 1) { c2 *= Di; c3 *= Di; }
-            if (i == b + 2) c3 *= Di;
+            const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
+            const float4 d0 = dp[0], d1 = dp[1];
+            D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
+            D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
           }
-          pre[j] = a; suf[j] = zz; rD[j] = __frcp_rn(Db); x2[j] = c2; x3[j] = c3;
-          Pl[j] = Pb[j] * kLog2e;
-          El[j] = Eb[j] * kLog2e;
+          float Eb[8], Pb[8];
+          ld_f32x8(smem + P_RAW_G, BB * kSub + kSub - 1, cc0, Eb);
+          if (BB > 0) ld_f32x8(smem + P_RAW_G, BB * kSub - 1, cc0, Pb);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float a = 1.f, zz = 1.f, c2 = 1.f, c3 = 1.f;
+#pragma unroll
+            for (int i = 0; i < kNumSub; ++i) {
+              if (i < BB) a *= D[i][j];
+              if (i > BB) zz *= D[i][j];
+            }
+            if (BB + 2 < kNumSub) { c2 = D[BB + 1][j]; c3 = c2; }
+            if (BB + 3 < kNumSub) c3 *= D[BB + 2][j];
+            pre[j] = a; suf[j] = zz; rD[j] = __frcp_rn(D[BB][j]); x2[j] = c2; x3[j] = c3;
+            Pl[j] = BB > 0 ? Pb[j] * kLog2e : 0.f;
+            El[j] = Eb[j] * kLog2e;
+          }
         }
-      }
 #pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int r = kSub * b + 8 * i2 + rl;
-        const bool valid = r < n;
-        const float br = sBeta[r];
-        float kk[8], qq[8], G[8];
-        ld_bf16x8(smem + P_RAW_K + r * 256 + cc0 * 2, kk);
-        ld_bf16x8(smem + P_RAW_Q + r * 256 + cc0 * 2, qq);
-        {
-          const float4 *gp = reinterpret_cast<const float4 *>(sG + r * KD + cc0);
-          const float4 g0 = gp[0], g1 = gp[1];
-          G[0] = g0.x; G[1] = g0.y; G[2] = g0.z; G[3] = g0.w;
-          G[4] = g1.x; G[5] = g1.y; G[6] = g1.z; G[7] = g1.w;
+        for (int i2 = 0; i2 < 2; ++i2) {
+          const int r = kSub * BB + 8 * i2 + rl;
+          const bool valid = r < n;
+          float kk[8], qq[8], G[8];
+          ld_bf16x8(smem + P_RAW_K + kq_off(r, cc0), kk);
+          ld_bf16x8(smem + P_RAW_Q + kq_off(r, cc0), qq);
+          ld_f32x8(smem + P_RAW_G, r, cc0, G);
+          // Outputs are packed to bf16 pairs as they are computed: X rows r
+          // (k) and 64 + r (q), Y_b .. Y_3 rows r, and the pairs kept for
+          // after the MMA issue.
+          uint32_t pxk[4], pxq[4], pyd[4], py1[4], py2[4], py3[4];
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            float o_xk[2], o_xq[2], o_yd[2], o_y1[2], o_y2[2], o_y3[2], o_qt[2], o_kb[2], o_kh[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int j = 2 * q2 + t;
+              const float gl = G[j] * kLog2e;
+              const float e1 = ex2(gl - Pl[j]);  // e^{G - P_b}
+              const float e2 = ex2(El[j] - gl);  // e^{E_b - G}
+              const float kv = valid ? kk[j] : 0.f;
+              const float qv = valid ? qq[j] : 0.f;
+              const float xk = kv * e1, xq = qv * e1, ke2 = kv * e2;
+              o_xk[t] = xk;
+              o_xq[t] = xq;
+              o_qt[t] = BB > 0 ? xq * pre[j] : xq;
+              o_kb[t] = BB > 0 ? xk * pre[j] : xk;
+              o_kh[t] = BB + 1 < kNumSub ? ke2 * suf[j] : ke2;
+              o_yd[t] = ke2 * rD[j];
+              o_y1[t] = ke2;
+              o_y2[t] = ke2 * x2[j];
+              o_y3[t] = ke2 * x3[j];
+            }
+            pxk[q2] = pack_bf16(o_xk[0], o_xk[1]);
+            pxq[q2] = pack_bf16(o_xq[0], o_xq[1]);
+            pyd[q2] = pack_bf16(o_yd[0], o_yd[1]);
+            if (BB + 1 < kNumSub) py1[q2] = pack_bf16(o_y1[0], o_y1[1]);
+            if (BB + 2 < kNumSub) py2[q2] = pack_bf16(o_y2[0], o_y2[1]);
+            if (BB + 3 < kNumSub) py3[q2] = pack_bf16(o_y3[0], o_y3[1]);
+            kbp[i2][q2] = pack_bf16(o_kb[0], o_kb[1]);
+            qtp[i2][q2] = pack_bf16(o_qt[0], o_qt[1]);
+            khp[i2][q2] = pack_bf16(o_kh[0], o_kh[1]);
+          }
+          auto st4 = [&](uint32_t off, const uint32_t (&w)[4]) {
+            *reinterpret_cast<uint4 *>(smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          };
+          st4(P_X + op_off(r, cc0, KD), pxk);
+          st4(P_X + op_off(64 + r, cc0, KD), pxq);
+          st4(p_y_off(BB) + op_off(r, cc0, KD), pyd);
+          if (BB + 1 < kNumSub) st4(p_y_off(BB + 1) + op_off(r, cc0, KD), py1);
+          if (BB + 2 < kNumSub) st4(p_y_off(BB + 2) + op_off(r, cc0, KD), py2);
+          if (BB + 3 < kNumSub) st4(p_y_off(BB + 3) + op_off(r, cc0, KD), py3);
         }
-        float xk[8], xq[8], yd[8], y1[8], y2[8], y3[8], qt[8], kb[8], kh[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float gl = G[j] * kLog2e;
-          const float e1 = ex2(gl - Pl[j]);  // e^{G - P_b}
-          const float e2 = ex2(El[j] - gl);  // e^{E_b - G}
-          const float kv = valid ? kk[j] : 0.f;
-          const float qv = valid ? qq[j] : 0.f;
-          xk[j] = kv * e1;
-          xq[j] = qv * e1;
-          qt[j] = xq[j] * pre[j];
-          kb[j] = xk[j] * (br * pre[j]);
-          const float ke2 = kv * e2;
-          kh[j] = ke2 * suf[j];
-          yd[j] = ke2 * rD[j];
-          y1[j] = ke2;
-          y2[j] = ke2 * x2[j];
-          y3[j] = ke2 * x3[j];
-        }
-        st_bf16x8(smem, P_X + op_off(r, cc0, KD), xk);
-        st_bf16x8(smem, P_X + op_off(64 + r, cc0, KD), xq);
-        st_bf16x8(smem, p_y_off(b) + op_off(r, cc0, KD), yd);
-        if (b + 1 < kNumSub) st_bf16x8(smem, p_y_off(b + 1) + op_off(r, cc0, KD), y1);
-        if (b + 2 < kNumSub) st_bf16x8(smem, p_y_off(b + 2) + op_off(r, cc0, KD), y2);
-        if (b + 3 < kNumSub) st_bf16x8(smem, p_y_off(b + 3) + op_off(r, cc0, KD), y3);
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          kbp[i2][q2] = pack_bf16(kb[2 * q2], kb[2 * q2 + 1]);
-          qtp[i2][q2] = pack_bf16(qt[2 * q2], qt[2 * q2 + 1]);
-          khp[i2][q2] = pack_bf16(kh[2 * q2], kh[2 * q2 + 1]);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {  // (beta V)^T, read before the next tiles land
-        const int r = tid >> 3, vg = (tid & 7) + 8 * e;
-        float vv[8];
-        ld_bf16x8(smem + P_RAW_V + r * 256 + vg * 16, vv);
-        const float br = r < n ? sBeta[r] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vv[i] *= br;
-        st_bf16x8(smem, P_RHST + mn_off(KD + 8 * vg, r, C), vv);
+      };
+      switch (b) {
+        case 0: build_rows(std::integral_constant<int, 0>{}); break;
+        case 1: build_rows(std::integral_constant<int, 1>{}); break;
+        case 2: build_rows(std::integral_constant<int, 2>{}); break;
+        default: build_rows(std::integral_constant<int, 3>{}); break;
       }
     }
     fence_proxy_async();
@@ -366,8 +435,8 @@ __global__ void __launch_bounds__(PT, 1)
       tc_fence_after();
       mma_group(tmem, sb + P_X, sb + P_Y, KD, 160, false, 0, 0);
       mma_commit(mma_bar);
-      if (has_next) issue_tma(next);
     }
+    if (has_next && warp == 1) issue_tma(next);
 #pragma unroll
     for (int i2 = 0; i2 < 2; ++i2) {
       const int r = kSub * b + 8 * i2 + rl;
@@ -434,14 +503,14 @@ __global__ void __launch_bounds__(PT, 1)
               a0[i] = (j0 + i <= r) ? v[e][i] : 0.f;
               a1[i] = (j0 + 8 + i <= r) ? v[e][8 + i] : 0.f;
             }
-            st_g16(gi, I_TAQ + op_off(64 + r, j0, C), a0);
-            st_g16(gi, I_TAQ + op_off(64 + r, j0 + 8, C), a1);
+            st_g16(gi, I_AQK + op_off(r, j0, C), a0);
+            st_g16(gi, I_AQK + op_off(r, j0 + 8, C), a1);
           }
         }
       }
       if (is_q && sub == 0) {
         const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int jj = 16 * (bme + 1); jj < C; jj += 8) st_g16(gi, I_TAQ + op_off(64 + r, jj, C), z);
+        for (int jj = 16 * (bme + 1); jj < C; jj += 8) st_g16(gi, I_AQK + op_off(r, jj, C), z);
       }
     }
     tc_fence_before();
@@ -464,59 +533,70 @@ __global__ void __launch_bounds__(PT, 1)
       for (int rr = 0; rr < 16; ++rr) sT[(base + rr) * LDF + base + cc] = x[rr];
     }
     __syncthreads();
-    for (int d = 1; d < kNumSub; ++d) {
-      const int nblk = kNumSub - d;
-      const int blk = tid >> 6, e = tid & 63, ra = 2 * (e >> 3), cb = 2 * (e & 7);
-      const bool act = blk < nblk;
-      const int i = d + blk, j = blk;
-      if (act) {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        for (int m = j; m < i; ++m) {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float l0 = sAkk[(16 * i + ra) * LDF + 16 * m + t];
-            const float l1 = sAkk[(16 * i + ra + 1) * LDF + 16 * m + t];
-            const float2 tv = *reinterpret_cast<const float2 *>(sT + (16 * m + t) * LDF + 16 * j + cb);
-            a00 = fmaf(l0, tv.x, a00); a01 = fmaf(l0, tv.y, a01);
-            a10 = fmaf(l1, tv.x, a10); a11 = fmaf(l1, tv.y, a11);
-          }
-        }
-        float *mm = sScr + blk * 256;
-        *reinterpret_cast<float2 *>(mm + ra * 16 + cb) = make_float2(a00, a01);
-        *reinterpret_cast<float2 *>(mm + (ra + 1) * 16 + cb) = make_float2(a10, a11);
+    // ---- P7: off-diagonal blocks of T.  With D = blockdiag(I + N_ii) and L
+    //      the blocks below it, T = (I + D^-1 L)^-1 D^-1; with Nt = D^-1 L
+    //      (Nt_ij = T_ii N_ij) and R = (I + Nt)^-1 (R_ij = -sum_m Nt_im R_mj),
+    //      T_ij = R_ij T_jj.  Four steps of independent 16 x 16 products.
+    {
+      const int pr = tid >> 6, e = tid & 63;
+      auto Tb = [&](int i, int j) { return sT + 16 * i * LDF + 16 * j; };
+      auto Sc = [&](int k) { return sScr + k * 16 * LDS; };
+      if (pr < 6) {  // Nt_ij for (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+        const int i = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
+        const int j = pr < 3 ? pr : (pr < 5 ? pr - 3 : 0);
+        blk_prod(Sc(pr), LDS, Tb(i, i), LDF, sAkk + 16 * i * LDF + 16 * j, LDF, 1.f, nullptr, 0, e);
       }
       __syncthreads();
-      if (act) {
-        const float *mm = sScr + blk * 256;
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float d0 = sT[(16 * i + ra) * LDF + 16 * i + t];
-          const float d1 = sT[(16 * i + ra + 1) * LDF + 16 * i + t];
-          const float2 mv = *reinterpret_cast<const float2 *>(mm + t * 16 + cb);
-          a00 = fmaf(d0, mv.x, a00); a01 = fmaf(d0, mv.y, a01);
-          a10 = fmaf(d1, mv.x, a10); a11 = fmaf(d1, mv.y, a11);
-        }
-        *reinterpret_cast<float2 *>(sT + (16 * i + ra) * LDF + 16 * j + cb) = make_float2(-a00, -a01);
-        *reinterpret_cast<float2 *>(sT + (16 * i + ra + 1) * LDF + 16 * j + cb) = make_float2(-a10, -a11);
+      if (pr < 3) {          // T_{i,i-1} = -Nt_{i,i-1} T_{i-1,i-1}
+        blk_prod(Tb(pr + 1, pr), LDF, Sc(pr), LDS, Tb(pr, pr), LDF, -1.f, nullptr, 0, e);
+      } else if (pr == 3) {  // R_20 = Nt_21 Nt_10 - Nt_20
+        blk_prod(Sc(6), LDS, Sc(1), LDS, Sc(0), LDS, 1.f, Sc(3), LDS, e);
+      } else if (pr == 4) {  // R_31 = Nt_32 Nt_21 - Nt_31
+        blk_prod(Sc(7), LDS, Sc(2), LDS, Sc(1), LDS, 1.f, Sc(4), LDS, e);
+      } else if (pr == 5) {  // Nt_31 Nt_10 - Nt_30 (first two terms of R_30)
+        blk_prod(Sc(8), LDS, Sc(4), LDS, Sc(0), LDS, 1.f, Sc(5), LDS, e);
       }
+      __syncthreads();
+      if (pr == 0) {         // T_20 = R_20 T_00
+        blk_prod(Tb(2, 0), LDF, Sc(6), LDS, Tb(0, 0), LDF, 1.f, nullptr, 0, e);
+      } else if (pr == 1) {  // T_31 = R_31 T_11
+        blk_prod(Tb(3, 1), LDF, Sc(7), LDS, Tb(1, 1), LDF, 1.f, nullptr, 0, e);
+      } else if (pr == 2) {  // R_30 = (Nt_31 Nt_10 - Nt_30) - Nt_32 R_20
+        blk_prod(Sc(9), LDS, Sc(2), LDS, Sc(6), LDS, -1.f, Sc(8), LDS, e, 1.f);
+      }
+      __syncthreads();
+      if (pr == 0)           // T_30 = R_30 T_00
+        blk_prod(Tb(3, 0), LDF, Sc(9), LDS, Tb(0, 0), LDF, 1.f, nullptr, 0, e);
       __syncthreads();
     }
-    {  // T -> bf16: smem operand (rows 0..63) and rows 0..63 of [T ; A_qk]
-      const int r = tid >> 3, j8 = (tid & 7) * 8;
+    // ---- P8: T diag(beta) to bf16 (beta folds into T's columns, so the
+    //      right-hand side is [K e^G | V] as loaded); v of this item landed
+    {
+      const int rl = tid & 7, jc = (tid >> 3) & 7, r = 8 * (tid >> 6) + rl, j8 = 8 * jc;
       const float4 *src = reinterpret_cast<const float4 *>(sT + r * LDF + j8);
       const float4 a = src[0], b4 = src[1];
       float t8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
-      if ((j8 >> 4) > (r >> 4)) {
+      const bool upper = (j8 >> 4) > (r >> 4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = 0.f;
-      }
+      for (int i = 0; i < 8; ++i) t8[i] = upper ? 0.f : t8[i] * sBeta[j8 + i];
       st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
-      st_g16(gi, I_TAQ + op_off(r, j8, C), t8);
+    }
+    v_inflight = true;
+    if (!mbar_wait(v_bar, v_phase)) abort_all();
+    else v_inflight = false;
+    v_phase ^= 1u;
+    if (n < C) {  // rows past the chunk's end: zero (they may hold anything)
+      const int m = C - n;
+      for (int i = tid; i < (VD / 8) * m; i += PT) {
+        const int grp = i / m, rr = n + i % m;
+        *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(KD + 8 * grp, rr, C)) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
+    if (*sAbort) goto done;
 
     // ---- P5: [w | u] = T [beta K e^G | beta V] (N = 256) ----
     if (tid == 0) {
@@ -532,6 +612,12 @@ __global__ void __launch_bounds__(PT, 1)
     __syncthreads();
     if (*sAbort) goto done;
     tc_fence_after();
+    if (has_next) {  // RHST is free again: the next item's v
+      if (warp == 1) issue_v(next);
+      v_inflight = true;
+      v_pending = v_phase;
+    }
+    // ---- P9: [w | u] out of TMEM into the item
     if (quad < 2) {  // lanes 0..63: chunk rows; 4 warps share the 16 column pieces
       const int r = L;
 #pragma unroll
@@ -572,6 +658,7 @@ __global__ void __launch_bounds__(PT, 1)
 
 done:
   if (tma_inflight) mbar_wait(tma_bar, tma_pending);
+  if (v_inflight) mbar_wait(v_bar, v_pending);
   if (mma_inflight) mbar_wait(mma_bar, mma_pending);
   tc_fence_before();
   __syncthreads();
@@ -585,9 +672,12 @@ done:
 // 256 threads: two warps per TMEM lane quadrant, each owning 16 of the 32
 // value columns (warp w: quadrant w % 4, columns 16 (w / 4) ..).
 constexpr int RT = 256;
-// One stage: [w ; Q e^G] | [T ; A_qk] | K^T (one 64 KiB copy), this unit's
-// u tile (64 x 32 bf16), e^{G_C}.
+// One stage: [w ; Q e^G] | [0 ; A_qk] | (K e^{G_C-G})^T (the 128-row A
+// operands; the zero rows stay zero for the whole kernel), this unit's u tile
+// (64 x 32 bf16), e^{G_C}.
+constexpr uint32_t S_WQ = 0, S_TAQ = 32768, S_KHT = 49152;
 constexpr uint32_t S_U = 65536, S_GAM = S_U + 4096, S_BYTES = S_GAM + 512;
+constexpr uint32_t S_TX = 32768 + 24576 + 4096 + 512;  // bytes copied per stage
 constexpr uint32_t R_STAGE = 70656;            // S_BYTES rounded to 1 KiB
 constexpr uint32_t R_ST = 2 * R_STAGE;         // S^T MN-major 32 x Kd 128
 constexpr uint32_t R_UT = R_ST + 8192;         // U^T MN-major 32 x Kd 64
@@ -596,7 +686,8 @@ constexpr uint32_t R_SLOT = R_BAR + 24;
 constexpr uint32_t R_ABORT = R_SLOT + 4;
 constexpr uint32_t R_SMEM = R_ABORT + 12;
 constexpr uint32_t R_ALLOC = R_SMEM + 1024;
-static_assert(S_BYTES <= R_STAGE && I_KHT + 16384 == S_U, "stage layout");
+static_assert(S_BYTES <= R_STAGE && S_KHT + 16384 == S_U && I_AQK + 8192 == I_KHT,
+              "stage layout");
 static_assert(R_ALLOC <= 232448, "rec smem fits");
 // TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
 // while the first MMA of chunk n + 1 runs; D2 single.
@@ -640,8 +731,9 @@ __global__ void __launch_bounds__(RT, 1)
   auto issue_stage = [&](int s, const unsigned char *src, int vt) {
     const uint32_t dst = sb + (uint32_t)s * R_STAGE;
     const uint32_t bar = bar0 + 8u * (uint32_t)s;
-    mbar_expect_tx(bar, S_BYTES);
-    bulk_load(dst, src, S_U, bar);
+    mbar_expect_tx(bar, S_TX);
+    bulk_load(dst + S_WQ, src + I_WQ, 32768, bar);
+    bulk_load(dst + S_TAQ + 8192, src + I_AQK, 24576, bar);  // A_qk rows, then K^T
     bulk_load(dst + S_U, src + I_U + (size_t)vt * 4096, 4096, bar);
     bulk_load(dst + S_GAM, src + I_GAM, 512, bar);
   };
@@ -657,6 +749,12 @@ __global__ void __launch_bounds__(RT, 1)
     else mma_inflight = false;
     mma_phase ^= 1u;
   };
+
+  for (int i = tid; i < 2 * 512; i += RT) {  // rows 0..63 of [0 ; A_qk], both stages
+    const int st = i >> 9, o16 = i & 511;
+    *reinterpret_cast<uint4 *>(smem + (uint32_t)st * R_STAGE + S_TAQ + 16 * o16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
 
   float S[16];  // S[key row L][col0 .. col0 + 15], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
@@ -707,7 +805,7 @@ __global__ void __launch_bounds__(RT, 1)
     // ---- P11: D1[0] = [w ; Q e^G] S for chunk 0
     if (tid == 0) {
       tc_fence_after();
-      mma_group(tmem + R_TM_D1, sb + I_WQ, sb + R_ST, KD, VT, false, 0, 1);
+      mma_group(tmem + R_TM_D1, sb + S_WQ, sb + R_ST, KD, VT, false, 0, 1);
       mma_commit(mma_bar);
     }
 
@@ -746,8 +844,8 @@ __global__ void __launch_bounds__(RT, 1)
       // ---- P13: D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + d1, sstg + I_TAQ, sb + R_UT, C, VT, true, 0, 1);
-        mma_group(tmem + R_TM_D2, sstg + I_KHT, sb + R_UT, C, VT, false, 1, 1);
+        mma_group(tmem + d1, sstg + S_TAQ, sb + R_UT, C, VT, true, 0, 1);
+        mma_group(tmem + R_TM_D2, sstg + S_KHT, sb + R_UT, C, VT, false, 1, 1);
         mma_commit(mma_bar);
       }
       wait_mma();
@@ -775,14 +873,14 @@ __global__ void __launch_bounds__(RT, 1)
       tc_fence_before();
       __syncthreads();
       if (c + 2 < n_chunks) {  // stage s is free: its MMAs and reads are done
-        if (tid == 0) issue_stage(s, item_ptr(c + 2), vt);
+        if (tid == 32) issue_stage(s, item_ptr(c + 2), vt);  // beside the MMA issue
         st_issued |= 1u << s;
       }
       if (c + 1 < n_chunks) {
         wait_stage(s ^ 1);
         if (tid == 0) {
           tc_fence_after();
-          mma_group(tmem + R_TM_D1 + 32u * (uint32_t)(s ^ 1), sb + (uint32_t)(s ^ 1) * R_STAGE + I_WQ,
+          mma_group(tmem + R_TM_D1 + 32u * (uint32_t)(s ^ 1), sb + (uint32_t)(s ^ 1) * R_STAGE + S_WQ,
                     sb + R_ST, KD, VT, false, 0, 1);
           mma_commit(mma_bar);
         }
@@ -846,7 +944,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
-              uint64_t cols, uint64_t rows, uint32_t box_cols) {
+              uint64_t cols, uint64_t rows, uint32_t box_cols, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -854,7 +952,7 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
   const cuuint32_t box[2] = {box_cols, (cuuint32_t)C};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
@@ -909,10 +1007,12 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   }
   const uint64_t rows = (uint64_t)p.B * p.T;
   CUtensorMap mq, mk, mg, mv;
-  if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, KD) ||
-      !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, KD) ||
-      !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, KD) ||
-      !make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * VD, rows, VD))
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
+      !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
+      !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, 32, sw) ||
+      !make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * VD, rows, 8,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_prep_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_ALLOC);

@@ -111,7 +111,7 @@ KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_
 /*
  * Workspace bytes implementation `impl` needs (same zero-fill rule).  For
  * KDA_IMPL_SPLIT this holds the per-chunk operands the recurrence kernel
- * reads: about 81 KB per (row, 64-token chunk, head).  With segment ids the
+ * reads: about 73 KB per (row, 64-token chunk, head).  With segment ids the
  * chunks are those of each run, so their number depends on the runs: the
  * size returned here assumes at most ceil(T/64) runs per row (see
  * kda_chunk_fwd_workspace_size_packed for another bound).  For

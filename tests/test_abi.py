@@ -122,14 +122,14 @@ def test_impl_available_query(L):
 def test_workspace_size_for_each_impl(L):
     base = kda.workspace_size(1, 8192, 32, 128, 128)
     split = kda.workspace_size(1, 8192, 32, 128, 128, impl="split")
-    assert split == 1024 + 128 * 32 * 82944          # one 81 KiB item per chunk-head
+    assert split == 1024 + 128 * 32 * 74240          # one 72.5 KiB item per chunk-head
     assert kda.workspace_size(1, 8192, 32, 128, 128, impl="auto") == split
     assert kda.workspace_size(1, 8192, 32, 128, 128, impl="tc") == base
     # packed: header + run list + chunk tables, then B*(ceil(T/64) + runs bound) items
     packed = kda.workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="split")
     assert packed == kda.workspace_size_packed(1, 100, 2, 128, 128, 2)
     assert kda.workspace_size_packed(1, 100, 2, 128, 128, 5) - \
-        kda.workspace_size_packed(1, 100, 2, 128, 128, 2) == 3 * 2 * 82944
+        kda.workspace_size_packed(1, 100, 2, 128, 128, 2) == 3 * 2 * 74240
     assert kda.workspace_size_packed(1, 100, 2, 128, 128, 0) == 0
     assert kda.workspace_size_packed(1, 100, 2, 64, 64, 3) == 0
     assert kda.workspace_size(1, 100, 2, 64, 64, impl="split") == 0
