@@ -27,8 +27,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <type_traits>
-
 #include "kda_internal.cuh"
 #include "kda_tc_common.cuh"
 
@@ -50,43 +48,65 @@ constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
 constexpr uint32_t ITEM_BYTES = 74240;     // 72.5 KiB, 256-byte aligned
 constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
 
-// ---- prep kernel shared memory ----------------------------------------------
-constexpr int PT = 512;                       // threads
-// Raw q / k tiles: two 64-column halves, g: four 32-column quarters, each
-// 64 rows of 128 bytes with the TMA 128-byte swizzle (16-byte unit u of row
-// r stored at unit u ^ (r % 8)), so that row- and column-wise reads are both
-// free of bank conflicts.  v goes straight into the V part of RHST.
-constexpr uint32_t P_RAW_Q = 0, P_RAW_K = 16384, P_RAW_G = 32768;
-constexpr uint32_t P_RAW_TX = 16384 * 2 + 32768;
+// ---- prep kernel --------------------------------------------------------------
+// Two CTAs of 256 threads per SM, each working on its own item, so that one
+// CTA's serial phases (the block solve, the MMA round trips) overlap the
+// other's.  To fit two CTAs, the intra-chunk operands are built in two
+// halves of 64 key channels (the A products accumulate over both halves on
+// the tensor cores).  Shared memory (offsets from a 1 KiB-aligned base):
+//   RAW   q, k (64 rows x 64 channels bf16) and g (64 x 64 fp32) of one
+//         channel half, TMA 128-byte swizzle (16-byte unit u of row r at
+//         u ^ (r % 8)), so that row- and column-wise reads are conflict free;
+//   X, Y  [K e1 ; Q e1] (128 rows) and Y_0..Y_3 (160 rows), Kd 64 each;
+//   RHST  [K e^G | V]^T, MN-major 256 x Kd 64 (v lands here by TMA);
+//   solver fp32 buffers, aliased over RAW + X + Y once the A products are
+//   in TMEM.
+constexpr int PT = 256;                       // threads
+constexpr int KH = 64;                        // key channels per half
+constexpr uint32_t P_RAW_Q = 0, P_RAW_K = 8192, P_RAW_G = 16384;
+constexpr uint32_t P_RAW_TX = 8192 * 2 + 16384;
 constexpr uint32_t P_V_TX = 16384;
-constexpr uint32_t P_X = 65536;               // 128 x Kd 128
-constexpr uint32_t P_Y = P_X + 32768;         // Y_0..Y_3, 160 rows x Kd 128
-constexpr uint32_t P_RHST = P_Y + 40960;      // [beta K e^G | beta V]^T MN-major 256 x 64
+constexpr uint32_t P_X = 32768;               // 128 x Kd 64
+constexpr uint32_t P_Y = P_X + 16384;         // Y_0..Y_3, 160 rows x Kd 64
+constexpr uint32_t P_RHST = P_Y + 20480;      // 256 x Kd 64, MN-major
 constexpr uint32_t P_MISC = P_RHST + 32768;
 constexpr uint32_t P_BETA = P_MISC;           // 64 fp32
-constexpr uint32_t P_DBLK = P_MISC + 256;     // 4 x 128 fp32
-constexpr uint32_t P_BSUM = P_DBLK + 2048;    // 4 x 128 fp32 block sums of g
-constexpr uint32_t P_BAR = P_BSUM + 2048;     // tma, mma, v
+constexpr uint32_t P_DBLK = P_MISC + 256;     // 4 x 128 fp32: e^{block sum of g}
+constexpr uint32_t P_BSUM = P_DBLK + 2048;    // 4 x 64 fp32 block sums (one half)
+constexpr uint32_t P_FAC = P_BSUM + 1024;     // factor table, 4 x 7 x 64 fp32
+constexpr uint32_t P_BAR = P_FAC + 7168;      // raw, mma, v
 constexpr uint32_t P_SLOT = P_BAR + 24;
 constexpr uint32_t P_ABORT = P_SLOT + 4;
-constexpr uint32_t P_SMEM = P_ABORT + 12;
+constexpr uint32_t P_SMEM = P_ABORT + 20;
 constexpr uint32_t P_ALLOC = P_SMEM + 1024;
 constexpr int LDF = C + 4;
-constexpr uint32_t P_AKK = P_X;                    // fp32 64 x 68
-constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68
-constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T bf16 K-major (128-row operand)
-constexpr uint32_t P_SCR = P_TB + 16384;           // 10 blocks of 16 x LDS fp32
+constexpr uint32_t P_AKK = 0;                      // fp32 64 x 68 (beta A_kk)
+constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68 (T)
+constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T diag(beta) bf16, K-major rows 0..63
+constexpr uint32_t P_SCR = P_TB + 8192;            // 10 blocks of 16 x LDS fp32
 constexpr int LDS = 20;                            // padded: conflict-free rows
-static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_RHST, "prep aliases inside X / Y");
-static_assert(P_ALLOC <= 232448, "prep smem fits");
-constexpr uint32_t P_TM_TX = 256;  // TMEM: X Y^T at 0..159, [w | u] at 256
+static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_RHST && P_TB + 16384 <= P_RHST,
+              "solver buffers and the 128-row T operand (rows 64..127 ignored) stay below RHST");
+static_assert(P_RHST % 1024 == 0 && P_X % 1024 == 0, "operand alignment");
+// Per-(block, channel) factors of one channel half, built with the cumsum and
+// read by the operand build: prod_{i<b} D_i, prod_{i>b} D_i, 1/D_b, D_{b+1},
+// D_{b+1} D_{b+2}, and (log2e times) G before block b and at its last row.
+enum { F_PRE, F_SUF, F_RD, F_X2, F_X3, F_PL, F_EL, kFac };
+static_assert(kNumSub * kFac * KH * 4 == 7168, "factor table size");
+static_assert(2 * (P_ALLOC + 1024) <= 233472, "two prep CTAs fit one SM");
 
-// Byte offsets of element (row r, column c) in the swizzled raw tiles.
+// Byte offsets of element (row r, channel c of the half) in the raw tiles.
 __device__ __forceinline__ uint32_t kq_off(int r, int c) {
-  return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+  return (uint32_t)(r * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
 }
 __device__ __forceinline__ uint32_t g_off(int r, int c) {
   return (uint32_t)((c >> 5) * 8192 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
+}
+__device__ __forceinline__ void ld_f32x8s(const float *p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(p);
+  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 __device__ __forceinline__ void ld_f32x8(const unsigned char *tile, int r, int c8, float (&v)[8]) {
   const float4 a = *reinterpret_cast<const float4 *>(tile + g_off(r, c8));
@@ -95,13 +115,15 @@ __device__ __forceinline__ void ld_f32x8(const unsigned char *tile, int r, int c
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__device__ __forceinline__ uint32_t p_y_off(int b) {
-  return P_Y + 256u * (uint32_t)(8 * b * (b + 1));
-}
 // Y_0..Y_3 are stored back to back (row groups of 8), so together they form
 // one 160-row B operand: a single N = 160 MMA gives X Y_b^T for every b at
 // TMEM columns 8 b (b + 1) ... 8 b (b + 1) + 16 (b + 1) - 1.
+__device__ __forceinline__ uint32_t p_y_off(int b) {
+  return P_Y + 128u * (uint32_t)(8 * b * (b + 1));
+}
 __device__ __forceinline__ uint32_t tm_a(int b) { return 8u * (uint32_t)(b * (b + 1)); }
+// The 16-column TMEM pieces of X Y^T that hold the products of the rows of
+// lane quadrant `quad` (blocks 0-1 for even quadrants, 2-3 for odd ones).
 __device__ __forceinline__ int piece_count(int quad) { return (quad & 1) ? 7 : 3; }
 __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
   if ((quad & 1) == 0) {
@@ -165,34 +187,39 @@ __device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const flo
   *reinterpret_cast<uint4 *>(g + off) = w;
 }
 
-// One 16 x 16 block product on the CUDA cores, 64 threads (e = 0..63, one
-// row and four columns each): dst = sgn X Y + add_sgn add  (add optional).
+
+// One 16 x 16 block product on the CUDA cores by one warp (e = lane: rows
+// e / 4 and e / 4 + 8, four columns each): dst = sgn X Y + add_sgn add.
 __device__ __forceinline__ void blk_prod(float *dst, int ldd, const float *X, int ldx,
                                          const float *Y, int ldy, float sgn, const float *add,
                                          int lda, int e, float add_sgn = -1.f) {
   const int r = e >> 2, c4 = (e & 3) * 4;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  float a[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
-    const float x = X[r * ldx + t];
+    const float x0 = X[r * ldx + t], x1 = X[(r + 8) * ldx + t];
     const float4 y = *reinterpret_cast<const float4 *>(Y + t * ldy + c4);
-    a0 = fmaf(x, y.x, a0);
-    a1 = fmaf(x, y.y, a1);
-    a2 = fmaf(x, y.z, a2);
-    a3 = fmaf(x, y.w, a3);
+    a[0][0] = fmaf(x0, y.x, a[0][0]); a[0][1] = fmaf(x0, y.y, a[0][1]);
+    a[0][2] = fmaf(x0, y.z, a[0][2]); a[0][3] = fmaf(x0, y.w, a[0][3]);
+    a[1][0] = fmaf(x1, y.x, a[1][0]); a[1][1] = fmaf(x1, y.y, a[1][1]);
+    a[1][2] = fmaf(x1, y.z, a[1][2]); a[1][3] = fmaf(x1, y.w, a[1][3]);
   }
-  float4 o = make_float4(sgn * a0, sgn * a1, sgn * a2, sgn * a3);
-  if (add) {
-    const float4 z = *reinterpret_cast<const float4 *>(add + r * lda + c4);
-    o.x = fmaf(add_sgn, z.x, o.x);
-    o.y = fmaf(add_sgn, z.y, o.y);
-    o.z = fmaf(add_sgn, z.z, o.z);
-    o.w = fmaf(add_sgn, z.w, o.w);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rr = r + 8 * h;
+    float4 o = make_float4(sgn * a[h][0], sgn * a[h][1], sgn * a[h][2], sgn * a[h][3]);
+    if (add) {
+      const float4 z = *reinterpret_cast<const float4 *>(add + rr * lda + c4);
+      o.x = fmaf(add_sgn, z.x, o.x);
+      o.y = fmaf(add_sgn, z.y, o.y);
+      o.z = fmaf(add_sgn, z.z, o.z);
+      o.w = fmaf(add_sgn, z.w, o.w);
+    }
+    *reinterpret_cast<float4 *>(dst + rr * ldd + c4) = o;
   }
-  *reinterpret_cast<float4 *>(dst + r * ldd + c4) = o;
 }
 
-__global__ void __launch_bounds__(PT, 1)
+__global__ void __launch_bounds__(PT, 2)
     fwd_prep_kernel(const FwdParams p, unsigned char *items, const ChunkTable ct,
                     const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -208,16 +235,17 @@ __global__ void __launch_bounds__(PT, 1)
   float *sAkk = reinterpret_cast<float *>(smem + P_AKK);
   float *sT = reinterpret_cast<float *>(smem + P_TF);
   float *sScr = reinterpret_cast<float *>(smem + P_SCR);
+  float *sFac = reinterpret_cast<float *>(smem + P_FAC);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + P_ABORT);
-  const uint32_t tma_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8, v_bar = sb + P_BAR + 16;
+  const uint32_t raw_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8, v_bar = sb + P_BAR + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, sub = warp >> 2;  // 4 warps per TMEM lane quadrant
+  const int quad = warp & 3, sub = warp >> 2;  // 2 warps per TMEM lane quadrant
   const int L = 32 * quad + lane;
   const int H = p.H, T = p.T;
 
-  if (warp == 0) tmem_alloc(sb + P_SLOT, 512);
+  if (warp == 0) tmem_alloc(sb + P_SLOT, 256);
   if (tid == 0) {
-    mbar_init(tma_bar, 1);
+    mbar_init(raw_bar, 1);
     mbar_init(mma_bar, 1);
     mbar_init(v_bar, 1);
     *sAbort = 0u;
@@ -228,12 +256,24 @@ __global__ void __launch_bounds__(PT, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P_SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
-  uint32_t tma_phase = 0, mma_phase = 0, v_phase = 0, tma_pending = 0, mma_pending = 0,
-           v_pending = 0;
-  bool tma_inflight = false, mma_inflight = false, v_inflight = false;
+  uint32_t raw_phase = 0, mma_phase = 0, v_phase = 0;
+  uint32_t raw_pending = 0, mma_pending = 0, v_pending = 0;
+  bool raw_inflight = false, mma_inflight = false, v_inflight = false;
   auto abort_all = [&]() {
     *sAbort = 1u;
     set_status(p.status, KDA_DEVICE_TIMEOUT);
+  };
+  auto wait_raw = [&]() {
+    if (!mbar_wait(raw_bar, raw_phase)) abort_all();
+    else raw_inflight = false;
+    raw_phase ^= 1u;
+  };
+  auto wait_mma = [&]() {
+    mma_inflight = true;
+    mma_pending = mma_phase;
+    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
+    else mma_inflight = false;
+    mma_phase ^= 1u;
   };
 
   const uint32_t n_chunk_items = total_chunk_count(ct, p.B);
@@ -246,18 +286,15 @@ __global__ void __launch_bounds__(PT, 1)
   };
   // Both issue functions are called by all 32 lanes of one warp: lane 0
   // arms the barrier, then one box per lane.
-  auto issue_tma = [&](uint32_t it) {
+  auto issue_raw = [&](uint32_t it, int half) {  // q, k, g of one channel half
     int b, t0, end, h;
     item_coords(it, b, t0, end, h);
-    const int y = b * T + t0;
-    if (lane == 0) mbar_expect_tx(tma_bar, P_RAW_TX);
+    const int y = b * T + t0, x = h * KD + KH * half;
+    if (lane == 0) mbar_expect_tx(raw_bar, P_RAW_TX);
     __syncwarp();
-    if (lane < 2)
-      tma_load_2d(sb + P_RAW_Q + 8192 * lane, &tm_q, h * KD + 64 * lane, y, tma_bar);
-    else if (lane < 4)
-      tma_load_2d(sb + P_RAW_K + 8192 * (lane - 2), &tm_k, h * KD + 64 * (lane - 2), y, tma_bar);
-    else if (lane < 8)
-      tma_load_2d(sb + P_RAW_G + 8192 * (lane - 4), &tm_g, h * KD + 32 * (lane - 4), y, tma_bar);
+    if (lane == 0) tma_load_2d(sb + P_RAW_Q, &tm_q, x, y, raw_bar);
+    else if (lane == 1) tma_load_2d(sb + P_RAW_K, &tm_k, x, y, raw_bar);
+    else if (lane < 4) tma_load_2d(sb + P_RAW_G + 8192 * (lane - 2), &tm_g, x + 32 * (lane - 2), y, raw_bar);
   };
   // v as 16 column groups of 8, each 64 rows x 16 bytes: the MN-major layout
   // of the V part of RHST (read by the [w | u] MMA).
@@ -280,10 +317,10 @@ __global__ void __launch_bounds__(PT, 1)
   uint32_t item = blockIdx.x;
   float beta_next = 0.f;
   if (item < n_items) {
-    if (warp == 0) issue_tma(item);
+    if (warp == 0) issue_raw(item, 0);
     if (warp == 1) issue_v(item);
-    tma_inflight = v_inflight = true;
-    tma_pending = tma_phase;
+    raw_inflight = v_inflight = true;
+    raw_pending = raw_phase;
     v_pending = v_phase;
     if (tid < C) beta_next = load_beta(item);
   }
@@ -294,170 +331,147 @@ __global__ void __launch_bounds__(PT, 1)
     const uint32_t next = item + gridDim.x;
     const bool has_next = next < n_items;
     unsigned char *gi = items + (size_t)item * ITEM_BYTES;
-
     if (tid < C) sBeta[tid] = beta_next;
-    if (!mbar_wait(tma_bar, tma_phase)) abort_all();
-    else tma_inflight = false;
-    tma_phase ^= 1u;
-    __syncthreads();
-    if (*sAbort) goto done;
 
-    // ---- P0: gate cumsum, one thread per (channel, 16-row block) ----
-    {
-      const int c = tid & 127, q4 = tid >> 7;
-      unsigned char *graw = smem + P_RAW_G;
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = 16 * q4 + i;
-        v[i] = r < n ? *reinterpret_cast<const float *>(graw + g_off(r, c)) : 0.f;
-      }
-#pragma unroll
-      for (int i = 1; i < 16; ++i) v[i] += v[i - 1];
-      sBsum[q4 * KD + c] = v[15];
-      sDblk[q4 * KD + c] = ex2(v[15] * kLog2e);
-      __syncthreads();
-      float off = 0.f;
-      for (int i = 0; i < q4; ++i) off += sBsum[i * KD + c];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<float *>(graw + g_off(16 * q4 + i, c)) = v[i] + off;
-    }
-    __syncthreads();
-
-    // ---- P1: operands X, Y_b (the intra-chunk MMA inputs) first ----
-    // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform,
-    // and a compile-time constant inside build_rows), so the per-channel
-    // block factors are built once per thread and only those block b needs.
-    uint32_t kbp[2][4], qtp[2][4], khp[2][4];  // bf16 pairs stored after the MMA issue
-    const int rl = tid & 7, cg = (tid >> 3) & 15, b = tid >> 7;
+    // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform).
+    const int rl = tid & 7, cg = (tid >> 3) & 7, b = tid >> 6;
     const int cc0 = cg * 8;
-    {
-      auto build_rows = [&](auto bconst) {
-        constexpr int BB = decltype(bconst)::value;
-        float pre[8], suf[8], rD[8], x2[8], x3[8], Pl[8], El[8];
-        {
-          float D[kNumSub][8];
+    for (int half = 0; half < 2; ++half) {
+      const int ch0 = KH * half + cc0;  // first of this thread's channels (global)
+      wait_raw();
+      __syncthreads();
+      if (*sAbort) goto done;
+
+      // ---- P0: gate cumsum, one thread per (channel, 16-row block b); the
+      //      block factors of (b, channel) go to the factor table ----
+      {
+        const int c = tid & 63, q4 = tid >> 6;
+        unsigned char *graw = smem + P_RAW_G;
+        float v[16];
 #pragma unroll
-          for (int i = 0; i < kNumSub; ++i) {
-            const float4 *dp = reinterpret_cast<const float4 *>(sDblk + i * KD + cc0);
-            const float4 d0 = dp[0], d1 = dp[1];
-            D[i][0] = d0.x; D[i][1] = d0.y; D[i][2] = d0.z; D[i][3] = d0.w;
-            D[i][4] = d1.x; D[i][5] = d1.y; D[i][6] = d1.z; D[i][7] = d1.w;
-          }
-          float Eb[8], Pb[8];
-          ld_f32x8(smem + P_RAW_G, BB * kSub + kSub - 1, cc0, Eb);
-          if (BB > 0) ld_f32x8(smem + P_RAW_G, BB * kSub - 1, cc0, Pb);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float a = 1.f, zz = 1.f, c2 = 1.f, c3 = 1.f;
-#pragma unroll
-            for (int i = 0; i < kNumSub; ++i) {
-              if (i < BB) a *= D[i][j];
-              if (i > BB) zz *= D[i][j];
-            }
-            if (BB + 2 < kNumSub) { c2 = D[BB + 1][j]; c3 = c2; }
-            if (BB + 3 < kNumSub) c3 *= D[BB + 2][j];
-            pre[j] = a; suf[j] = zz; rD[j] = __frcp_rn(D[BB][j]); x2[j] = c2; x3[j] = c3;
-            Pl[j] = BB > 0 ? Pb[j] * kLog2e : 0.f;
-            El[j] = Eb[j] * kLog2e;
-          }
+        for (int i = 0; i < 16; ++i) {
+          const int r = 16 * q4 + i;
+          v[i] = r < n ? *reinterpret_cast<const float *>(graw + g_off(r, c)) : 0.f;
         }
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          const int r = kSub * BB + 8 * i2 + rl;
-          const bool valid = r < n;
-          float kk[8], qq[8], G[8];
+        for (int i = 1; i < 16; ++i) v[i] += v[i - 1];
+        sBsum[q4 * KH + c] = v[15];
+        sDblk[q4 * KD + KH * half + c] = ex2(v[15] * kLog2e);
+        __syncthreads();
+        float off = 0.f;
+        for (int i = 0; i < q4; ++i) off += sBsum[i * KH + c];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float *>(graw + g_off(16 * q4 + i, c)) = v[i] + off;
+        float D[kNumSub];
+#pragma unroll
+        for (int i = 0; i < kNumSub; ++i) D[i] = sDblk[i * KD + KH * half + c];
+        float pre = 1.f, suf = 1.f, Db = 1.f;
+#pragma unroll
+        for (int i = 0; i < kNumSub; ++i) {
+          if (i < q4) pre *= D[i];
+          if (i > q4) suf *= D[i];
+          if (i == q4) Db = D[i];
+        }
+        const float x2 = q4 + 2 < kNumSub ? D[min(q4 + 1, kNumSub - 1)] : 1.f;
+        const float x3 = q4 + 3 < kNumSub ? x2 * D[min(q4 + 2, kNumSub - 1)] : 1.f;
+        float *f = sFac + q4 * kFac * KH + c;
+        f[F_PRE * KH] = pre;
+        f[F_SUF * KH] = suf;
+        f[F_RD * KH] = __frcp_rn(Db);
+        f[F_X2 * KH] = x2;
+        f[F_X3 * KH] = x3;
+        f[F_PL * KH] = off * kLog2e;             // G before the block
+        f[F_EL * KH] = (v[15] + off) * kLog2e;   // G at the block's last row
+      }
+      __syncthreads();
+
+      // ---- P1: operands of this channel half: X, Y_b (smem, for the MMA),
+      //      beta-free K e^G (RHST), Q e^G and K e^{G_C-G} (the item) ----
+      // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform).
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int r = kSub * b + 8 * i2 + rl;
+        const bool valid = r < n;
+        const float *fb = sFac + b * kFac * KH + cc0;
+        float xk[8], xq[8], ke[8];  // k e^{G-P_b}, q e^{G-P_b}, k e^{E_b-G}
+        {
+          float kk[8], qq[8], G[8], Pl[8], El[8];
           ld_bf16x8(smem + P_RAW_K + kq_off(r, cc0), kk);
           ld_bf16x8(smem + P_RAW_Q + kq_off(r, cc0), qq);
           ld_f32x8(smem + P_RAW_G, r, cc0, G);
-          // Outputs are packed to bf16 pairs as they are computed: X rows r
-          // (k) and 64 + r (q), Y_b .. Y_3 rows r, and the pairs kept for
-          // after the MMA issue.
-          uint32_t pxk[4], pxq[4], pyd[4], py1[4], py2[4], py3[4];
+          ld_f32x8s(fb + F_PL * KH, Pl);
+          ld_f32x8s(fb + F_EL * KH, El);
 #pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2) {
-            float o_xk[2], o_xq[2], o_yd[2], o_y1[2], o_y2[2], o_y3[2], o_qt[2], o_kb[2], o_kh[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int j = 2 * q2 + t;
-              const float gl = G[j] * kLog2e;
-              const float e1 = ex2(gl - Pl[j]);  // e^{G - P_b}
-              const float e2 = ex2(El[j] - gl);  // e^{E_b - G}
-              const float kv = valid ? kk[j] : 0.f;
-              const float qv = valid ? qq[j] : 0.f;
-              const float xk = kv * e1, xq = qv * e1, ke2 = kv * e2;
-              o_xk[t] = xk;
-              o_xq[t] = xq;
-              o_qt[t] = BB > 0 ? xq * pre[j] : xq;
-              o_kb[t] = BB > 0 ? xk * pre[j] : xk;
-              o_kh[t] = BB + 1 < kNumSub ? ke2 * suf[j] : ke2;
-              o_yd[t] = ke2 * rD[j];
-              o_y1[t] = ke2;
-              o_y2[t] = ke2 * x2[j];
-              o_y3[t] = ke2 * x3[j];
-            }
-            pxk[q2] = pack_bf16(o_xk[0], o_xk[1]);
-            pxq[q2] = pack_bf16(o_xq[0], o_xq[1]);
-            pyd[q2] = pack_bf16(o_yd[0], o_yd[1]);
-            if (BB + 1 < kNumSub) py1[q2] = pack_bf16(o_y1[0], o_y1[1]);
-            if (BB + 2 < kNumSub) py2[q2] = pack_bf16(o_y2[0], o_y2[1]);
-            if (BB + 3 < kNumSub) py3[q2] = pack_bf16(o_y3[0], o_y3[1]);
-            kbp[i2][q2] = pack_bf16(o_kb[0], o_kb[1]);
-            qtp[i2][q2] = pack_bf16(o_qt[0], o_qt[1]);
-            khp[i2][q2] = pack_bf16(o_kh[0], o_kh[1]);
+          for (int j = 0; j < 8; ++j) {
+            const float gl = G[j] * kLog2e;
+            const float e1 = ex2(gl - Pl[j]);
+            const float e2 = ex2(El[j] - gl);
+            const float kv = valid ? kk[j] : 0.f;
+            xk[j] = kv * e1;
+            xq[j] = (valid ? qq[j] : 0.f) * e1;
+            ke[j] = kv * e2;
           }
-          auto st4 = [&](uint32_t off, const uint32_t (&w)[4]) {
-            *reinterpret_cast<uint4 *>(smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
-          };
-          st4(P_X + op_off(r, cc0, KD), pxk);
-          st4(P_X + op_off(64 + r, cc0, KD), pxq);
-          st4(p_y_off(BB) + op_off(r, cc0, KD), pyd);
-          if (BB + 1 < kNumSub) st4(p_y_off(BB + 1) + op_off(r, cc0, KD), py1);
-          if (BB + 2 < kNumSub) st4(p_y_off(BB + 2) + op_off(r, cc0, KD), py2);
-          if (BB + 3 < kNumSub) st4(p_y_off(BB + 3) + op_off(r, cc0, KD), py3);
         }
-      };
-      switch (b) {
-        case 0: build_rows(std::integral_constant<int, 0>{}); break;
-        case 1: build_rows(std::integral_constant<int, 1>{}); break;
-        case 2: build_rows(std::integral_constant<int, 2>{}); break;
-        default: build_rows(std::integral_constant<int, 3>{}); break;
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- P2: intra-chunk products on the tensor cores; next item's tiles;
-    //      the remaining operands are stored while the MMAs run ----
-    if (tid == 0) {
-      tc_fence_after();
-      mma_group(tmem, sb + P_X, sb + P_Y, KD, 160, false, 0, 0);
-      mma_commit(mma_bar);
-    }
-    if (has_next && warp == 1) issue_tma(next);
+        // out = base * factor (factor row f of the table, or 1), to bf16
+        auto scaled = [&](const float (&base)[8], int f, uint4 &w) {
+          float fv[8];
+          if (f >= 0) ld_f32x8s(fb + f * KH, fv);
+          else {
 #pragma unroll
-    for (int i2 = 0; i2 < 2; ++i2) {
-      const int r = kSub * b + 8 * i2 + rl;
-      *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(cc0, r, C)) =
-          make_uint4(kbp[i2][0], kbp[i2][1], kbp[i2][2], kbp[i2][3]);
-      *reinterpret_cast<uint4 *>(gi + I_WQ + op_off(64 + r, cc0, KD)) =
-          make_uint4(qtp[i2][0], qtp[i2][1], qtp[i2][2], qtp[i2][3]);
-      *reinterpret_cast<uint4 *>(gi + I_KHT + mn_off(cc0, r, C)) =
-          make_uint4(khp[i2][0], khp[i2][1], khp[i2][2], khp[i2][3]);
+            for (int j = 0; j < 8; ++j) fv[j] = 1.f;
+          }
+          w.x = pack_bf16(base[0] * fv[0], base[1] * fv[1]);
+          w.y = pack_bf16(base[2] * fv[2], base[3] * fv[3]);
+          w.z = pack_bf16(base[4] * fv[4], base[5] * fv[5]);
+          w.w = pack_bf16(base[6] * fv[6], base[7] * fv[7]);
+        };
+        uint4 w;
+        scaled(xk, -1, w);
+        *reinterpret_cast<uint4 *>(smem + P_X + op_off(r, cc0, KH)) = w;
+        scaled(xq, -1, w);
+        *reinterpret_cast<uint4 *>(smem + P_X + op_off(64 + r, cc0, KH)) = w;
+        scaled(ke, F_RD, w);
+        *reinterpret_cast<uint4 *>(smem + p_y_off(b) + op_off(r, cc0, KH)) = w;
+        if (b + 1 < kNumSub) {
+          scaled(ke, -1, w);
+          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 1) + op_off(r, cc0, KH)) = w;
+        }
+        if (b + 2 < kNumSub) {
+          scaled(ke, F_X2, w);
+          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 2) + op_off(r, cc0, KH)) = w;
+        }
+        if (b + 3 < kNumSub) {
+          scaled(ke, F_X3, w);
+          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 3) + op_off(r, cc0, KH)) = w;
+        }
+        scaled(xk, F_PRE, w);  // K e^G (beta goes into T's columns)
+        *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(ch0, r, C)) = w;
+        scaled(xq, F_PRE, w);  // Q e^G
+        *reinterpret_cast<uint4 *>(gi + I_WQ + op_off(64 + r, ch0, KD)) = w;
+        scaled(ke, F_SUF, w);  // K e^{G_C - G}
+        *reinterpret_cast<uint4 *>(gi + I_KHT + mn_off(ch0, r, C)) = w;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- P2: this half's share of the A products on the tensor cores;
+      //      the next half's tiles ----
+      if (tid == 0) {
+        tc_fence_after();
+        mma_group(tmem, sb + P_X, sb + P_Y, KH, 160, half > 0, 0, 0);
+        mma_commit(mma_bar);
+      }
+      if (half == 0 && warp == 1) issue_raw(item, 1);  // the raw tiles are consumed
+      if (half == 0) {
+        raw_inflight = true;
+        raw_pending = raw_phase;
+      }
+      if (half == 1 && has_next && tid < C) beta_next = load_beta(next);
+      wait_mma();  // X / Y are free again (and, after half 1, A is in TMEM)
     }
     fence_proxy_async();
-    if (has_next) {
-      tma_inflight = true;
-      tma_pending = tma_phase;
-      if (tid < C) beta_next = load_beta(next);
-    }
-    mma_inflight = true;
-    mma_pending = mma_phase;
-    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
-    else mma_inflight = false;
-    mma_phase ^= 1u;
     __syncthreads();
     if (*sAbort) goto done;
     tc_fence_after();
@@ -468,13 +482,13 @@ __global__ void __launch_bounds__(PT, 1)
       const bool is_q = L >= 64;
       const int bme = r >> 4;
       const int np = piece_count(quad);
-      for (int pi = sub; pi < np; pi += 8) {
+      for (int pi = sub; pi < np; pi += 4) {
         float v[2][16];
         int bb[2], pp[2];
         piece(quad, pi, bb[0], pp[0]);
-        const bool two = pi + 4 < np;
+        const bool two = pi + 2 < np;
         if (two) {
-          piece(quad, pi + 4, bb[1], pp[1]);
+          piece(quad, pi + 2, bb[1], pp[1]);
           tmem_ld16x2(tq + tm_a(bb[0]) + 16 * pp[0], tq + tm_a(bb[1]) + 16 * pp[1], v[0], v[1]);
         } else {
           bb[1] = -1;
@@ -516,7 +530,7 @@ __global__ void __launch_bounds__(PT, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- P4: T = (I + beta A_kk)^-1, blocked fp32 ----
+    // ---- P4: T = (I + beta A_kk)^-1, blocked fp32: diagonal blocks ----
     if (tid < 64) {
       const int i = tid >> 4, cc = tid & 15, base = 16 * i;
       float x[16];
@@ -536,9 +550,10 @@ __global__ void __launch_bounds__(PT, 1)
     // ---- P7: off-diagonal blocks of T.  With D = blockdiag(I + N_ii) and L
     //      the blocks below it, T = (I + D^-1 L)^-1 D^-1; with Nt = D^-1 L
     //      (Nt_ij = T_ii N_ij) and R = (I + Nt)^-1 (R_ij = -sum_m Nt_im R_mj),
-    //      T_ij = R_ij T_jj.  Four steps of independent 16 x 16 products.
+    //      T_ij = R_ij T_jj.  Four steps of independent 16 x 16 products,
+    //      one warp each.
     {
-      const int pr = tid >> 6, e = tid & 63;
+      const int pr = warp, e = lane;
       auto Tb = [&](int i, int j) { return sT + 16 * i * LDF + 16 * j; };
       auto Sc = [&](int k) { return sScr + k * 16 * LDS; };
       if (pr < 6) {  // Nt_ij for (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
@@ -572,14 +587,18 @@ __global__ void __launch_bounds__(PT, 1)
     // ---- P8: T diag(beta) to bf16 (beta folds into T's columns, so the
     //      right-hand side is [K e^G | V] as loaded); v of this item landed
     {
-      const int rl = tid & 7, jc = (tid >> 3) & 7, r = 8 * (tid >> 6) + rl, j8 = 8 * jc;
-      const float4 *src = reinterpret_cast<const float4 *>(sT + r * LDF + j8);
-      const float4 a = src[0], b4 = src[1];
-      float t8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
-      const bool upper = (j8 >> 4) > (r >> 4);
+      const int rl8 = tid & 7, jc = (tid >> 3) & 3, r = 8 * (tid >> 5) + rl8;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) t8[i] = upper ? 0.f : t8[i] * sBeta[j8 + i];
-      st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
+      for (int e = 0; e < 2; ++e) {
+        const int j8 = 16 * jc + 8 * e;
+        const float4 *src = reinterpret_cast<const float4 *>(sT + r * LDF + j8);
+        const float4 a = src[0], b4 = src[1];
+        float t8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+        const bool upper = (j8 >> 4) > (r >> 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = upper ? 0.f : t8[i] * sBeta[j8 + i];
+        st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
+      }
     }
     v_inflight = true;
     if (!mbar_wait(v_bar, v_phase)) abort_all();
@@ -598,33 +617,33 @@ __global__ void __launch_bounds__(PT, 1)
     __syncthreads();
     if (*sAbort) goto done;
 
-    // ---- P5: [w | u] = T [beta K e^G | beta V] (N = 256) ----
+    // ---- P5: [w | u] = T diag(beta) [K e^G | V] (N = 256) over the A
+    //      products' TMEM columns (read out in P3); rows 64..127 of the A
+    //      operand are ignored ----
     if (tid == 0) {
       tc_fence_after();
-      mma_group(tmem + P_TM_TX, sb + P_TB, sb + P_RHST, C, KD + VD, false, 0, 1);
+      mma_group(tmem, sb + P_TB, sb + P_RHST, C, KD + VD, false, 0, 1);
       mma_commit(mma_bar);
     }
-    mma_inflight = true;
-    mma_pending = mma_phase;
-    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
-    else mma_inflight = false;
-    mma_phase ^= 1u;
+    wait_mma();
     __syncthreads();
     if (*sAbort) goto done;
     tc_fence_after();
-    if (has_next) {  // RHST is free again: the next item's v
+    if (has_next) {  // RAW, the solver buffers and RHST are free: next item's tiles
+      if (warp == 0) issue_raw(next, 0);
       if (warp == 1) issue_v(next);
-      v_inflight = true;
+      raw_inflight = v_inflight = true;
+      raw_pending = raw_phase;
       v_pending = v_phase;
     }
     // ---- P9: [w | u] out of TMEM into the item
-    if (quad < 2) {  // lanes 0..63: chunk rows; 4 warps share the 16 column pieces
+    if (quad < 2) {  // lanes 0..63: chunk rows; 2 warps share the 16 column pieces
       const int r = L;
 #pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2) {
-        const int p0 = sub + 8 * k2, p1 = p0 + 4;  // pieces of 16 columns
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const int p0 = sub + 4 * k2, p1 = p0 + 2;  // pieces of 16 columns
         float v0[16], v1[16];
-        tmem_ld16x2(tq + P_TM_TX + 16 * p0, tq + P_TM_TX + 16 * p1, v0, v1);
+        tmem_ld16x2(tq + 16 * p0, tq + 16 * p1, v0, v1);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int pc = e ? p1 : p0;
@@ -645,26 +664,26 @@ __global__ void __launch_bounds__(PT, 1)
           }
         }
       }
-    }
-    if (tid < KD) {
+    } else {
+      const int c = 64 * sub + (tid & 63);  // warps 2, 3, 6, 7: e^{G_C} per key channel
       float gam = 1.f;
 #pragma unroll
-      for (int i = 0; i < kNumSub; ++i) gam *= sDblk[i * KD + tid];
-      reinterpret_cast<float *>(gi + I_GAM)[tid] = gam;
+      for (int i = 0; i < kNumSub; ++i) gam *= sDblk[i * KD + c];
+      reinterpret_cast<float *>(gi + I_GAM)[c] = gam;
     }
     tc_fence_before();
     __syncthreads();
   }
 
 done:
-  if (tma_inflight) mbar_wait(tma_bar, tma_pending);
+  if (raw_inflight) mbar_wait(raw_bar, raw_pending);
   if (v_inflight) mbar_wait(v_bar, v_pending);
   if (mma_inflight) mbar_wait(mma_bar, mma_pending);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -1017,12 +1036,15 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   cudaError_t e = cudaFuncSetAttribute(fwd_prep_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_ALLOC);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fwd_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fwd_rec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)R_ALLOC);
   if (e != cudaSuccess) return e;
   const long sms = num_sms();
   const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
-  const int g1 = (int)(n_items < sms ? n_items : sms);
+  const int g1 = (int)(n_items < 2 * sms ? n_items : 2 * sms);  // two CTAs per SM
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
