@@ -10,7 +10,8 @@
 //      in the shared-memory layouts the tensor cores read:
 //         [w ; Q e^G] (128 x 128 bf16), A_qk (64 x 64 bf16),
 //         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 bf16), e^{G_C}.
-//   2. fwd_rec_kernel: one CTA per (row, head, 32-column value tile) walks
+//   2. fwd_rec_kernel: one CTA per (row, head, value tile of 32 or 64
+//      columns) walks
 //      the chunks in order with the fp32 state in registers; per chunk it
 //      bulk-copies the item (double-buffered) and runs only the
 //      state-dependent MMAs:  D1 = [w ; Q e^G] S,  U = u - w S,
@@ -688,45 +689,54 @@ done:
 }
 
 // ---- recurrence kernel --------------------------------------------------------
-// 256 threads: two warps per TMEM lane quadrant, each owning 16 of the 32
-// value columns (warp w: quadrant w % 4, columns 16 (w / 4) ..).
+// One CTA per (run, head, VTR-column value tile), 256 threads: two warps per
+// TMEM lane quadrant, each owning VTR / 2 of the tile's value columns (warp
+// w: quadrant w % 4, columns (VTR / 2) (w / 4) ..).  VTR is 32 or 64; the
+// wider tile halves the item bytes the CTAs pull from L2 per chunk.
 constexpr int RT = 256;
 // One stage: [w ; Q e^G] | [0 ; A_qk] | (K e^{G_C-G})^T (the 128-row A
-// operands; the zero rows stay zero for the whole kernel), this unit's u tile
-// (64 x 32 bf16), e^{G_C}.
-constexpr uint32_t S_WQ = 0, S_TAQ = 32768, S_KHT = 49152;
-constexpr uint32_t S_U = 65536, S_GAM = S_U + 4096, S_BYTES = S_GAM + 512;
-constexpr uint32_t S_TX = 32768 + 24576 + 4096 + 512;  // bytes copied per stage
-constexpr uint32_t R_STAGE = 70656;            // S_BYTES rounded to 1 KiB
-constexpr uint32_t R_ST = 2 * R_STAGE;         // S^T MN-major 32 x Kd 128
-constexpr uint32_t R_UT = R_ST + 8192;         // U^T MN-major 32 x Kd 64
-constexpr uint32_t R_BAR = R_UT + 4096;        // stage0, stage1, mma
-constexpr uint32_t R_SLOT = R_BAR + 24;
-constexpr uint32_t R_ABORT = R_SLOT + 4;
-constexpr uint32_t R_SMEM = R_ABORT + 12;
-constexpr uint32_t R_ALLOC = R_SMEM + 1024;
-static_assert(S_BYTES <= R_STAGE && S_KHT + 16384 == S_U && I_AQK + 8192 == I_KHT,
-              "stage layout");
-static_assert(R_ALLOC <= 232448, "rec smem fits");
-// TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
-// while the first MMA of chunk n + 1 runs; D2 single.
-constexpr uint32_t R_TM_D1 = 0, R_TM_D2 = 64, R_TM_COLS = 128;
+// operands; the zero rows stay zero for the whole kernel), this unit's u
+// columns (VTR / 32 tiles of 64 x 32 bf16), e^{G_C}.
+constexpr uint32_t S_WQ = 0, S_TAQ = 32768, S_KHT = 49152, S_U = 65536;
+static_assert(S_KHT + 16384 == S_U && I_AQK + 8192 == I_KHT, "stage layout");
+template <int VTR>
+struct RecLayout {
+  static constexpr int NT = VTR / VT;                            // u tiles per unit
+  static constexpr uint32_t S_GAM = S_U + 4096u * NT;
+  static constexpr uint32_t S_BYTES = S_GAM + 512;
+  static constexpr uint32_t S_TX = 32768 + 24576 + 4096u * NT + 512;  // copied per stage
+  static constexpr uint32_t STAGE = (S_BYTES + 1023) / 1024 * 1024;
+  static constexpr uint32_t ST = 2 * STAGE;                     // S^T MN-major VTR x Kd 128
+  static constexpr uint32_t UT = ST + 256u * VTR;               // U^T MN-major VTR x Kd 64
+  static constexpr uint32_t BAR = UT + 128u * VTR;              // stage0, stage1, mma
+  static constexpr uint32_t SLOT = BAR + 24;
+  static constexpr uint32_t ABORT = SLOT + 4;
+  static constexpr uint32_t ALLOC = ABORT + 12 + 1024;
+  // TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
+  // while the first MMA of chunk n + 1 runs; D2 single.
+  static constexpr uint32_t TM_D1 = 0, TM_D2 = 2 * VTR;
+  static constexpr uint32_t TM_COLS = 3 * VTR <= 128 ? 128 : 256;
+  static_assert(ALLOC <= 232448, "rec smem fits");
+};
 
+template <int VTR>
 __global__ void __launch_bounds__(RT, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
+  using Lay = RecLayout<VTR>;
+  constexpr int CPT = VTR / 2;  // value columns per thread
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + R_ABORT);
-  const uint32_t bar0 = sb + R_BAR, mma_bar = sb + R_BAR + 16;
+  volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + Lay::ABORT);
+  const uint32_t bar0 = sb + Lay::BAR, mma_bar = sb + Lay::BAR + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int L = 32 * quad + lane;   // TMEM lane: chunk row (0..63) / o row / key row
-  const int col0 = 16 * half;       // this thread's 16 value columns within the tile
+  const int col0 = CPT * half;      // this thread's value columns within the tile
   const int H = p.H, T = p.T;
 
-  if (warp == 0) tmem_alloc(sb + R_SLOT, R_TM_COLS);
+  if (warp == 0) tmem_alloc(sb + Lay::SLOT, Lay::TM_COLS);
   if (tid == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8, 1);
@@ -737,7 +747,7 @@ __global__ void __launch_bounds__(RT, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + R_SLOT);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + Lay::SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
   uint32_t st_phase[2] = {0u, 0u}, mma_phase = 0;
   uint32_t st_issued = 0;  // per-stage bit: copy issued and not yet waited
@@ -748,13 +758,13 @@ __global__ void __launch_bounds__(RT, 1)
     set_status(p.status, KDA_DEVICE_TIMEOUT);
   };
   auto issue_stage = [&](int s, const unsigned char *src, int vt) {
-    const uint32_t dst = sb + (uint32_t)s * R_STAGE;
+    const uint32_t dst = sb + (uint32_t)s * Lay::STAGE;
     const uint32_t bar = bar0 + 8u * (uint32_t)s;
-    mbar_expect_tx(bar, S_TX);
+    mbar_expect_tx(bar, Lay::S_TX);
     bulk_load(dst + S_WQ, src + I_WQ, 32768, bar);
     bulk_load(dst + S_TAQ + 8192, src + I_AQK, 24576, bar);  // A_qk rows, then K^T
-    bulk_load(dst + S_U, src + I_U + (size_t)vt * 4096, 4096, bar);
-    bulk_load(dst + S_GAM, src + I_GAM, 512, bar);
+    bulk_load(dst + S_U, src + I_U + (size_t)vt * (4096u * Lay::NT), 4096u * Lay::NT, bar);
+    bulk_load(dst + Lay::S_GAM, src + I_GAM, 512, bar);
   };
   auto wait_stage = [&](int s) {
     if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
@@ -768,20 +778,40 @@ __global__ void __launch_bounds__(RT, 1)
     else mma_inflight = false;
     mma_phase ^= 1u;
   };
+  // CPT consecutive fp32 TMEM columns of this thread's lane.
+  auto tmem_ld_cpt = [&](uint32_t taddr, float (&v)[CPT]) {
+    if constexpr (CPT == 16) {
+      tmem_ld16(taddr, v);
+    } else {
+      float a[16], b[16];
+      tmem_ld16x2(taddr, taddr + 16, a, b);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { v[i] = a[i]; v[16 + i] = b[i]; }
+    }
+  };
+  auto store_st = [&](const float (&S)[CPT], int key) {  // S^T bf16, MN-major
+#pragma unroll
+    for (int e = 0; e < CPT / 8; ++e) {
+      float t8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
+      st_bf16x8(smem, Lay::ST + mn_off(col0 + 8 * e, key, KD), t8);
+    }
+  };
 
   for (int i = tid; i < 2 * 512; i += RT) {  // rows 0..63 of [0 ; A_qk], both stages
     const int st = i >> 9, o16 = i & 511;
-    *reinterpret_cast<uint4 *>(smem + (uint32_t)st * R_STAGE + S_TAQ + 16 * o16) =
+    *reinterpret_cast<uint4 *>(smem + (uint32_t)st * Lay::STAGE + S_TAQ + 16 * o16) =
         make_uint4(0u, 0u, 0u, 0u);
   }
 
-  float S[16];  // S[key row L][col0 .. col0 + 15], fp32
+  float S[CPT];  // S[key row L][col0 .. col0 + CPT - 1], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
   const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
     const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
     const int vt = u.vt, h = u.h, b = u.b;
-    const int vc0 = vt * VT;
+    const int vc0 = vt * VTR;
     const int n_chunks = (u.end - u.start + C - 1) / C;
     const uint32_t cbase = ct.run_chunk_base
         ? (uint32_t)(ct.chunk_row_offsets[b] + ct.run_chunk_base[(size_t)b * T + u.run_in_row])
@@ -789,28 +819,20 @@ __global__ void __launch_bounds__(RT, 1)
     auto item_ptr = [&](int c) {
       return items + ((size_t)(cbase + c) * H + h) * ITEM_BYTES;
     };
-    {  // state entering the run; S^T operand (MN-major: v contiguous)
-      const int c = L;
-      if (u.first && p.initial_state) {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            p.initial_state + (((size_t)b * H + h) * KD + c) * p.V + vc0 + col0);
+    // state entering the run; S^T operand (MN-major: v contiguous)
+    if (u.first && p.initial_state) {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          p.initial_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 x = src[q4];
-          S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) S[i] = 0.f;
+      for (int q4 = 0; q4 < CPT / 4; ++q4) {
+        const float4 x = src[q4];
+        S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
       }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float t8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
-        st_bf16x8(smem, R_ST + mn_off(col0 + 8 * e, c, KD), t8);
-      }
+      for (int i = 0; i < CPT; ++i) S[i] = 0.f;
     }
+    store_st(S, L);
     if (tid == 0) {
       issue_stage(0, item_ptr(0), vt);
       if (n_chunks > 1) issue_stage(1, item_ptr(1), vt);
@@ -824,7 +846,7 @@ __global__ void __launch_bounds__(RT, 1)
     // ---- P11: D1[0] = [w ; Q e^G] S for chunk 0
     if (tid == 0) {
       tc_fence_after();
-      mma_group(tmem + R_TM_D1, sb + S_WQ, sb + R_ST, KD, VT, false, 0, 1);
+      mma_group(tmem + Lay::TM_D1, sb + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
       mma_commit(mma_bar);
     }
 
@@ -833,38 +855,39 @@ __global__ void __launch_bounds__(RT, 1)
       const int t0 = u.start + c * C;
       const int n = min(C, u.end - t0);
       const size_t tok0 = (size_t)b * T + t0;
-      const unsigned char *stg = smem + (uint32_t)s * R_STAGE;
-      const uint32_t sstg = sb + (uint32_t)s * R_STAGE;
-      const uint32_t d1 = R_TM_D1 + 32u * (uint32_t)s;
+      const unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
+      const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
+      const uint32_t d1 = Lay::TM_D1 + (uint32_t)VTR * (uint32_t)s;
       // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk
       wait_mma();
       __syncthreads();
       if (*sAbort) goto done;
       tc_fence_after();
 
-      // ---- P12: U = u - w S (lanes 0..63), 16 columns per thread
+      // ---- P12: U = u - w S (lanes 0..63)
       if (quad < 2) {
         const int r = L;
-        float v[16];
-        tmem_ld16(tq + d1 + col0, v);
+        float v[CPT];
+        tmem_ld_cpt(tq + d1 + col0, v);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
+        for (int e = 0; e < CPT / 8; ++e) {
+          const int col = col0 + 8 * e;
           float uu[8], a[8];
-          ld_bf16x8(stg + S_U + (size_t)r * VT * 2 + (col0 + 8 * e) * 2, uu);
+          ld_bf16x8(stg + S_U + (col >> 5) * 4096 + ((size_t)r * VT + (col & 31)) * 2, uu);
 #pragma unroll
           for (int i = 0; i < 8; ++i) a[i] = uu[i] - v[8 * e + i];
-          st_bf16x8(smem, R_UT + mn_off(col0 + 8 * e, r, C), a);
+          st_bf16x8(smem, Lay::UT + mn_off(col, r, C), a);
         }
       }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
 
-      // ---- P13: D1 += [T ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
+      // ---- P13: D1 += [0 ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + d1, sstg + S_TAQ, sb + R_UT, C, VT, true, 0, 1);
-        mma_group(tmem + R_TM_D2, sstg + S_KHT, sb + R_UT, C, VT, false, 1, 1);
+        mma_group(tmem + d1, sstg + S_TAQ, sb + Lay::UT, C, VTR, true, 0, 1);
+        mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 1, 1);
         mma_commit(mma_bar);
       }
       wait_mma();
@@ -874,19 +897,12 @@ __global__ void __launch_bounds__(RT, 1)
 
       // ---- P14: state update (all lanes = key rows), next chunk's first MMA
       {
-        const int cidx = L;
-        const float gam = reinterpret_cast<const float *>(stg + S_GAM)[cidx];
-        float v[16];
-        tmem_ld16(tq + R_TM_D2 + col0, v);
+        const float gam = reinterpret_cast<const float *>(stg + Lay::S_GAM)[L];
+        float v[CPT];
+        tmem_ld_cpt(tq + Lay::TM_D2 + col0, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) S[i] = fmaf(gam, S[i], v[i]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float t8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
-          st_bf16x8(smem, R_ST + mn_off(col0 + 8 * e, cidx, KD), t8);
-        }
+        for (int i = 0; i < CPT; ++i) S[i] = fmaf(gam, S[i], v[i]);
+        store_st(S, L);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -899,21 +915,21 @@ __global__ void __launch_bounds__(RT, 1)
         wait_stage(s ^ 1);
         if (tid == 0) {
           tc_fence_after();
-          mma_group(tmem + R_TM_D1 + 32u * (uint32_t)(s ^ 1), sb + (uint32_t)(s ^ 1) * R_STAGE + S_WQ,
-                    sb + R_ST, KD, VT, false, 0, 1);
+          mma_group(tmem + Lay::TM_D1 + (uint32_t)VTR * (uint32_t)(s ^ 1),
+                    sb + (uint32_t)(s ^ 1) * Lay::STAGE + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
           mma_commit(mma_bar);
         }
       }
       // o rows of this chunk (lanes 64..127) while the next MMA runs
       if (quad >= 2) {
         const int r = L - 64;
-        float v[16];
-        tmem_ld16(tq + d1 + col0, v);
+        float v[CPT];
+        tmem_ld_cpt(tq + d1 + col0, v);
         if (r < n) {
           uint4 *dst = reinterpret_cast<uint4 *>(
               static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0 + col0);
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
+          for (int e = 0; e < CPT / 8; ++e) {
             uint4 w;
             w.x = pack_bf16(p.scale * v[8 * e + 0], p.scale * v[8 * e + 1]);
             w.y = pack_bf16(p.scale * v[8 * e + 2], p.scale * v[8 * e + 3]);
@@ -929,7 +945,7 @@ __global__ void __launch_bounds__(RT, 1)
       float4 *dst = reinterpret_cast<float4 *>(
           p.final_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int q4 = 0; q4 < CPT / 4; ++q4)
         dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
     }
     __syncthreads();
@@ -943,7 +959,7 @@ done:
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, R_TM_COLS);
+    tmem_dealloc(tmem, Lay::TM_COLS);
   }
 }
 
@@ -995,8 +1011,26 @@ size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per
 }
 
 bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
-  return bf16 && K == KD && V == VD && (v_tile == 0 || v_tile == VT);
+  return bf16 && K == KD && V == VD && (v_tile == 0 || v_tile == 32 || v_tile == 64);
 }
+
+namespace {
+template <int VTR>
+cudaError_t launch_rec(const FwdParams &p, const unsigned char *items, const ChunkTable &ct,
+                       bool has_seg, cudaStream_t stream) {
+  using Lay = RecLayout<VTR>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_rec_kernel<VTR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Lay::ALLOC);
+  if (e != cudaSuccess) return e;
+  const long sms = num_sms();
+  const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
+                               : (long)p.B * p.H * p.n_vtiles;
+  const int g2 = (int)(n_units < sms ? n_units : sms);
+  fwd_rec_kernel<VTR><<<g2 > 0 ? g2 : 1, RT, Lay::ALLOC, stream>>>(p, items, ct);
+  return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream, bool with_fallback) {
@@ -1004,8 +1038,12 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, p_in.v_tile))
     return cudaErrorNotSupported;
   FwdParams p = p_in;
-  p.v_tile = VT;
-  p.n_vtiles = VD / VT;
+  // Recurrence value tile: 32 columns when every (run, head, tile) unit runs
+  // at once (one CTA each, no segment ids): the shortest serial chain; 64
+  // otherwise, which halves the units and the item bytes they pull from L2.
+  if (p_in.v_tile != 0) p.v_tile = p_in.v_tile;
+  else p.v_tile = (!has_seg && (long)p.B * p.H * (VD / 32) <= (long)num_sms()) ? 32 : 64;
+  p.n_vtiles = VD / p.v_tile;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   const size_t ioff = items_offset(p.B, p.T, has_seg);
   if (workspace_bytes < ioff + (size_t)p.H * ITEM_BYTES) return cudaErrorInvalidValue;
@@ -1039,20 +1077,14 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   e = cudaFuncSetAttribute(fwd_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fwd_rec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)R_ALLOC);
-  if (e != cudaSuccess) return e;
   const long sms = num_sms();
   const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
   const int g1 = (int)(n_items < 2 * sms ? n_items : 2 * sms);  // two CTAs per SM
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
-                               : (long)p.B * p.H * p.n_vtiles;
-  const int g2 = (int)(n_units < sms ? n_units : sms);
-  fwd_rec_kernel<<<g2 > 0 ? g2 : 1, RT, R_ALLOC, stream>>>(p, items, ct);
-  e = cudaGetLastError();
+  e = p.v_tile == 32 ? launch_rec<32>(p, items, ct, has_seg, stream)
+                     : launch_rec<64>(p, items, ct, has_seg, stream);
   if (e != cudaSuccess || !with_fallback || !has_seg) return e;
   // The fused kernel covers calls whose runs overflow the items (it exits
   // at once when they fit).

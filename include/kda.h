@@ -87,8 +87,11 @@ typedef enum kda_impl {
   KDA_IMPL_SIMT = 1,  /* fp32 CUDA-core kernel (every supported shape)      */
   KDA_IMPL_TC = 2,    /* fused tcgen05 / TMA kernel: bf16, K = V = 128      */
   KDA_IMPL_SPLIT = 3  /* tcgen05 in two kernels (parallel per-chunk prep,
-                         then the state recurrence): bf16, K = V = 128, no
-                         segment ids; needs the larger workspace reported by
+                         then the state recurrence): bf16, K = V = 128,
+                         value tile 32 or 64 (v_tile 0: 32 when every
+                         (row, head, tile) fits one CTA per SM and there are
+                         no segment ids, else 64); needs the larger
+                         workspace reported by
                          kda_chunk_fwd_workspace_size_for(.., KDA_IMPL_SPLIT) */
 } kda_impl;
 

@@ -186,3 +186,22 @@ def test_misaligned_pointer_rejected_on_gpu():
     with pytest.raises(kda.KdaError) as e:
         kda.chunk_fwd(qm, to_dev(x["k"]), to_dev(x["v"]), to_dev(x["g"]), to_dev(x["beta"]))
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("v_tile", [32, 64])
+@pytest.mark.parametrize("name", ["fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg"])
+def test_split_value_tiles(name, v_tile):
+    """The split path's recurrence with either value-tile width (32 or 64
+    columns per CTA) matches the oracle."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.WORKLOADS[name]
+    skip_unless_supported(w, "split")
+    x = ki.make_inputs(w, seed=3)
+    has_seg = w.segments is not None
+    ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, torch.bfloat16, has_seg, impl="split",
+                             max_runs_per_row=len(w.segments) if has_seg else None)
+    o, fs = run_gpu(x, impl="split", v_tile=v_tile, workspace=ws)
+    assert kda.read_device_status(ws) == 0
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, f"{name} v_tile {v_tile} o")
+    assert_parity(fs, fs_ref, True, f"{name} v_tile {v_tile} final_state")
