@@ -694,22 +694,24 @@ done:
 // w: quadrant w % 4, columns (VTR / 2) (w / 4) ..).  VTR is 32 or 64; the
 // wider tile halves the item bytes the CTAs pull from L2 per chunk.
 constexpr int RT = 256;
-// One stage: [w ; Q e^G] | [0 ; A_qk] | (K e^{G_C-G})^T (the 128-row A
-// operands; the zero rows stay zero for the whole kernel), this unit's u
-// columns (VTR / 32 tiles of 64 x 32 bf16), e^{G_C}.
-constexpr uint32_t S_WQ = 0, S_TAQ = 32768, S_KHT = 49152, S_U = 65536;
-static_assert(S_KHT + 16384 == S_U && I_AQK + 8192 == I_KHT, "stage layout");
-template <int VTR>
+// One stage mirrors the item's start: [w ; Q e^G] | A_qk | (K e^{G_C-G})^T
+// (one copy), then this unit's u columns (VTR / 32 tiles of 64 x 32 bf16)
+// and e^{G_C}.  A_qk is read as the 128-row A operand starting 64 rows
+// before it: those rows (the tail of Q e^G) only feed D1 rows 0..63, which
+// are dead once U is formed.
+constexpr uint32_t S_WQ = I_WQ, S_AQK = I_AQK, S_KHT = I_KHT, S_U = I_U;
+static_assert(S_WQ == 0 && S_AQK == 32768 && S_KHT == S_AQK + 8192 && S_U == S_KHT + 16384,
+              "stage layout");
+template <int VTR, int NST>
 struct RecLayout {
   static constexpr int NT = VTR / VT;                            // u tiles per unit
   static constexpr uint32_t S_GAM = S_U + 4096u * NT;
-  static constexpr uint32_t S_BYTES = S_GAM + 512;
-  static constexpr uint32_t S_TX = 32768 + 24576 + 4096u * NT + 512;  // copied per stage
+  static constexpr uint32_t S_BYTES = S_GAM + 512;               // copied per stage
   static constexpr uint32_t STAGE = (S_BYTES + 1023) / 1024 * 1024;
-  static constexpr uint32_t ST = 2 * STAGE;                     // S^T MN-major VTR x Kd 128
+  static constexpr uint32_t ST = NST * STAGE;                   // S^T MN-major VTR x Kd 128
   static constexpr uint32_t UT = ST + 256u * VTR;               // U^T MN-major VTR x Kd 64
-  static constexpr uint32_t BAR = UT + 128u * VTR;              // stage0, stage1, mma
-  static constexpr uint32_t SLOT = BAR + 24;
+  static constexpr uint32_t BAR = UT + 128u * VTR;              // stages, mma
+  static constexpr uint32_t SLOT = BAR + 8 * (NST + 1);
   static constexpr uint32_t ABORT = SLOT + 4;
   static constexpr uint32_t ALLOC = ABORT + 12 + 1024;
   // TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
@@ -719,17 +721,17 @@ struct RecLayout {
   static_assert(ALLOC <= 232448, "rec smem fits");
 };
 
-template <int VTR>
+template <int VTR, int NST>
 __global__ void __launch_bounds__(RT, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
-  using Lay = RecLayout<VTR>;
+  using Lay = RecLayout<VTR, NST>;
   constexpr int CPT = VTR / 2;  // value columns per thread
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + Lay::ABORT);
-  const uint32_t bar0 = sb + Lay::BAR, mma_bar = sb + Lay::BAR + 16;
+  const uint32_t bar0 = sb + Lay::BAR, mma_bar = sb + Lay::BAR + 8 * NST;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int L = 32 * quad + lane;   // TMEM lane: chunk row (0..63) / o row / key row
@@ -738,8 +740,7 @@ __global__ void __launch_bounds__(RT, 1)
 
   if (warp == 0) tmem_alloc(sb + Lay::SLOT, Lay::TM_COLS);
   if (tid == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
+    for (int i = 0; i < NST; ++i) mbar_init(bar0 + 8u * i, 1);
     mbar_init(mma_bar, 1);
     *sAbort = 0u;
     fence_mbar_init();
@@ -749,7 +750,7 @@ __global__ void __launch_bounds__(RT, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + Lay::SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
-  uint32_t st_phase[2] = {0u, 0u}, mma_phase = 0;
+  uint32_t st_phase[NST] = {}, mma_phase = 0;
   uint32_t st_issued = 0;  // per-stage bit: copy issued and not yet waited
   bool mma_inflight = false;
   uint32_t mma_pending = 0;
@@ -760,9 +761,8 @@ __global__ void __launch_bounds__(RT, 1)
   auto issue_stage = [&](int s, const unsigned char *src, int vt) {
     const uint32_t dst = sb + (uint32_t)s * Lay::STAGE;
     const uint32_t bar = bar0 + 8u * (uint32_t)s;
-    mbar_expect_tx(bar, Lay::S_TX);
-    bulk_load(dst + S_WQ, src + I_WQ, 32768, bar);
-    bulk_load(dst + S_TAQ + 8192, src + I_AQK, 24576, bar);  // A_qk rows, then K^T
+    mbar_expect_tx(bar, Lay::S_BYTES);
+    bulk_load(dst, src, S_U, bar);  // [w ; Q e^G] | A_qk | K^T
     bulk_load(dst + S_U, src + I_U + (size_t)vt * (4096u * Lay::NT), 4096u * Lay::NT, bar);
     bulk_load(dst + Lay::S_GAM, src + I_GAM, 512, bar);
   };
@@ -799,12 +799,6 @@ __global__ void __launch_bounds__(RT, 1)
     }
   };
 
-  for (int i = tid; i < 2 * 512; i += RT) {  // rows 0..63 of [0 ; A_qk], both stages
-    const int st = i >> 9, o16 = i & 511;
-    *reinterpret_cast<uint4 *>(smem + (uint32_t)st * Lay::STAGE + S_TAQ + 16 * o16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-
   float S[CPT];  // S[key row L][col0 .. col0 + CPT - 1], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
   const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
@@ -833,11 +827,9 @@ __global__ void __launch_bounds__(RT, 1)
       for (int i = 0; i < CPT; ++i) S[i] = 0.f;
     }
     store_st(S, L);
-    if (tid == 0) {
-      issue_stage(0, item_ptr(0), vt);
-      if (n_chunks > 1) issue_stage(1, item_ptr(1), vt);
-    }
-    st_issued = n_chunks > 1 ? 3u : 1u;
+    if (tid == 0)
+      for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt);
+    st_issued = (1u << (NST < n_chunks ? NST : n_chunks)) - 1u;
     fence_proxy_async();
     wait_stage(0);
     tc_fence_before();
@@ -850,18 +842,19 @@ __global__ void __launch_bounds__(RT, 1)
       mma_commit(mma_bar);
     }
 
+    int s = 0;  // stage of chunk c
     for (int c = 0; c < n_chunks; ++c) {
-      const int s = c & 1;
+      const int s1 = s + 1 == NST ? 0 : s + 1;  // stage of chunk c + 1
       const int t0 = u.start + c * C;
       const int n = min(C, u.end - t0);
       const size_t tok0 = (size_t)b * T + t0;
       const unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
       const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
-      const uint32_t d1 = Lay::TM_D1 + (uint32_t)VTR * (uint32_t)s;
-      // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk
+      const uint32_t d1 = Lay::TM_D1 + (uint32_t)VTR * (uint32_t)(c & 1);
+      // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk (every thread
+      //      waits on the barrier itself; an abort is seen after the next
+      //      block barrier, which also keeps the phases in step)
       wait_mma();
-      __syncthreads();
-      if (*sAbort) goto done;
       tc_fence_after();
 
       // ---- P12: U = u - w S (lanes 0..63)
@@ -882,17 +875,16 @@ __global__ void __launch_bounds__(RT, 1)
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
+      if (*sAbort) goto done;
 
-      // ---- P13: D1 += [0 ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
+      // ---- P13: D1 += [* ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem + d1, sstg + S_TAQ, sb + Lay::UT, C, VTR, true, 0, 1);
+        mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
         mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 1, 1);
         mma_commit(mma_bar);
       }
       wait_mma();
-      __syncthreads();
-      if (*sAbort) goto done;
       tc_fence_after();
 
       // ---- P14: state update (all lanes = key rows), next chunk's first MMA
@@ -907,16 +899,17 @@ __global__ void __launch_bounds__(RT, 1)
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
-      if (c + 2 < n_chunks) {  // stage s is free: its MMAs and reads are done
-        if (tid == 32) issue_stage(s, item_ptr(c + 2), vt);  // beside the MMA issue
+      if (*sAbort) goto done;
+      if (c + NST < n_chunks) {  // stage s is free: its MMAs and reads are done
+        if (tid == 32) issue_stage(s, item_ptr(c + NST), vt);  // beside the MMA issue
         st_issued |= 1u << s;
       }
       if (c + 1 < n_chunks) {
-        wait_stage(s ^ 1);
+        wait_stage(s1);
         if (tid == 0) {
           tc_fence_after();
-          mma_group(tmem + Lay::TM_D1 + (uint32_t)VTR * (uint32_t)(s ^ 1),
-                    sb + (uint32_t)(s ^ 1) * Lay::STAGE + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
+          mma_group(tmem + Lay::TM_D1 + (uint32_t)VTR * (uint32_t)((c + 1) & 1),
+                    sb + (uint32_t)s1 * Lay::STAGE + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
           mma_commit(mma_bar);
         }
       }
@@ -940,6 +933,7 @@ __global__ void __launch_bounds__(RT, 1)
         }
       }
       tc_fence_before();
+      s = s1;
     }
     if (u.last && p.final_state) {
       float4 *dst = reinterpret_cast<float4 *>(
@@ -952,7 +946,7 @@ __global__ void __launch_bounds__(RT, 1)
   }
 
 done:
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < NST; ++s)
     if (st_issued & (1u << s)) mbar_wait(bar0 + 8u * s, st_phase[s]);
   if (mma_inflight) mbar_wait(mma_bar, mma_pending);
   tc_fence_before();
@@ -1014,12 +1008,15 @@ bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
   return bf16 && K == KD && V == VD && (v_tile == 0 || v_tile == 32 || v_tile == 64);
 }
 
+// Two stages in flight: a third only lengthens the copies' latency (more
+// bytes queued at the same L2 -> SM throughput) and measured slower.
+constexpr int kRecStages = 2;
 namespace {
-template <int VTR>
+template <int VTR, int NST>
 cudaError_t launch_rec(const FwdParams &p, const unsigned char *items, const ChunkTable &ct,
                        bool has_seg, cudaStream_t stream) {
-  using Lay = RecLayout<VTR>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_rec_kernel<VTR>,
+  using Lay = RecLayout<VTR, NST>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_rec_kernel<VTR, NST>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Lay::ALLOC);
   if (e != cudaSuccess) return e;
@@ -1027,7 +1024,7 @@ cudaError_t launch_rec(const FwdParams &p, const unsigned char *items, const Chu
   const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
                                : (long)p.B * p.H * p.n_vtiles;
   const int g2 = (int)(n_units < sms ? n_units : sms);
-  fwd_rec_kernel<VTR><<<g2 > 0 ? g2 : 1, RT, Lay::ALLOC, stream>>>(p, items, ct);
+  fwd_rec_kernel<VTR, NST><<<g2 > 0 ? g2 : 1, RT, Lay::ALLOC, stream>>>(p, items, ct);
   return cudaGetLastError();
 }
 }  // namespace
@@ -1083,8 +1080,8 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = p.v_tile == 32 ? launch_rec<32>(p, items, ct, has_seg, stream)
-                     : launch_rec<64>(p, items, ct, has_seg, stream);
+  e = p.v_tile == 32 ? launch_rec<32, kRecStages>(p, items, ct, has_seg, stream)
+                     : launch_rec<64, kRecStages>(p, items, ct, has_seg, stream);
   if (e != cudaSuccess || !with_fallback || !has_seg) return e;
   // The fused kernel covers calls whose runs overflow the items (it exits
   // at once when they fit).
