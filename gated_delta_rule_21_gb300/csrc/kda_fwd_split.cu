@@ -281,15 +281,21 @@ __global__ void __launch_bounds__(PT, 2)
   if (n_chunk_items > ct.capacity && ct.report_overflow && tid == 0 && blockIdx.x == 0)
     set_status(p.status, KDA_DEVICE_WORKSPACE);  // the items cannot hold every chunk
   const uint32_t n_items = n_chunk_items > ct.capacity ? 0u : n_chunk_items * (uint32_t)H;
-  auto item_coords = [&](uint32_t it, int &b, int &t0, int &end, int &h) {
-    h = (int)(it % (uint32_t)H);
-    chunk_of(ct, p.runs, p.B, T, it / (uint32_t)H, b, t0, end);
+  // Where an item's tokens are (with segment ids, two binary searches over
+  // global tables): computed once per item and carried to the next iteration.
+  struct Coords {
+    int b, t0, end, h;
+  };
+  auto item_coords = [&](uint32_t it) {
+    Coords x;
+    x.h = (int)(it % (uint32_t)H);
+    chunk_of(ct, p.runs, p.B, T, it / (uint32_t)H, x.b, x.t0, x.end);
+    return x;
   };
   // Both issue functions are called by all 32 lanes of one warp: lane 0
   // arms the barrier, then one box per lane.
-  auto issue_raw = [&](uint32_t it, int half) {  // q, k, g of one channel half
-    int b, t0, end, h;
-    item_coords(it, b, t0, end, h);
+  auto issue_raw = [&](const Coords &xc, int half) {  // q, k, g of one channel half
+    const int b = xc.b, t0 = xc.t0, h = xc.h;
     const int y = b * T + t0, x = h * KD + KH * half;
     if (lane == 0) mbar_expect_tx(raw_bar, P_RAW_TX);
     __syncwarp();
@@ -299,38 +305,36 @@ __global__ void __launch_bounds__(PT, 2)
   };
   // v as 16 column groups of 8, each 64 rows x 16 bytes: the MN-major layout
   // of the V part of RHST (read by the [w | u] MMA).
-  auto issue_v = [&](uint32_t it) {
-    int b, t0, end, h;
-    item_coords(it, b, t0, end, h);
+  auto issue_v = [&](const Coords &xc) {
+    const int b = xc.b, t0 = xc.t0, h = xc.h;
     const int y = b * T + t0;
     if (lane == 0) mbar_expect_tx(v_bar, P_V_TX);
     __syncwarp();
     if (lane < VD / 8)
       tma_load_2d(sb + P_RHST + mn_off(KD + 8 * lane, 0, C), &tm_v, h * VD + 8 * lane, y, v_bar);
   };
-  auto load_beta = [&](uint32_t it) -> float {
-    int b, t0, end, h;
-    item_coords(it, b, t0, end, h);
-    const int t = t0 + tid;
-    return t < end ? p.beta[((size_t)b * T + t) * H + h] : 0.f;
+  auto load_beta = [&](const Coords &xc) -> float {
+    const int t = xc.t0 + tid;
+    return t < xc.end ? p.beta[((size_t)xc.b * T + t) * H + xc.h] : 0.f;
   };
 
   uint32_t item = blockIdx.x;
   float beta_next = 0.f;
+  Coords cur = {0, 0, 0, 0};
   if (item < n_items) {
-    if (warp == 0) issue_raw(item, 0);
-    if (warp == 1) issue_v(item);
+    cur = item_coords(item);
+    if (warp == 0) issue_raw(cur, 0);
+    if (warp == 1) issue_v(cur);
     raw_inflight = v_inflight = true;
     raw_pending = raw_phase;
     v_pending = v_phase;
-    if (tid < C) beta_next = load_beta(item);
+    if (tid < C) beta_next = load_beta(cur);
   }
   for (; item < n_items; item += gridDim.x) {
-    int b_, t0_, end_, h_;
-    item_coords(item, b_, t0_, end_, h_);
-    const int n = min(C, end_ - t0_);
+    const int n = min(C, cur.end - cur.t0);
     const uint32_t next = item + gridDim.x;
     const bool has_next = next < n_items;
+    const Coords nxt = has_next ? item_coords(next) : cur;
     unsigned char *gi = items + (size_t)item * ITEM_BYTES;
     if (tid < C) sBeta[tid] = beta_next;
 
@@ -464,12 +468,12 @@ __global__ void __launch_bounds__(PT, 2)
         mma_group(tmem, sb + P_X, sb + P_Y, KH, 160, half > 0, 0, 0);
         mma_commit(mma_bar);
       }
-      if (half == 0 && warp == 1) issue_raw(item, 1);  // the raw tiles are consumed
+      if (half == 0 && warp == 1) issue_raw(cur, 1);  // the raw tiles are consumed
       if (half == 0) {
         raw_inflight = true;
         raw_pending = raw_phase;
       }
-      if (half == 1 && has_next && tid < C) beta_next = load_beta(next);
+      if (half == 1 && has_next && tid < C) beta_next = load_beta(nxt);
       wait_mma();  // X / Y are free again (and, after half 1, A is in TMEM)
     }
     fence_proxy_async();
@@ -631,8 +635,8 @@ __global__ void __launch_bounds__(PT, 2)
     if (*sAbort) goto done;
     tc_fence_after();
     if (has_next) {  // RAW, the solver buffers and RHST are free: next item's tiles
-      if (warp == 0) issue_raw(next, 0);
-      if (warp == 1) issue_v(next);
+      if (warp == 0) issue_raw(nxt, 0);
+      if (warp == 1) issue_v(nxt);
       raw_inflight = v_inflight = true;
       raw_pending = raw_phase;
       v_pending = v_phase;
@@ -674,6 +678,7 @@ __global__ void __launch_bounds__(PT, 2)
     }
     tc_fence_before();
     __syncthreads();
+    cur = nxt;
   }
 
 done:
