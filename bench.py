@@ -415,10 +415,11 @@ def run_ours(args, dist):
                           "unit": "tokens/s", "roofline": roofline(packed),
                           "vs_pages_tpu": (packed["tokens"] / (packed["ms_max"] * 1e-3))
                           / (pw.B * pw.T / (PAGES_TPU_PACKED_MS * 1e-3)),
-                          # run builder, then prep + recurrence (+ the fused kernel
-                          # AUTO enqueues gated on an overflow of the split items)
-                          "gpu_launches": (1 + ((3 if args.kda_impl == "auto" else 2)
-                                                if kernel_impl(pw) == "split" else 1)) * args.steps}
+                          # run builder (+ the chunk table for the split path), then
+                          # prep + recurrence (+ the fused kernel AUTO enqueues gated
+                          # on an overflow of the split items)
+                          "gpu_launches": ((5 if args.kda_impl == "auto" else 4)
+                                           if kernel_impl(pw) == "split" else 2) * args.steps}
         line["gpu_launches"] += line["packed"]["gpu_launches"]
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, budget_s=args.cpu_seconds)

@@ -142,6 +142,7 @@ __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
 struct ChunkTable {
   const int32_t *run_chunk_base;     // [B*T] or nullptr (no segment ids)
   const int32_t *chunk_row_offsets;  // [B+1]
+  const int2 *coords;                // [B*T]: {b*T + first token, tokens} per chunk
   const uint32_t *total_chunks;      // device count
   uint32_t capacity;                 // chunk items the workspace holds
   int n_chunks_row;                  // chunks per row without segment ids
@@ -153,30 +154,18 @@ __device__ __forceinline__ uint32_t total_chunk_count(const ChunkTable &ct, int 
 }
 
 // First token and end of chunk k, and its row.
-__device__ __forceinline__ void chunk_of(const ChunkTable &ct, const RunTable &rt, int B,
-                                         int T, uint32_t k, int &b, int &t0, int &end) {
+__device__ __forceinline__ void chunk_of(const ChunkTable &ct, int T, uint32_t k, int &b,
+                                         int &t0, int &end) {
   if (!ct.run_chunk_base) {
     b = (int)(k / (uint32_t)ct.n_chunks_row);
     t0 = (int)(k % (uint32_t)ct.n_chunks_row) * C;
     end = T;
     return;
   }
-  int lo = 0, hi = B;  // chunk_row_offsets[lo] <= k < chunk_row_offsets[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((uint32_t)ct.chunk_row_offsets[mid] <= k) lo = mid; else hi = mid;
-  }
-  b = lo;
-  const int kk = (int)k - ct.chunk_row_offsets[lo];
-  const int32_t *base = ct.run_chunk_base + (size_t)lo * T;
-  int rl = 0, rh = rt.row_offsets[lo + 1] - rt.row_offsets[lo];  // runs of row
-  while (rh - rl > 1) {
-    const int mid = (rl + rh) >> 1;
-    if (base[mid] <= kk) rl = mid; else rh = mid;
-  }
-  const int2 run = rt.runs[(size_t)lo * T + rl];
-  t0 = run.x + (kk - base[rl]) * C;
-  end = run.y;
+  const int2 e = ct.coords[k];
+  b = e.x / T;
+  t0 = e.x - b * T;
+  end = t0 + e.y;
 }
 
 __device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const float (&v)[8]) {
@@ -289,7 +278,7 @@ __global__ void __launch_bounds__(PT, 2)
   auto item_coords = [&](uint32_t it) {
     Coords x;
     x.h = (int)(it % (uint32_t)H);
-    chunk_of(ct, p.runs, p.B, T, it / (uint32_t)H, x.b, x.t0, x.end);
+    chunk_of(ct, T, it / (uint32_t)H, x.b, x.t0, x.end);
     return x;
   };
   // Both issue functions are called by all 32 lanes of one warp: lane 0
@@ -1059,9 +1048,11 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
     ct.chunk_row_offsets = reinterpret_cast<const int32_t *>(
         ws + ws_bytes(p.B, p.T, true) + align_up(sizeof(int32_t) * (size_t)p.B * p.T, 256));
     ct.total_chunks = &reinterpret_cast<const WsHeader *>(ws)->total_chunks;
+    ct.coords = reinterpret_cast<const int2 *>(ws + ws_chunk_coords_offset(p.B, p.T));
   } else {
     ct.run_chunk_base = nullptr;
     ct.chunk_row_offsets = nullptr;
+    ct.coords = nullptr;
     ct.total_chunks = nullptr;
   }
   const uint64_t rows = (uint64_t)p.B * p.T;

@@ -45,9 +45,16 @@ inline size_t ws_bytes(int B, int T, bool has_seg) {
 // The split path with segment ids appends, after ws_bytes(B, T, true):
 //   int32 run_chunk_base[B*T] (first chunk of run i of row b, within the row),
 //   int32 chunk_row_offsets[B+1] (prefix of chunk counts over rows),
+//   int2 chunk_coords[B*T] ({b*T + first token, tokens} of every chunk, in
+//   chunk order; a row of T tokens has at most T chunks),
 // then its per-chunk items.
+inline size_t ws_chunk_coords_offset(int B, int T) {
+  return ws_bytes(B, T, true) + align_up(sizeof(int32_t) * (size_t)B * T, 256) +
+         ws_row_offsets_bytes(B);
+}
 inline size_t ws_chunk_tables_bytes(int B, int T) {
-  return align_up(sizeof(int32_t) * (size_t)B * T, 256) + ws_row_offsets_bytes(B);
+  return align_up(sizeof(int32_t) * (size_t)B * T, 256) + ws_row_offsets_bytes(B) +
+         align_up(sizeof(int2) * (size_t)B * T, 256);
 }
 
 // Where one unit of work lives: a run of one row, for one head, for one

@@ -201,6 +201,24 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Every chunk of every run, in chunk order: {b*T + first token, tokens}, so
+// that the split path's per-chunk work finds its tokens with one load.  One
+// thread per (row, run index).
+__global__ void __launch_bounds__(256)
+    chunk_coords_kernel(int B, int T, const int32_t *__restrict__ row_offsets,
+                        const int2 *__restrict__ runs, const int32_t *__restrict__ run_chunk_base,
+                        const int32_t *__restrict__ chunk_row_offsets, int2 *coords) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * T) return;
+  const int b = (int)(idx / (size_t)T), i = (int)(idx % (size_t)T);
+  if (i >= row_offsets[b + 1] - row_offsets[b]) return;
+  const int2 r = runs[idx];
+  const int k0 = chunk_row_offsets[b] + run_chunk_base[idx];
+  const int y0 = b * T + r.x;
+  for (int j = 0, t = 0; t < r.y - r.x; ++j, t += kChunk)
+    coords[k0 + j] = make_int2(y0 + t, min(kChunk, r.y - r.x - t));
+}
+
 }  // namespace
 
 cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
@@ -222,6 +240,12 @@ cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
   segment_runs_kernel<<<B, kThreads, 0, stream>>>(
       B, T, H, K, V, segment_ids, static_cast<char *>(o), o_is_bf16 ? 2 : 4,
       initial_state, final_state, hdr, row_offsets, runs, chunk_base, chunk_rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !with_chunks) return e;
+  int2 *coords = reinterpret_cast<int2 *>(ws + ws_chunk_coords_offset(B, T));
+  const size_t n = (size_t)B * T;
+  chunk_coords_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+      B, T, row_offsets, runs, chunk_base, chunk_rows, coords);
   return cudaGetLastError();
 }
 
