@@ -92,6 +92,8 @@ def lib():
         L.kda_impl_available.restype = i
         L.kda_version.argtypes = []
         L.kda_version.restype = i
+        L.kda_selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
+        L.kda_selftest_wait_timeout.restype = i
         _lib = L
         return L
 
@@ -258,6 +260,16 @@ def read_device_status(workspace, stream=None) -> int:
     if st not in (KDA_OK, 4, 6, 7):
         raise KdaError(st, "kda_read_device_status")
     return int(bits.value)
+
+
+def selftest_wait_timeout(workspace, limit_cycles=1 << 20, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: one device wait that nothing ends,
+    given up after ``limit_cycles`` SM clocks, reported as KDA_DEVICE_TIMEOUT
+    in ``workspace``'s status word (read it with read_device_status)."""
+    st = lib().kda_selftest_wait_timeout(_ptr(workspace), int(limit_cycles),
+                                         _stream_ptr(stream, workspace.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_wait_timeout")
 
 
 def clear_device_status(workspace, stream=None) -> None:

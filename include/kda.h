@@ -257,6 +257,19 @@ KDA_API kda_status kda_read_device_status(const void *workspace, kda_stream_t st
 /* Enqueues a reset of the device status word to zero on `stream`. */
 KDA_API kda_status kda_clear_device_status(void *workspace, kda_stream_t stream);
 
+/*
+ * Test hook for failure detection (no counterpart in the pages): enqueues
+ * one thread that waits, for at most `limit_cycles` SM clocks (1 .. about
+ * 2^31), on an mbarrier nothing ever arrives at, using the bounded wait of
+ * the tensor-core kernels; when the limit runs out it sets
+ * KDA_DEVICE_TIMEOUT in the status word of `workspace` (a zero-filled
+ * workspace of any size >= 256 bytes), which kda_read_device_status then
+ * reports.  Nothing faults or hangs; the context stays usable.
+ * KDA_ERR_INVALID_ARG for a NULL workspace or a limit out of range.
+ */
+KDA_API kda_status kda_selftest_wait_timeout(void *workspace, long long limit_cycles,
+                                             kda_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 KDA_API const char *kda_status_string(kda_status status);
 
