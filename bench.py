@@ -337,15 +337,30 @@ def run_ours(args, dist):
         h2d = sum(host[n].numel() * host[n].element_size() for n in names)
         d2h = o_h.numel() * o_h.element_size() + fs_h.numel() * fs_h.element_size()
 
-        def e2e_step():
-            for n in names:
-                d[n].copy_(host[n], non_blocking=True)
-            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
-                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
-                          output_final_state=True, out=o, final_state_out=fs,
-                          workspace=ws, impl=args.kda_impl, v_tile=args.v_tile, stream=stream)
-            o_h.copy_(o, non_blocking=True)
-            fs_h.copy_(fs, non_blocking=True)
+        if args.kda_impl == "auto" and args.v_tile == 0:
+            # the library's host-buffer call: copies in, forward, copies out,
+            # pipelined by head groups
+            dbuf = torch.zeros(kda.host_buffer_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype,
+                                                    has_seg),
+                               dtype=torch.uint8, device=d["q"].device)
+
+            def e2e_step():
+                kda.chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                                   scale=x["scale"], initial_state=host.get("initial_state"),
+                                   segment_ids=host.get("segment_ids"), output_final_state=True,
+                                   out=o_h, final_state_out=fs_h, device_buffer=dbuf,
+                                   stream=stream)
+        else:
+            def e2e_step():
+                for n in names:
+                    d[n].copy_(host[n], non_blocking=True)
+                kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                              initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                              output_final_state=True, out=o, final_state_out=fs,
+                              workspace=ws, impl=args.kda_impl, v_tile=args.v_tile,
+                              stream=stream)
+                o_h.copy_(o, non_blocking=True)
+                fs_h.copy_(fs, non_blocking=True)
 
         times, _ = time_steps(e2e_step, args.steps, args.warmup, stream, flush, dist)
         ms = dist.max(statistics.mean(times))

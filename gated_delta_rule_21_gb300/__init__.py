@@ -92,6 +92,11 @@ def lib():
         L.kda_impl_available.restype = i
         L.kda_version.argtypes = []
         L.kda_version.restype = i
+        L.kda_chunk_fwd_host_buffer_size.argtypes = [sp, i]
+        L.kda_chunk_fwd_host_buffer_size.restype = u64
+        L.kda_chunk_fwd_host.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp,
+                                         vp, vp, u64, vp]
+        L.kda_chunk_fwd_host.restype = i
         L.kda_selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
         L.kda_selftest_wait_timeout.restype = i
         _lib = L
@@ -250,6 +255,58 @@ def short_conv_silu(x_q, x_k, x_v, w, segment_ids=None, l2norm_qk=True,
     if st != KDA_OK:
         raise KdaError(st, "kda_short_conv_silu")
     return q, k, v
+
+
+def host_buffer_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
+    """Bytes of device memory chunk_fwd_host needs for this shape."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_host_buffer_size(ctypes.byref(s), 1 if has_segment_ids else 0))
+
+
+def chunk_fwd_host(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None,
+                   segment_ids=None, output_final_state=False, out=None,
+                   final_state_out=None, device_buffer=None, stream=None):
+    """End-to-end forward on HOST tensors (pin them for asynchronous copies):
+    the library copies the inputs in, runs the forward and copies o (and the
+    final state) back, pipelined by head groups.  ``device_buffer`` is a
+    zero-filled CUDA uint8 tensor of host_buffer_size() bytes (allocated here
+    when None).  The host outputs are valid once ``stream`` synchronises.
+    Returns ``(o, final_state or None)`` (CPU tensors)."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    cpu = torch.device("cpu")
+    dt = q.dtype
+    for t, name, shape, tdt in ((q, "q", (B, T, H, K), dt), (k, "k", (B, T, H, K), dt),
+                                (v, "v", (B, T, H, V), dt),
+                                (g, "g", (B, T, H, K), torch.float32),
+                                (beta, "beta", (B, T, H), torch.float32),
+                                (initial_state, "initial_state", (B, H, K, V), torch.float32),
+                                (segment_ids, "segment_ids", (B, T), torch.int32)):
+        _check(t, name, shape, tdt, cpu)
+    if scale is None:
+        scale = K ** -0.5
+    o = out if out is not None else torch.empty(B, T, H, V, dtype=dt).pin_memory()
+    _check(o, "out", (B, T, H, V), dt, cpu)
+    fs = None
+    if output_final_state:
+        fs = final_state_out if final_state_out is not None else torch.empty(
+            B, H, K, V, dtype=torch.float32).pin_memory()
+        _check(fs, "final_state_out", (B, H, K, V), torch.float32, cpu)
+    n = host_buffer_size(B, T, H, K, V, dt, segment_ids is not None)
+    if n == 0:
+        raise KdaError(2, "kda_chunk_fwd_host_buffer_size")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if device_buffer is None:
+        device_buffer = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_fwd_host(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        int(chunk_size), _ptr(initial_state), _ptr(segment_ids), _ptr(o), _ptr(fs),
+        _ptr(device_buffer), int(device_buffer.numel() * device_buffer.element_size()),
+        _stream_ptr(stream, device_buffer.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_host")
+    return o, fs
 
 
 def read_device_status(workspace, stream=None) -> int:

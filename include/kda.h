@@ -258,6 +258,35 @@ KDA_API kda_status kda_read_device_status(const void *workspace, kda_stream_t st
 KDA_API kda_status kda_clear_device_status(void *workspace, kda_stream_t stream);
 
 /*
+ * End to end on HOST buffers (an API shape of this library, not of the
+ * pages): q, k, v, g, beta, initial_state, segment_ids, o and final_state
+ * are host pointers in the layouts of kda_chunk_fwd (pin them with
+ * cudaHostAlloc or cudaHostRegister, else the copies are synchronous).
+ * The call copies the inputs in, runs the forward and copies o and
+ * final_state back, pipelined by groups of heads: each group's copies in,
+ * forward and copies out run on an internal stream, the copies in chained
+ * group after group, so one group's compute overlaps the next groups'
+ * copies.  The work is ordered after prior work on `stream`, and later work
+ * on `stream` waits for it; the host outputs are valid once `stream`
+ * synchronises.  `device_buffer` (caller-owned, 256-byte aligned,
+ * zero-filled before its first use, reusable) holds the device copies and
+ * the per-group workspaces: kda_chunk_fwd_host_buffer_size bytes.  The
+ * library creates its internal streams and events once per device and
+ * keeps them for the process lifetime; enqueues are serialised by a mutex.
+ * Errors: as kda_chunk_fwd (KDA_ERR_WORKSPACE for a small device_buffer,
+ * KDA_ERR_ALIGNMENT for a misaligned one); a CUDA error while enqueuing
+ * returns KDA_ERR_CUDA with part of the work possibly enqueued.
+ */
+KDA_API size_t kda_chunk_fwd_host_buffer_size(const kda_shape *s, int has_segment_ids);
+KDA_API kda_status kda_chunk_fwd_host(const kda_shape *s, const void *q, const void *k,
+                                      const void *v, const float *g, const float *beta,
+                                      float scale, int chunk_size,
+                                      const float *initial_state,
+                                      const int32_t *segment_ids, void *o,
+                                      float *final_state, void *device_buffer,
+                                      size_t device_buffer_bytes, kda_stream_t stream);
+
+/*
  * Test hook for failure detection (no counterpart in the pages): enqueues
  * one thread that waits, for at most `limit_cycles` SM clocks (1 .. about
  * 2^31), on an mbarrier nothing ever arrives at, using the bounded wait of
