@@ -332,6 +332,7 @@ __global__ void __launch_bounds__(PT, 2)
     const int cc0 = cg * 8;
     for (int half = 0; half < 2; ++half) {
       const int ch0 = KH * half + cc0;  // first of this thread's channels (global)
+      // ---- P17: this half's raw tiles
       wait_raw();
       __syncthreads();
       if (*sAbort) goto done;
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(PT, 2)
         raw_pending = raw_phase;
       }
       if (half == 1 && has_next && tid < C) beta_next = load_beta(nxt);
+      // ---- P16: the A products of this half
       wait_mma();  // X / Y are free again (and, after half 1, A is in TMEM)
     }
     fence_proxy_async();
