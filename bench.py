@@ -51,6 +51,7 @@ KERNEL_NAMES = {"simt": "fwd_simt_kernel", "tc": "fwd_tc_kernel",
                 "split": "fwd_prep_kernel + fwd_rec_kernel"}
 HEADLINE = "fixed_bf16_h32_t8192"
 PACKED = "packed_bf16_h32_t8192_25seg"
+PROLOGUE = "packed_bf16_h32_t8192_25seg_conv"   # the packed shape behind the conv prologue
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -101,7 +102,8 @@ def measured_peaks():
 
 
 def kernel_source_digest(impl_name: str) -> str:
-    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu"}[impl_name]
+    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu",
+             "conv": "kda_conv.cu"}[impl_name]
     path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -384,6 +386,56 @@ def run_ours(args, dist):
                 "tensor_frac": round(flops / t / 1e12 / tc_peak, 4),
                 "roofline_ms": round(max(nbytes / (hbm_peak * 1e9), flops / (tc_peak * 1e12)) * 1e3, 4)}
 
+    def measure_prologue(wname):
+        """The short-conv prologue (conv + SiLU + L2 on q, k) alone and followed
+        by the forward, on the packed shape with pre-conv inputs."""
+        w = ki.WORKLOADS[wname]
+        x = ki.make_inputs(w, seed=args.seed + dist.rank)
+        d = device_inputs(x, dev)
+        cw = x["conv_w"].to(dev)
+        o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
+        fs = torch.empty(w.B, w.H, w.K, w.V, dtype=torch.float32, device=dev)
+        ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, True, dev,
+                                 impl=args.kda_impl, max_runs_per_row=len(w.segments))
+
+        def conv():
+            return kda.short_conv_silu(d["q"], d["k"], d["v"], cw, segment_ids=d["segment_ids"],
+                                       l2norm_qk=True, stream=stream)
+
+        def full():
+            q, k_, v = conv()
+            kda.chunk_fwd(q, k_, v, d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                          output_final_state=True, out=o, final_state_out=fs, workspace=ws,
+                          impl=args.kda_impl, v_tile=args.v_tile, stream=stream)
+
+        t_conv, _ = time_steps(conv, args.steps, args.warmup, stream, flush, dist)
+        t_full, _ = time_steps(full, args.steps, args.warmup, stream, flush, dist)
+        conv_ms = dist.max(statistics.mean(t_conv))
+        full_ms = dist.max(statistics.mean(t_full))
+        esz = d["q"].element_size()
+        # reads x_q, x_k, x_v, the weights and the ids; writes q, k, v
+        conv_bytes = (2 * w.B * w.T * w.H * (2 * w.K + w.V) * esz
+                      + 4 * 4 * w.H * (2 * w.K + w.V) + 4 * w.B * w.T)
+        gbs = conv_bytes / (conv_ms * 1e-3) / 1e9
+        return {"workload": w.name, "conv_ms": conv_ms,
+                "conv_roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                                  "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                  "traffic": profiled_traffic("conv", w.name),
+                                  "algorithmic_bytes": conv_bytes, "kernel": "short_conv_kernel"},
+                "ms_per_step": full_ms, "unit": "tokens/s",
+                "value": whole_job_value(dist.world, w.B * w.T, full_ms),
+                # the conv leg, then conv + the packed forward
+                "gpu_launches": args.steps * (2 + packed_launches(w))}
+
+    def packed_launches(w):
+        """Kernels one packed forward launches: segment runs, chunk
+        coordinates, prep, recurrence (+ the fused kernel AUTO enqueues
+        gated on an overflow of the split items); 2 on the one-kernel paths."""
+        if kernel_impl(w) == "split":
+            return 5 if args.kda_impl == "auto" else 4
+        return 2
+
     def kernel_impl(w):
         import gated_delta_rule_21_gb300 as kda
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -398,6 +450,8 @@ def run_ours(args, dist):
     head = measure(args.workload, with_e2e=not args.no_e2e, clocks_=clocks)
     packed = (measure(PACKED, with_e2e=False)
               if args.workload == HEADLINE and not args.no_packed else None)
+    prologue = (measure_prologue(PROLOGUE)
+                if args.workload == HEADLINE and not args.no_prologue else None)
     clk = clocks.stop()
 
     w = head["workload"]
@@ -431,11 +485,11 @@ def run_ours(args, dist):
                           "vs_pages_tpu": (packed["tokens"] / (packed["ms_max"] * 1e-3))
                           / (pw.B * pw.T / (PAGES_TPU_PACKED_MS * 1e-3)),
                           # run builder (+ the chunk table for the split path), then
-                          # prep + recurrence (+ the fused kernel AUTO enqueues gated
-                          # on an overflow of the split items)
-                          "gpu_launches": ((5 if args.kda_impl == "auto" else 4)
-                                           if kernel_impl(pw) == "split" else 2) * args.steps}
+                          "gpu_launches": packed_launches(pw) * args.steps}
         line["gpu_launches"] += line["packed"]["gpu_launches"]
+    if prologue is not None:
+        line["prologue"] = prologue
+        line["gpu_launches"] += prologue["gpu_launches"]
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, budget_s=args.cpu_seconds)
     return line
@@ -521,6 +575,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--no-packed", action="store_true", help="skip the packed N=25 leg")
+    ap.add_argument("--no-prologue", action="store_true",
+                    help="skip the conv prologue leg (packed N=25 shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -234,7 +234,8 @@ kda_status kda_short_conv_silu(const kda_shape *s, const void *x_q,
   for (const void *ptr : ptrs)
     if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
   if (x_q == q || x_k == k || x_v == v) return KDA_ERR_INVALID_ARG;
-  if ((long long)s->B * ((s->T + 31) / 32) > 65535) return KDA_ERR_UNSUPPORTED;
+  // grid.y = B x tiles of 24 tokens
+  if ((long long)s->B * ((s->T + 23) / 24) > 65535) return KDA_ERR_UNSUPPORTED;
   ConvParams p;
   memset(&p, 0, sizeof(p));
   p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;

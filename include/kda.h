@@ -230,13 +230,18 @@ KDA_API int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile);
  *     y_t[c] = SiLU( sum_{i=0}^{3} w[c][3-i] * x_{t-i}[c] )
  * with taps before t = 0 or before the start of t's run equal to zero, no
  * bias, and y = 0 on padding tokens.  With l2norm_qk != 0, q and k are then
- * scaled per (token, head) by 1 / sqrt(sum y^2 + 1e-6).  fp32 arithmetic.
+ * scaled per (token, head) by 1 / sqrt(sum y^2 + 1e-6).  fp32 arithmetic;
+ * the sigmoid uses the approximate exp2 and reciprocal instructions
+ * (relative error a few fp32 ulp); bf16 outputs are rounded to nearest.
  *   x_q, x_k      device [B,T,H,K] of s->qkv_dtype; x_v [B,T,H,V].
  *   w             device float32, three weight blocks back to back:
  *                 w_q [H*K][4], w_k [H*K][4], w_v [H*V][4].
  *   segment_ids   device int32 [B,T] or NULL.
  *   q, k, v       device outputs, same shapes and dtype as the inputs; they
  *                 must not alias the inputs.
+ * Every pointer must be 16-byte aligned (KDA_ERR_ALIGNMENT).  Returns
+ * KDA_ERR_UNSUPPORTED when B * ceil(T / 24) exceeds 65535; the call is
+ * asynchronous on `stream`.
  */
 KDA_API kda_status kda_short_conv_silu(const kda_shape *s, const void *x_q,
                                const void *x_k, const void *x_v,

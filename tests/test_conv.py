@@ -53,6 +53,30 @@ def test_conv_matches_oracle(dtype, l2, shape):
     assert torch.all(q.cpu()[pad] == 0) and torch.all(v.cpu()[pad] == 0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_conv_short_runs_several_channel_blocks(dtype):
+    """Runs of 1-5 tokens, padding between and at the start, run starts on
+    and next to the 24-token tile edges, 2048 channels per tensor (two
+    1024-channel blocks) and a ragged last tile."""
+    import gated_delta_rule_21_gb300 as kda
+    B, T, H, K, V = 2, 203, 16, 128, 128
+    rows = [[("pad", 1), 1, 2, 3, ("pad", 2), 1, 5, 9, 24, 1, 23, ("pad", 3), 2, 48, 1, 1, 30, 46],
+            [22, 2, 1, 24, 25, ("pad", 1), 1, 3, 60, 4, 4, 50]]
+    w_ = ki.custom_workload(B, T, H, K, V, dtype=dtype, prologue=True, segments=rows)
+    x = ki.make_inputs(w_, seed=11)
+    seg = x["segment_ids"]
+    q, k, v = kda.short_conv_silu(to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]),
+                                  to_dev(x["conv_w"]), segment_ids=to_dev(seg), l2norm_qk=True)
+    refs = oracle_prologue(x, x["conv_w"], seg.numpy(), True, H, K, V, store_bf16=False)
+    for got, ref, name in zip((q, k, v), refs, "qkv"):
+        g = got.double().cpu().numpy()
+        tol = (1.02 * 2.0 ** -8 if dtype == "bf16" else 1e-5) * np.abs(ref) + 1e-6
+        bad = np.abs(g - ref) > tol
+        assert not bad.any(), f"{name}: {bad.sum()} elements off, max {np.abs(g - ref).max():.3e}"
+    pad = torch.from_numpy((seg == 0).numpy())
+    assert torch.all(k.cpu()[pad] == 0) and torch.all(v.cpu()[pad] == 0)
+
+
 def test_prologue_then_chunk_fwd_packed_n25():
     """Prologue (conv + SiLU + L2 on q, k) followed by the chunked forward
     on the packed B=1 H=32 T=8192 K=V=128 shape with 25 segments, against
