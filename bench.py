@@ -341,7 +341,7 @@ def run_ours(args, dist):
 
         if args.kda_impl == "auto" and args.v_tile == 0:
             # the library's host-buffer call: copies in, forward, copies out,
-            # pipelined by head groups
+            # pipelined over token ranges
             dbuf = torch.zeros(kda.host_buffer_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype,
                                                     has_seg),
                                dtype=torch.uint8, device=d["q"].device)

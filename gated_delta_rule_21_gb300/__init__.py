@@ -268,7 +268,8 @@ def chunk_fwd_host(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state
                    final_state_out=None, device_buffer=None, stream=None):
     """End-to-end forward on HOST tensors (pin them for asynchronous copies):
     the library copies the inputs in, runs the forward and copies o (and the
-    final state) back, pipelined by head groups.  ``device_buffer`` is a
+    final state) back, pipelined over token ranges (over head groups with
+    segment ids).  ``device_buffer`` is a
     zero-filled CUDA uint8 tensor of host_buffer_size() bytes (allocated here
     when None).  The host outputs are valid once ``stream`` synchronises.
     Returns ``(o, final_state or None)`` (CPU tensors)."""

@@ -268,14 +268,20 @@ KDA_API kda_status kda_clear_device_status(void *workspace, kda_stream_t stream)
  * are host pointers in the layouts of kda_chunk_fwd (pin them with
  * cudaHostAlloc or cudaHostRegister, else the copies are synchronous).
  * The call copies the inputs in, runs the forward and copies o and
- * final_state back, pipelined by groups of heads: each group's copies in,
- * forward and copies out run on an internal stream, the copies in chained
- * group after group, so one group's compute overlaps the next groups'
- * copies.  The work is ordered after prior work on `stream`, and later work
+ * final_state back, with the copies overlapped with the compute.  Without
+ * segment ids it pipelines over time: the tokens are split into ranges of
+ * a multiple of 64 tokens (at least 512, at most 8 ranges), each range's
+ * forward enters with the exact fp32 state the previous one left, and the
+ * copies in, the forwards and the copies out run on three internal streams,
+ * so the result is bitwise that of kda_chunk_fwd on the whole input.  With
+ * segment ids it pipelines over two groups of heads (each group's copies
+ * in, forward and copies out on an internal stream, the copies in chained
+ * group after group), again bitwise equal to kda_chunk_fwd.  The work is
+ * ordered after prior work on `stream`, and later work
  * on `stream` waits for it; the host outputs are valid once `stream`
  * synchronises.  `device_buffer` (caller-owned, 256-byte aligned,
  * zero-filled before its first use, reusable) holds the device copies and
- * the per-group workspaces: kda_chunk_fwd_host_buffer_size bytes.  The
+ * the workspaces: kda_chunk_fwd_host_buffer_size bytes.  The
  * library creates its internal streams and events once per device and
  * keeps them for the process lifetime; enqueues are serialised by a mutex.
  * Errors: as kda_chunk_fwd (KDA_ERR_WORKSPACE for a small device_buffer,

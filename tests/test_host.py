@@ -1,7 +1,9 @@
-"""The host-buffer entry point (copies in, forward, copies out, pipelined by
-head groups): argument checks on the host, and on the GPU bitwise equality
-with the device entry point on the same inputs (the per-group forward runs
-the same kernels on the same per-head data) plus oracle parity."""
+"""The host-buffer entry point (copies in, forward, copies out, pipelined
+over token ranges without segment ids and over head groups with them):
+argument checks on the host, and on the GPU bitwise equality with the device
+entry point on the same inputs (each range's forward enters with the exact
+fp32 state the previous range left; each head group's forward runs the same
+kernels on the same per-head data) plus oracle parity."""
 import ctypes
 
 import numpy as np
@@ -41,12 +43,21 @@ def _pinned(x):
     return None if x is None else x.contiguous().pin_memory()
 
 
+# Several token ranges (512 tokens each, a ragged last one), B > 1, with and
+# without an initial state, and the fp32 paths.
+HOST_CASES = {
+    "b2_bf16_h4_t1600_s0": dict(B=2, T=1600, H=4, K=128, V=128, dtype="bf16", init_state_std=0.1),
+    "b3_bf16_h2_t1100": dict(B=3, T=1100, H=2, K=128, V=128, dtype="bf16"),
+    "b2_fp32_h2_t1030_d64_s0": dict(B=2, T=1030, H=2, K=64, V=64, dtype="f32", init_state_std=0.1),
+}
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg",
-                                  "tiny_fp32_h2_t128_d32"])
+                                  "tiny_fp32_h2_t128_d32"] + sorted(HOST_CASES))
 def test_host_matches_device_path(name):
     import gated_delta_rule_21_gb300 as kda
-    w = ki.WORKLOADS[name]
+    w = ki.WORKLOADS[name] if name in ki.WORKLOADS else ki.custom_workload(**HOST_CASES[name])
     x = ki.make_inputs(w, seed=7)
     o_d, fs_d = run_gpu(x)
     h = {n: _pinned(x[n]) for n in ("q", "k", "v", "g", "beta", "initial_state", "segment_ids")}
