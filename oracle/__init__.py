@@ -17,6 +17,9 @@ and CP support":
   depthwise conv + SiLU), segment-aware.
 * :func:`l2norm` -- section "Layer architecture", step 5 / "Public API"
   ``use_qk_l2norm_in_kernel``.
+* :func:`kda_backward` -- the gradient of :func:`kda_forward` (its
+  vector-Jacobian product), reverse-mode differentiation of the same token
+  recurrence written out step by step (C, ``kda_ref_bwd.c``).
 
 Pins (tests/test_oracle.py) check these against closed forms, invariants and an
 independent brute-force transcription; see the test file for which property
@@ -32,7 +35,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "kda_ref.c")
+_SRCS = [os.path.join(_HERE, "kda_ref.c"), os.path.join(_HERE, "kda_ref_bwd.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkda_ref.so")
 
@@ -41,18 +44,19 @@ _lock = threading.Lock()
 
 
 def build(force: bool = False) -> str:
-    """Compile ``kda_ref.c`` into ``oracle/_build/libkda_ref.so`` with gcc.
+    """Compile ``kda_ref.c`` and ``kda_ref_bwd.c`` into
+    ``oracle/_build/libkda_ref.so`` with gcc.
 
     Plain -O2, no fast-math (IEEE fp64 exp and arithmetic), no
     machine-specific flags, so it builds the same on x86_64 and aarch64.
     """
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+           "-fno-fast-math", "-o", tmp] + _SRCS + ["-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -67,6 +71,11 @@ def _bind(path):
         ctypes.c_int, dp, dp, dp, dp, dp, ctypes.c_double, dp, ip,
         dp, dp, ctypes.c_int]
     lib.kda_ref_forward.restype = ctypes.c_int
+    lib.kda_ref_backward.argtypes = [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, dp, dp, dp, dp, dp, ctypes.c_double, dp, ip,
+        dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+    lib.kda_ref_backward.restype = ctypes.c_int
     lib.kda_ref_short_conv_silu.argtypes = [
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
         dp, ip, dp]
@@ -171,6 +180,41 @@ def kda_forward(q, k, v, g, beta, scale=None, initial_state=None,
     if rc != 0:
         raise RuntimeError(f"kda_ref_forward failed with status {rc}")
     return o, fs
+
+
+def kda_backward(q, k, v, g, beta, scale=None, initial_state=None, segment_ids=None,
+                 d_o=None, d_final=None, threads=None):
+    """fp64 gradient of :func:`kda_forward`: reverse-mode differentiation of
+    the token recurrence, given the upstream gradients ``d_o`` [B,T,H,V] of o
+    and ``d_final`` [B,H,K,V] of the final state (None = zeros).  Returns
+    ``(dq, dk, dv, dg, dbeta, d_initial)`` as float64 numpy arrays (layouts
+    of q, k, v, g, beta and the state); ``d_initial`` is the gradient with
+    respect to the initial state (a zero one when none is given).
+    """
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    S0 = _f64(initial_state)
+    seg = _i32(segment_ids)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dO = _f64(d_o) if d_o is not None else np.zeros((B, T, H, V))
+    dF = _f64(d_final)
+    assert dO.shape == (B, T, H, V)
+    if dF is not None:
+        assert dF.shape == (B, H, K, V)
+    if scale is None:
+        scale = K ** -0.5
+    dq = np.zeros((B, T, H, K)); dk = np.zeros((B, T, H, K)); dg = np.zeros((B, T, H, K))
+    dv = np.zeros((B, T, H, V)); dbeta = np.zeros((B, T, H)); dS0 = np.zeros((B, H, K, V))
+    n = threads if threads is not None else default_threads()
+    dp, ip = ctypes.c_double, ctypes.c_int32
+    rc = _load().kda_ref_backward(
+        B, T, H, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(g, dp),
+        _ptr(beta, dp), float(scale), _ptr(S0, dp), _ptr(seg, ip), _ptr(dO, dp),
+        _ptr(dF, dp), _ptr(dq, dp), _ptr(dk, dp), _ptr(dv, dp), _ptr(dg, dp),
+        _ptr(dbeta, dp), _ptr(dS0, dp), int(n))
+    if rc != 0:
+        raise RuntimeError(f"kda_ref_backward failed with status {rc}")
+    return dq, dk, dv, dg, dbeta, dS0
 
 
 def short_conv_silu(x, w, segment_ids=None):
