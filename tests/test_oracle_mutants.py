@@ -16,6 +16,8 @@ import oracle
 import test_oracle as P
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_ref.c")
+# linked unchanged into every mutant library (the binding resolves its symbols)
+BWD_SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_ref_bwd.c")
 
 OUT_BLOCK = """    /* o_t = scale * q_t^T S (the updated S) */
     for (int j = 0; j < V; ++j) ot[j] = 0.0;
@@ -103,7 +105,7 @@ def test_pins_reject_mutant(name):
         so = os.path.join(d, "libm.so")
         open(c, "w").write(mutated)
         subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                        "-o", so, c, "-lm"], check=True)
+                        "-o", so, c, BWD_SRC, "-lm"], check=True)
         assert _caught(so), f"no pin rejects mutant {name!r}"
 
 
