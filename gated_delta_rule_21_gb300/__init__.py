@@ -11,6 +11,7 @@ package fails loudly when ``libkda.so`` has not been built.
 Entry points (same names as the C ABI, minus the ``kda_`` prefix):
 
 * :func:`chunk_fwd` -- the chunked KDA forward (``kda_chunk_fwd[_ex]``).
+* :func:`chunk_bwd` -- its gradient (``kda_chunk_bwd``).
 * :func:`short_conv_silu` -- the causal conv + SiLU (+ L2) prologue.
 * :func:`workspace_size`, :func:`read_device_status`,
   :func:`clear_device_status`, :func:`status_string`, :func:`version`.
@@ -97,6 +98,11 @@ def lib():
         L.kda_chunk_fwd_host.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp,
                                          vp, vp, u64, vp]
         L.kda_chunk_fwd_host.restype = i
+        L.kda_chunk_bwd_workspace_size.argtypes = [sp, i]
+        L.kda_chunk_bwd_workspace_size.restype = u64
+        L.kda_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
+                                    vp, vp, vp, vp, u64, vp]
+        L.kda_chunk_bwd.restype = i
         L.kda_selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
         L.kda_selftest_wait_timeout.restype = i
         _lib = L
@@ -226,6 +232,57 @@ def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
     return o, fs
+
+
+def bwd_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
+    """Workspace bytes of chunk_bwd for this shape (0 when unsupported)."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_bwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+
+
+def chunk_bwd(q, k, v, g, beta, d_o, scale=None, chunk_size=CHUNK, initial_state=None,
+              segment_ids=None, d_final=None, want_d_initial=True, workspace=None,
+              stream=None):
+    """Gradient of chunk_fwd on the GPU: given ``d_o`` [B,T,H,V] (dtype of q)
+    and ``d_final`` [B,H,K,V] fp32 or None, returns fp32 ``(dq, dk, dv, dg,
+    dbeta, d_initial or None)`` of ``sum(d_o * o) + sum(d_final *
+    final_state)``.  Inputs as chunk_fwd."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("chunk_bwd needs CUDA tensors")
+    dt = q.dtype
+    _check(q, "q", (B, T, H, K), dt, dev)
+    _check(k, "k", (B, T, H, K), dt, dev)
+    _check(v, "v", (B, T, H, V), dt, dev)
+    _check(d_o, "d_o", (B, T, H, V), dt, dev)
+    _check(g, "g", (B, T, H, K), torch.float32, dev)
+    _check(beta, "beta", (B, T, H), torch.float32, dev)
+    _check(initial_state, "initial_state", (B, H, K, V), torch.float32, dev)
+    _check(d_final, "d_final", (B, H, K, V), torch.float32, dev)
+    _check(segment_ids, "segment_ids", (B, T), torch.int32, dev)
+    if scale is None:
+        scale = K ** -0.5
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty(B, T, H, K, **f32) for _ in range(3))
+    dv = torch.empty(B, T, H, V, **f32)
+    dbeta = torch.empty(B, T, H, **f32)
+    d_init = torch.empty(B, H, K, V, **f32) if want_d_initial else None
+    if workspace is None:
+        n = bwd_workspace_size(B, T, H, K, V, dt, segment_ids is not None)
+        if n == 0:
+            raise KdaError(2, "kda_chunk_bwd_workspace_size")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_bwd(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        int(chunk_size), _ptr(initial_state), _ptr(segment_ids), _ptr(d_o), _ptr(d_final),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(d_init), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, d_init
 
 
 def short_conv_silu(x_q, x_k, x_v, w, segment_ids=None, l2norm_qk=True,

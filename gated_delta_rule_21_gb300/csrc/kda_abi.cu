@@ -270,4 +270,72 @@ kda_status kda_clear_device_status(void *workspace, kda_stream_t stream) {
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids) {
+  if (check_shape(s) != KDA_OK || !bwd_supported(s->K, s->V)) return 0;
+  return align_up(ws_bytes(s->B, s->T, has_segment_ids != 0), 256) +
+         bwd_scratch_bytes(s->B, s->T, s->H, s->K, s->V);
+}
+
+kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float scale, int chunk_size,
+                         const float *initial_state, const int32_t *segment_ids,
+                         const void *d_o, const float *d_final, float *dq, float *dk,
+                         float *dv, float *dg, float *dbeta, float *d_initial,
+                         void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+  kda_status st = check_shape(s);
+  if (st != KDA_OK) return st;
+  if (!bwd_supported(s->K, s->V)) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
+    return KDA_ERR_INVALID_ARG;
+  if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, d_o, initial_state, d_final, segment_ids,
+                        dq, dk, dv, dg, dbeta, d_initial};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  const bool has_seg = segment_ids != nullptr;
+  const size_t need = kda_chunk_bwd_workspace_size(s, has_seg ? 1 : 0);
+  if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+
+  const size_t nck = ((size_t)s->T + 7) / 8;
+  const size_t n_vt = (size_t)s->V / 32;
+  const size_t nK = (size_t)s->B * s->T * s->H * s->K;
+  char *ws = static_cast<char *>(workspace);
+  char *scratch = ws + align_up(ws_bytes(s->B, s->T, has_seg), 256);
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;
+  p.n_vtiles = (int)n_vt;
+  p.q = q; p.k = k; p.v = v; p.d_o = d_o;
+  p.g = g; p.beta = beta; p.initial_state = initial_state; p.d_final = d_final;
+  p.scale = scale;
+  p.dv = dv; p.d_initial = d_initial;
+  p.ckpt_cta_floats = nck * (size_t)s->K * 32;
+  p.ckpt = reinterpret_cast<float *>(scratch);
+  size_t off = align_up(sizeof(float) * kBwdMaxCtas * p.ckpt_cta_floats, 256);
+  p.part_q = reinterpret_cast<float *>(scratch + off); off += align_up(sizeof(float) * n_vt * nK, 256);
+  p.part_k = reinterpret_cast<float *>(scratch + off); off += align_up(sizeof(float) * n_vt * nK, 256);
+  p.part_g = reinterpret_cast<float *>(scratch + off); off += align_up(sizeof(float) * n_vt * nK, 256);
+  p.part_b = reinterpret_cast<float *>(scratch + off);
+  const long long max_units =
+      (long long)s->B * (has_seg ? s->T : 1) * s->H * (long long)n_vt;
+  p.grid = (int)(max_units < kBwdMaxCtas ? max_units : kBwdMaxCtas);
+  if (has_seg) {
+    p.runs.row_offsets = reinterpret_cast<const int32_t *>(ws + sizeof(WsHeader));
+    p.runs.runs = reinterpret_cast<const int2 *>(ws + sizeof(WsHeader) +
+                                                 ws_row_offsets_bytes(s->B));
+    p.runs.total_runs = &reinterpret_cast<WsHeader *>(ws)->total_runs;
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (has_seg) {
+    // Runs; dv = 0 on padding; d_initial = d_final (or 0) for rows without a run.
+    cudaError_t e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, dv, 0,
+                                        d_final, d_initial, workspace, cs, false);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return from_cuda(launch_bwd(p, s->qkv_dtype == KDA_DTYPE_BF16, segment_ids, dq, dk, dg,
+                              dbeta, cs));
+}
+
 }  // extern "C"

@@ -117,6 +117,28 @@ bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile);
 cudaError_t launch_fwd_split(const FwdParams &p, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream, bool with_fallback = false);
 
+// Backward (kda_bwd.cu).  Per-tile partial sums of dq, dk, dg ([n_vtiles]
+// x [B*T*H*K]) and dbeta ([n_vtiles] x [B*T*H]) are summed into the outputs
+// by a second kernel; dv and d_initial are written directly.
+struct BwdParams {
+  int B, T, H, K, V, n_vtiles;
+  const void *q, *k, *v, *d_o;
+  const float *g, *beta, *initial_state, *d_final;
+  float scale;
+  float *dv, *d_initial;
+  float *part_q, *part_k, *part_g, *part_b;
+  float *ckpt;              // per-CTA checkpoint scratch
+  size_t ckpt_cta_floats;   // floats per CTA
+  int grid;                 // CTAs (the scratch is sized for them)
+  RunTable runs;
+};
+constexpr int kBwdMaxCtas = 152;
+// Scratch after the run table: checkpoints, then the partial sums.
+size_t bwd_scratch_bytes(int B, int T, int H, int K, int V);
+bool bwd_supported(int K, int V);
+cudaError_t launch_bwd(const BwdParams &p, bool bf16, const int32_t *segment_ids,
+                       float *dq, float *dk, float *dg, float *dbeta, cudaStream_t stream);
+
 cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
                               cudaStream_t stream);
 

@@ -298,6 +298,40 @@ KDA_API kda_status kda_chunk_fwd_host(const kda_shape *s, const void *q, const v
                                       size_t device_buffer_bytes, kda_stream_t stream);
 
 /*
+ * Backward of kda_chunk_fwd: the gradients of
+ *     L = sum_t <d_o_t, o_t> + <d_final, final_state>
+ * with respect to q, k, v, g, beta and initial_state, for the forward of page
+ * "feat(kda): integrate KDA attention with tokamax backend and CP support",
+ * section "Delta Rule formulation", with the packed runs of section "Public
+ * API" (the pages' roadmap lists the backward as the next step; they print no
+ * formula for it: this is reverse-mode differentiation of that recurrence).
+ * Inputs as kda_chunk_fwd (q, k, v, g, beta, scale, chunk_size = 64,
+ * initial_state or NULL = zeros, segment_ids or NULL), plus
+ *   d_o        device [B,T,H,V] in s->qkv_dtype (the gradient of o);
+ *   d_final    device float32 [B,H,K,V] or NULL (= zeros).
+ * Outputs, all float32, caller-allocated:
+ *   dq, dk, dg [B,T,H,K]; dv [B,T,H,V]; dbeta [B,T,H];
+ *   d_initial  [B,H,K,V] or NULL (not wanted): the gradient with respect to
+ *              the initial state (a zero one when initial_state is NULL).
+ * Padding tokens get zero gradients; a row without a run passes d_final to
+ * d_initial.  Supports K in {32, 64, 128} and V a multiple of 32.  The first
+ * implementation runs on the CUDA cores in fp32: it recomputes the states
+ * from checkpoints every 8 tokens and walks each (run, head, 32-column value
+ * tile) backwards.  workspace: kda_chunk_bwd_workspace_size bytes,
+ * 256-byte aligned, zero-filled before first use, reusable; it holds the
+ * run list, the checkpoints and per-tile partial sums.  Errors as
+ * kda_chunk_fwd; the call is asynchronous on `stream`.
+ */
+KDA_API size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids);
+KDA_API kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k,
+                                 const void *v, const float *g, const float *beta,
+                                 float scale, int chunk_size, const float *initial_state,
+                                 const int32_t *segment_ids, const void *d_o,
+                                 const float *d_final, float *dq, float *dk, float *dv,
+                                 float *dg, float *dbeta, float *d_initial, void *workspace,
+                                 size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * Test hook for failure detection (no counterpart in the pages): enqueues
  * one thread that waits, for at most `limit_cycles` SM clocks (1 .. about
  * 2^31), on an mbarrier nothing ever arrives at, using the bounded wait of

@@ -159,3 +159,13 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
                beta=beta.contiguous(), initial_state=S0, segment_ids=seg,
                conv_w=conv_w, scale=K ** -0.5)
     return out
+
+
+def make_upstream_grads(w: Workload, seed: int = 0) -> dict:
+    """Upstream gradients for the backward: d_o [B,T,H,V] ~ N(0,1) in the
+    workload's q/k/v dtype and d_final [B,H,K,V] ~ N(0,1) fp32, drawn on the
+    CPU from their own seeded generator."""
+    gen = torch.Generator().manual_seed(10_000 + seed)
+    d_o = torch.randn(w.B, w.T, w.H, w.V, generator=gen, dtype=torch.float32)
+    d_final = torch.randn(w.B, w.H, w.K, w.V, generator=gen, dtype=torch.float32)
+    return dict(d_o=_cast(d_o, w.dtype).contiguous(), d_final=d_final.contiguous())
