@@ -428,6 +428,46 @@ def run_ours(args, dist):
                 # the conv leg, then conv + the packed forward
                 "gpu_launches": args.steps * (2 + packed_launches(w))}
 
+    def measure_backward(wname):
+        """The backward (kda_chunk_bwd) on the same workload: the gradients
+        of sum(d_o * o) + sum(d_final * final_state) for seeded upstream
+        gradients, workspace allocated once."""
+        w = ki.WORKLOADS[wname]
+        x = ki.make_inputs(w, seed=args.seed + dist.rank)
+        u = ki.make_upstream_grads(w, seed=args.seed + dist.rank)
+        d = device_inputs(x, dev)
+        d_o, d_f = u["d_o"].to(dev), u["d_final"].to(dev)
+        has_seg = d["segment_ids"] is not None
+        ws = torch.zeros(kda.bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d_o, scale=x["scale"],
+                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                          d_final=d_f, workspace=ws, stream=stream)
+
+        steps = min(args.steps, 20)
+        times, _ = time_steps(step, steps, args.warmup, stream, flush, dist)
+        ms = dist.max(statistics.mean(times))
+        th = w.token_heads
+        esz = d["q"].element_size()
+        # reads q k v d_o (input dtype), g, beta; writes dq dk dg dv (fp32), dbeta;
+        # initial state and d_final read, d_initial written
+        nbytes = (th * (2 * w.K * esz + 2 * w.V * esz + 4 * w.K + 4)
+                  + th * (3 * 4 * w.K + 4 * w.V + 4) + 3 * w.B * w.H * w.K * w.V * 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res = {"workload": w.name, "ms_per_step": ms, "unit": "tokens/s",
+               "value": whole_job_value(dist.world, w.B * w.T, ms), "steps": steps,
+               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                            "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                            "algorithmic_bytes": nbytes,
+                            "kernel": "bwd_simt_kernel + bwd_reduce_kernel"},
+               # (runs +) the backward kernel + the reduction
+               "gpu_launches": steps * (3 if has_seg else 2)}
+        if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_backward(w, args.seed, budget_s=args.cpu_seconds / 2)
+        return res
+
     def packed_launches(w):
         """Kernels one packed forward launches: segment runs, chunk
         coordinates, prep, recurrence (+ the fused kernel AUTO enqueues
@@ -452,6 +492,10 @@ def run_ours(args, dist):
               if args.workload == HEADLINE and not args.no_packed else None)
     prologue = (measure_prologue(PROLOGUE)
                 if args.workload == HEADLINE and not args.no_prologue else None)
+    backward = (measure_backward(args.workload)
+                if not args.no_backward and kda.bwd_workspace_size(
+                    1, 64, 1, ki.WORKLOADS[args.workload].K, ki.WORKLOADS[args.workload].V) > 0
+                else None)
     clk = clocks.stop()
 
     w = head["workload"]
@@ -490,6 +534,9 @@ def run_ours(args, dist):
     if prologue is not None:
         line["prologue"] = prologue
         line["gpu_launches"] += prologue["gpu_launches"]
+    if backward is not None:
+        line["backward"] = backward
+        line["gpu_launches"] += backward["gpu_launches"]
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.seed, budget_s=args.cpu_seconds)
     return line
@@ -527,6 +574,29 @@ def cpu_baseline(w, seed, budget_s=10.0):
             "kind": "oracle",
             "sample": f"{heads} of {w.H} heads x {w.B * w.T} tokens (fp64 token recurrence), "
                       f"{runs} runs, {t_total:.1f} s; tokens/s scaled by heads/H"}
+
+
+def cpu_baseline_backward(w, seed, budget_s=5.0):
+    """The fp64 backward oracle on a head sample of the workload."""
+    import oracle
+    cores = oracle.default_threads()
+    heads = min(w.H, cores)
+    arrs, s0, seg, scale = oracle_sample(w, seed, heads)
+    u = ki.make_upstream_grads(w, seed=seed)
+    d_o = oracle._f64(u["d_o"][:, :, :heads])
+    d_f = oracle._f64(u["d_final"][:, :heads])
+    runs, t_total = 0, 0.0
+    while t_total < budget_s and runs < 100:
+        t = time.perf_counter()
+        oracle.kda_backward(*arrs, scale, initial_state=s0, segment_ids=seg, d_o=d_o,
+                            d_final=d_f, threads=cores)
+        t_total += time.perf_counter() - t
+        runs += 1
+    per_run = t_total / runs
+    return {"value": w.B * w.T * heads / w.H / per_run, "unit": "tokens/s",
+            "cores": min(cores, w.B * heads), "kind": "oracle",
+            "sample": f"{heads} of {w.H} heads x {w.B * w.T} tokens (fp64 reverse-mode token "
+                      f"recurrence), {runs} runs, {t_total:.1f} s; tokens/s scaled by heads/H"}
 
 
 def run_reference(args, dist):
@@ -575,6 +645,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--no-packed", action="store_true", help="skip the packed N=25 leg")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip the conv prologue leg (packed N=25 shape)")
     args = ap.parse_args()

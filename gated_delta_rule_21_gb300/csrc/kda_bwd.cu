@@ -20,10 +20,13 @@
 // The states S_{t-1} are recomputed: a forward pass over the run keeps S at
 // every 8th token (global scratch, per CTA); then, block by block from the
 // end, the block is replayed from its checkpoint with the states kept in
-// shared memory and walked backwards.  256 threads: warp w owns keys
-// w K/8 .. (w+1) K/8 - 1, lane = value column; sums over keys go through
-// shared memory, sums over value columns are butterfly reductions inside the
-// warp.  This is the first correct path (no tensor cores).
+// shared memory and walked backwards.  256 threads: warp w owns the tile's
+// value columns 4w .. 4w + 3 for all keys (lane l: keys l, l + 32, ...).
+// The value columns are independent in the recurrence, so each warp's chain
+// needs only in-warp sums over keys and no block barrier per token; the
+// sums over value columns (dq, dk, dg, dbeta) are per-warp partials in
+// shared memory, added up every 4 tokens.  This is the first path on the
+// CUDA cores (no tensor cores).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -34,6 +37,9 @@ constexpr int kWarps = kBwdThreads / 32;
 constexpr int kVT = 32;   // value columns per CTA
 constexpr int kCKB = 8;   // tokens per checkpoint block
 
+constexpr int kCPW = kVT / kWarps;   // value columns per warp
+constexpr int kFlush = 4;             // tokens per reduction of the column sums
+
 template <int K>
 struct BwdSmem {
   // floats, in order
@@ -43,62 +49,44 @@ struct BwdSmem {
   static constexpr int VV = E + kCKB * K;           // v tile  [kCKB][kVT]
   static constexpr int DO = VV + kCKB * kVT;        // do tile [kCKB][kVT]
   static constexpr int BETA = DO + kCKB * kVT;      // beta    [kCKB]
-  static constexpr int RED = BETA + 32;             // [2 parities][2][kWarps][kVT]
-  static constexpr int BLK = RED + 2 * 2 * kWarps * kVT;  // states [kCKB][K][kVT]
-  static constexpr int FLOATS = BLK + kCKB * K * kVT;
+  static constexpr int PQ = BETA + 32;              // per-warp column sums [kFlush][kWarps][K]
+  static constexpr int PK = PQ + kFlush * kWarps * K;
+  static constexpr int PG = PK + kFlush * kWarps * K;
+  static constexpr int PB = PG + kFlush * kWarps * K;   // [kFlush][kWarps]
+  static constexpr int BLK = PB + kFlush * kWarps;      // states [kCKB][kVT][K]
+  static constexpr int FLOATS = BLK + kCKB * kVT * K;
   static constexpr size_t BYTES = sizeof(float) * (size_t)FLOATS;
 };
 
-// N values per lane (N = 4, 8 or 16, one per key of the warp); returns the
-// sum over the 32 lanes for key (lane >> (5 - log2 N)) & (N - 1), in every
-// lane.  Each step halves the values a lane keeps and adds its partner's.
+// x[m] <- the sum of x[m] over the 32 lanes, for N independent values.
 template <int N>
-__device__ __forceinline__ float lane_sum_transposed(const float (&v)[N], int lane) {
-  float cur[N];
+__device__ __forceinline__ void warp_sums(float (&x)[N]) {
 #pragma unroll
-  for (int i = 0; i < N; ++i) cur[i] = v[i];
-  int off = 16;
+  for (int off = 16; off >= 1; off >>= 1) {
 #pragma unroll
-  for (int n = N; n > 1; n >>= 1, off >>= 1) {
-    const bool up = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = up ? cur[i] : cur[i + n / 2];
-      const float keep = up ? cur[i + n / 2] : cur[i];
-      cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
+    for (int m = 0; m < N; ++m) x[m] += __shfl_xor_sync(0xffffffffu, x[m], off);
   }
-  float d = cur[0];
-#pragma unroll
-  for (; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-  return d;
 }
 
-template <int N>
-__host__ __device__ constexpr int log2_of() { return N == 4 ? 2 : N == 8 ? 3 : 4; }
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
-
+// One CTA's walk of one unit.  Lane l of warp w holds keys l, l + 32, ...
+// (K / 32 of them) for the warp's 4 value columns 4w .. 4w + 3.  The state
+// recurrence is independent per value column, so a warp's chain needs only
+// in-warp sums over keys; the sums over value columns (dq, dk, dg, dbeta)
+// are per-warp partials in shared memory, added up every kFlush tokens.
 template <typename TI, int K>
 struct BwdCta {
-  static constexpr int KPW = K / kWarps;  // keys per warp
+  static constexpr int KPL = K / 32;  // keys per lane
   using L = BwdSmem<K>;
   const BwdParams &p;
   float *sm;
-  int warp, lane, i0;
-  int par = 0;                            // reduction buffer of this token
-  float S[KPW], dS[KPW];
+  int warp, lane, c0;
+  float S[KPL][kCPW], dS[KPL][kCPW];
 
   __device__ BwdCta(const BwdParams &p_, float *sm_) : p(p_), sm(sm_) {
     warp = threadIdx.x >> 5;
     lane = threadIdx.x & 31;
-    i0 = warp * KPW;
+    c0 = warp * kCPW;
   }
-  __device__ float *red(int which, int w) { return sm + L::RED + ((par * 2 + which) * kWarps + w) * kVT; }
 
   // Tokens t0 .. t0 + n - 1 of row b, head h, into shared memory (q and do
   // only for the backward walk).
@@ -135,97 +123,145 @@ struct BwdCta {
     }
   }
 
-  // One forward token on S (the staged token tau).
-  __device__ void fwd_token(int tau) {
-    const float *kt = sm + L::KK + tau * K + i0, *et = sm + L::E + tau * K + i0;
-    float pr = 0.f;
+  __device__ void load_k_e(int tau, float (&kk)[KPL], float (&ee)[KPL]) const {
 #pragma unroll
-    for (int m = 0; m < KPW; ++m) {
-      S[m] *= et[m];
-      pr = fmaf(S[m], kt[m], pr);
+    for (int n = 0; n < KPL; ++n) {
+      kk[n] = sm[L::KK + tau * K + lane + 32 * n];
+      ee[n] = sm[L::E + tau * K + lane + 32 * n];
     }
-    red(0, warp)[lane] = pr;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += red(0, w)[lane];
-    const float r = sm[L::VV + tau * kVT + lane] - tot;
-    const float bt = sm[L::BETA + tau];
-#pragma unroll
-    for (int m = 0; m < KPW; ++m) S[m] = fmaf(bt * kt[m], r, S[m]);
-    par ^= 1;
   }
 
-
+  // One forward token on S (the staged token tau).
+  __device__ void fwd_token(int tau) {
+    float kk[KPL], ee[KPL], pr[kCPW];
+    load_k_e(tau, kk, ee);
+#pragma unroll
+    for (int m = 0; m < kCPW; ++m) pr[m] = 0.f;
+#pragma unroll
+    for (int n = 0; n < KPL; ++n)
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        S[n][m] *= ee[n];
+        pr[m] = fmaf(S[n][m], kk[n], pr[m]);
+      }
+    warp_sums(pr);
+    const float bt = sm[L::BETA + tau];
+#pragma unroll
+    for (int m = 0; m < kCPW; ++m) {
+      const float r = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+#pragma unroll
+      for (int n = 0; n < KPL; ++n) S[n][m] = fmaf(bt * kk[n], r, S[n][m]);
+    }
+  }
   // One backward token (the staged token tau, its entering state in BLK);
-  // th = (b T + t) H + h.
-  __device__ void bwd_token(int tau, size_t th, int vt) {
-    const float *kt = sm + L::KK + tau * K + i0, *et = sm + L::E + tau * K + i0;
-    const float *qt = sm + L::Q + tau * K + i0;
-    const float *bk = sm + L::BLK + (size_t)tau * K * kVT;
-    const float bt = sm[L::BETA + tau], dov = sm[L::DO + tau * kVT + lane];
-    float Sp[KPW];
-    float pr = 0.f, pa = 0.f;
+  // the per-warp column sums go to slot `slot` of PQ/PK/PG/PB.
+  __device__ void bwd_token(int tau, int slot, size_t th, int vt) {
+    float kk[KPL], ee[KPL], qq[KPL];
+    load_k_e(tau, kk, ee);
 #pragma unroll
-    for (int m = 0; m < KPW; ++m) {
-      Sp[m] = bk[(i0 + m) * kVT + lane] * et[m];
-      pr = fmaf(Sp[m], kt[m], pr);
-      dS[m] = fmaf(p.scale * qt[m], dov, dS[m]);   // o_t = scale S_t^T q_t
-      pa = fmaf(dS[m], kt[m], pa);
+    for (int n = 0; n < KPL; ++n) qq[n] = sm[L::Q + tau * K + lane + 32 * n];
+    const float *bk = sm + L::BLK + (size_t)tau * kVT * K;
+    const float bt = sm[L::BETA + tau];
+    float dov[kCPW], Sp[KPL][kCPW], pr[kCPW], pa[kCPW];
+#pragma unroll
+    for (int m = 0; m < kCPW; ++m) {
+      dov[m] = sm[L::DO + tau * kVT + c0 + m];
+      pr[m] = 0.f;
+      pa[m] = 0.f;
     }
-    red(0, warp)[lane] = pr;
-    red(1, warp)[lane] = pa;
+#pragma unroll
+    for (int n = 0; n < KPL; ++n)
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        Sp[n][m] = bk[(c0 + m) * K + lane + 32 * n] * ee[n];
+        pr[m] = fmaf(Sp[n][m], kk[n], pr[m]);
+        dS[n][m] = fmaf(p.scale * qq[n], dov[m], dS[n][m]);   // o_t = scale S_t^T q_t
+        pa[m] = fmaf(dS[n][m], kk[n], pa[m]);
+      }
+    warp_sums(pr);
+    warp_sums(pa);
+    float r[kCPW], dr[kCPW], db = 0.f;
+#pragma unroll
+    for (int m = 0; m < kCPW; ++m) {
+      r[m] = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+      dr[m] = bt * pa[m];
+      db = fmaf(pa[m], r[m], db);
+    }
+    float* const pq = sm + L::PQ + (slot * kWarps + warp) * K;
+    float* const pk = sm + L::PK + (slot * kWarps + warp) * K;
+    float* const pg = sm + L::PG + (slot * kWarps + warp) * K;
+#pragma unroll
+    for (int n = 0; n < KPL; ++n) {
+      float aq = 0.f, ak = 0.f, ag = 0.f;
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        const float st = fmaf(bt * kk[n], r[m], Sp[n][m]);          // S_t
+        aq = fmaf(st, dov[m], aq);
+        ak += bt * dS[n][m] * r[m] - Sp[n][m] * dr[m];
+        const float dsp = fmaf(-kk[n], dr[m], dS[n][m]);           // dS'
+        ag = fmaf(Sp[n][m], dsp, ag);
+        dS[n][m] = ee[n] * dsp;                                     // gradient of S_{t-1}
+      }
+      pq[lane + 32 * n] = p.scale * aq;
+      pk[lane + 32 * n] = ak;
+      pg[lane + 32 * n] = ag;
+    }
+    if (lane == 0) sm[L::PB + slot * kWarps + warp] = db;
+    float drl = dr[0];
+#pragma unroll
+    for (int m = 1; m < kCPW; ++m)
+      if (lane == m) drl = dr[m];
+    if (lane < kCPW) p.dv[th * p.V + vt * kVT + c0 + lane] = drl;
+  }
+
+  // The column sums of `count` tokens (slot s = token t_hi - s), over the
+  // warps, into this tile's partials.
+  __device__ void flush(size_t th_hi, int count, int vt) {
     __syncthreads();
-    float rs = 0.f, as = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      rs += red(0, w)[lane];
-      as += red(1, w)[lane];
-    }
-    const float r = sm[L::VV + tau * kVT + lane] - rs;   // r_j
-    const float dr = bt * as;                              // dr_j
-    float vq[KPW], vk[KPW], vg[KPW];
-#pragma unroll
-    for (int m = 0; m < KPW; ++m) {
-      const float st = fmaf(bt * kt[m], r, Sp[m]);         // S_t[i][j]
-      vq[m] = st * dov;
-      vk[m] = bt * dS[m] * r - Sp[m] * dr;
-      const float dsp = fmaf(-kt[m], dr, dS[m]);          // dS'[i][j]
-      vg[m] = Sp[m] * dsp;
-      dS[m] = et[m] * dsp;                                 // gradient of S_{t-1}
-    }
-    const float sq = lane_sum_transposed<KPW>(vq, lane);
-    const float sk = lane_sum_transposed<KPW>(vk, lane);
-    const float sg = lane_sum_transposed<KPW>(vg, lane);
-    const float db = warp_sum(as * r);
-    constexpr int SH = 5 - log2_of<KPW>();
     const size_t nK = (size_t)p.B * p.T * p.H * K;
-    if ((lane & ((1 << SH) - 1)) == 0) {
-      const size_t o = (size_t)vt * nK + th * K + i0 + (lane >> SH);
-      p.part_q[o] = p.scale * sq;
-      p.part_k[o] = sk;
-      p.part_g[o] = sg;
+    for (int idx = threadIdx.x; idx < count * K; idx += kBwdThreads) {
+      const int slot = idx / K, i = idx % K;
+      float a = 0.f, c = 0.f, d = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        a += sm[L::PQ + (slot * kWarps + w) * K + i];
+        c += sm[L::PK + (slot * kWarps + w) * K + i];
+        d += sm[L::PG + (slot * kWarps + w) * K + i];
+      }
+      const size_t o = (size_t)vt * nK + (th_hi - (size_t)slot * p.H) * K + i;
+      p.part_q[o] = a;
+      p.part_k[o] = c;
+      p.part_g[o] = d;
     }
-    if (warp == 0) {
-      p.dv[th * p.V + vt * kVT + lane] = dr;
-      if (lane == 0) p.part_b[(size_t)vt * ((size_t)p.B * p.T * p.H) + th] = db;
+    if (threadIdx.x < count) {
+      const int slot = threadIdx.x;
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) a += sm[L::PB + slot * kWarps + w];
+      p.part_b[(size_t)vt * ((size_t)p.B * p.T * p.H) + th_hi - (size_t)slot * p.H] = a;
     }
-    par ^= 1;
+    __syncthreads();
   }
 
   __device__ void run_unit(const Unit &u) {
     const int b = u.b, h = u.h, vt = u.vt;
     const int nck = (u.end - u.start + kCKB - 1) / kCKB;
-    float *ck = p.ckpt + (size_t)blockIdx.x * p.ckpt_cta_floats;   // [nck][K][kVT]
-    const size_t st0 = ((size_t)b * p.H + h) * K * p.V + (size_t)vt * kVT + lane;
+    float *ck = p.ckpt + (size_t)blockIdx.x * p.ckpt_cta_floats;   // [nck][kVT][K]
+    const size_t st0 = ((size_t)b * p.H + h) * K * p.V + (size_t)vt * kVT + c0;
 #pragma unroll
-    for (int m = 0; m < KPW; ++m)
-      S[m] = (u.first && p.initial_state) ? p.initial_state[st0 + (size_t)(i0 + m) * p.V] : 0.f;
+    for (int n = 0; n < KPL; ++n)
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m)
+        S[n][m] = (u.first && p.initial_state)
+                      ? p.initial_state[st0 + (size_t)(lane + 32 * n) * p.V + m] : 0.f;
     // forward over the run, keeping S at every kCKB-th token
     for (int c = 0; c < nck; ++c) {
       const int t0 = u.start + c * kCKB, n = min(kCKB, u.end - t0);
 #pragma unroll
-      for (int m = 0; m < KPW; ++m) ck[((size_t)c * K + i0 + m) * kVT + lane] = S[m];
+      for (int kn = 0; kn < KPL; ++kn)
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m)
+          ck[((size_t)c * kVT + c0 + m) * K + lane + 32 * kn] = S[kn][m];
       stage(b, h, vt, t0, n, false);
       __syncthreads();
       for (int tau = 0; tau < n; ++tau) fwd_token(tau);
@@ -233,27 +269,40 @@ struct BwdCta {
     }
     // backward, block by block from the end
 #pragma unroll
-    for (int m = 0; m < KPW; ++m)
-      dS[m] = (u.last && p.d_final) ? p.d_final[st0 + (size_t)(i0 + m) * p.V] : 0.f;
+    for (int n = 0; n < KPL; ++n)
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m)
+        dS[n][m] = (u.last && p.d_final)
+                       ? p.d_final[st0 + (size_t)(lane + 32 * n) * p.V + m] : 0.f;
     for (int c = nck - 1; c >= 0; --c) {
       const int t0 = u.start + c * kCKB, n = min(kCKB, u.end - t0);
 #pragma unroll
-      for (int m = 0; m < KPW; ++m) S[m] = ck[((size_t)c * K + i0 + m) * kVT + lane];
+      for (int kn = 0; kn < KPL; ++kn)
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m) S[kn][m] = ck[((size_t)c * kVT + c0 + m) * K + lane + 32 * kn];
       stage(b, h, vt, t0, n, true);
       __syncthreads();
       for (int tau = 0; tau < n; ++tau) {   // replay: the state entering each token
-        float *bk = sm + L::BLK + (size_t)tau * K * kVT;
+        float *bk = sm + L::BLK + (size_t)tau * kVT * K;
 #pragma unroll
-        for (int m = 0; m < KPW; ++m) bk[(i0 + m) * kVT + lane] = S[m];
+        for (int kn = 0; kn < KPL; ++kn)
+#pragma unroll
+          for (int m = 0; m < kCPW; ++m) bk[(c0 + m) * K + lane + 32 * kn] = S[kn][m];
         if (tau + 1 < n) fwd_token(tau);
       }
-      for (int tau = n - 1; tau >= 0; --tau)
-        bwd_token(tau, ((size_t)b * p.T + t0 + tau) * p.H + h, vt);
-      __syncthreads();
+      for (int hi = n - 1; hi >= 0; hi -= kFlush) {   // groups of kFlush tokens
+        const int count = min(kFlush, hi + 1);
+        for (int s = 0; s < count; ++s)
+          bwd_token(hi - s, s, ((size_t)b * p.T + t0 + hi - s) * p.H + h, vt);
+        flush(((size_t)b * p.T + t0 + hi) * p.H + h, count, vt);
+      }
     }
     if (u.first && p.d_initial) {
 #pragma unroll
-      for (int m = 0; m < KPW; ++m) p.d_initial[st0 + (size_t)(i0 + m) * p.V] = dS[m];
+      for (int n = 0; n < KPL; ++n)
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m)
+          p.d_initial[st0 + (size_t)(lane + 32 * n) * p.V + m] = dS[n][m];
     }
   }
 };
