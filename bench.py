@@ -103,7 +103,7 @@ def measured_peaks():
 
 def kernel_source_digest(impl_name: str) -> str:
     fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu",
-             "conv": "kda_conv.cu"}[impl_name]
+             "conv": "kda_conv.cu", "bwd": "kda_bwd.cu"}[impl_name]
     path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -459,7 +459,8 @@ def run_ours(args, dist):
         res = {"workload": w.name, "ms_per_step": ms, "unit": "tokens/s",
                "value": whole_job_value(dist.world, w.B * w.T, ms), "steps": steps,
                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                            "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                            "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                            "traffic": profiled_traffic("bwd", w.name),
                             "algorithmic_bytes": nbytes,
                             "kernel": "bwd_simt_kernel + bwd_reduce_kernel"},
                # (runs +) the backward kernel + the reduction
