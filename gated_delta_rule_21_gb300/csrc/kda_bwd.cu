@@ -20,25 +20,25 @@
 // The states S_{t-1} are recomputed: a forward pass over the run keeps S at
 // every 8th token (global scratch, per CTA); then, block by block from the
 // end, the block is replayed from its checkpoint with the states kept in
-// shared memory and walked backwards.  256 threads: warp w owns the tile's
-// value columns 4w .. 4w + 3 for all keys (lane l: keys l, l + 32, ...).
+// shared memory and walked backwards.  512 threads: warp w owns the tile's
+// value columns 2w, 2w + 1 for all keys (lane l: keys l, l + 32, ...).
 // The value columns are independent in the recurrence, so each warp's chain
 // needs only in-warp sums over keys and no block barrier per token; the
 // sums over value columns (dq, dk, dg, dbeta) are per-warp partials in
-// shared memory, added up every 4 tokens.  This is the first path on the
+// shared memory, added up every 2 tokens.  This is the first path on the
 // CUDA cores (no tensor cores).
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 512;
 constexpr int kWarps = kBwdThreads / 32;
 constexpr int kVT = 32;   // value columns per CTA
 constexpr int kCKB = 8;   // tokens per checkpoint block
 
 constexpr int kCPW = kVT / kWarps;   // value columns per warp
-constexpr int kFlush = 4;             // tokens per reduction of the column sums
+constexpr int kFlush = 2;             // tokens per reduction of the column sums
 
 template <int K>
 struct BwdSmem {
@@ -69,7 +69,7 @@ __device__ __forceinline__ void warp_sums(float (&x)[N]) {
 }
 
 // One CTA's walk of one unit.  Lane l of warp w holds keys l, l + 32, ...
-// (K / 32 of them) for the warp's 4 value columns 4w .. 4w + 3.  The state
+// (K / 32 of them) for the warp's kCPW value columns.  The state
 // recurrence is independent per value column, so a warp's chain needs only
 // in-warp sums over keys; the sums over value columns (dq, dk, dg, dbeta)
 // are per-warp partials in shared memory, added up every kFlush tokens.
