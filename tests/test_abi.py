@@ -146,3 +146,36 @@ def test_status_calls_reject_null(L):
     bits = ctypes.c_uint32(0)
     assert L.kda_read_device_status(None, None, ctypes.byref(bits)) == 1
     assert L.kda_clear_device_status(None, None) == 1
+
+
+def test_backward_workspace_size_and_argument_checks(L):
+    # supported: K in {32, 64, 128}, V a multiple of 32
+    n = kda.bwd_workspace_size(1, 8192, 32, 128, 128)
+    nck, n_vt, nK, nB = 8192 // 8, 4, 8192 * 32 * 128, 8192 * 32
+    assert n == 256 + 152 * nck * 128 * 32 * 4 + 3 * n_vt * nK * 4 + n_vt * nB * 4
+    assert kda.bwd_workspace_size(1, 100, 2, 64, 64, has_segment_ids=True) > \
+        kda.bwd_workspace_size(1, 100, 2, 64, 64)
+    assert kda.bwd_workspace_size(1, 0, 2, 128, 128) == 0
+    s = kda.kda_shape(1, 64, 2, 128, 128, 1)
+    nb = kda.bwd_workspace_size(1, 64, 2, 128, 128)
+    vp = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, chunk=64, s0=None,
+                 seg=None, d_o=FAKE, d_f=None, dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, db=FAKE,
+                 di=None, ws=FAKE, nbytes=nb)
+        a.update(kw)
+        p = lambda x: None if x is None else vp(x)
+        return L.kda_chunk_bwd(ctypes.byref(s), p(a["q"]), p(a["k"]), p(a["v"]), p(a["g"]),
+                               p(a["beta"]), a["scale"], a["chunk"], p(a["s0"]), p(a["seg"]),
+                               p(a["d_o"]), p(a["d_f"]), p(a["dq"]), p(a["dk"]), p(a["dv"]),
+                               p(a["dg"]), p(a["db"]), p(a["di"]), p(a["ws"]), a["nbytes"], None)
+    assert call(d_o=None) == 1                 # NULL d_o
+    assert call(dq=None) == 1                  # NULL output
+    assert call(chunk=32) == 2                 # chunk size
+    assert call(scale=float("nan")) == 1
+    assert call(d_o=FAKE + 4) == 3             # misaligned
+    assert call(nbytes=nb - 1) == 4            # small workspace
+    assert call(ws=FAKE + 16) == 3          # workspace not 256-byte aligned
+    s48 = kda.kda_shape(1, 64, 2, 128, 48, 1)
+    assert L.kda_chunk_bwd_workspace_size(ctypes.byref(s48), 0) == 0
