@@ -1,6 +1,6 @@
 /*
  * kda.h -- C ABI of libkda, a GB300 (sm_103a) implementation of the chunked
- * Kimi Delta Attention (KDA) forward pass.
+ * Kimi Delta Attention (KDA) forward pass and its backward.
  *
  * The operation (page "feat(kda): integrate KDA attention with tokamax backend
  * and CP support", section "Delta Rule formulation"), per batch row b and head
@@ -314,7 +314,7 @@ KDA_API kda_status kda_chunk_fwd_host(const kda_shape *s, const void *q, const v
  *   d_initial  [B,H,K,V] or NULL (not wanted): the gradient with respect to
  *              the initial state (a zero one when initial_state is NULL).
  * Padding tokens get zero gradients; a row without a run passes d_final to
- * d_initial.  Supports K in {32, 64, 128} and V a multiple of 32.  The first
+ * d_initial.  Supports K and V in {32, 64, 128}.  The first
  * implementation runs on the CUDA cores in fp32: it recomputes the states
  * from checkpoints every 8 tokens and walks each (run, head, 32-column value
  * tile) backwards.  workspace: kda_chunk_bwd_workspace_size bytes,

@@ -62,6 +62,10 @@ CASES = {
     "f32_k64_v128_t130": dict(B=2, T=130, H=2, K=64, V=128, dtype="f32"),
     "bf16_k128_v64_t77": dict(B=1, T=77, H=3, K=128, V=64, init_state_std=0.1),
     "T1": dict(B=1, T=1, H=1, K=128, V=128, init_state_std=0.1),
+    "bf16_k32_v64_t70": dict(B=1, T=70, H=2, K=32, V=64, init_state_std=0.1),
+    "f32_k128_v32_t9": dict(B=3, T=9, H=1, K=128, V=32, dtype="f32"),
+    "len1_runs_only": dict(B=1, T=12, H=2, K=64, V=64, init_state_std=0.1,
+                           segments=[1, 1, 1, ("pad", 1), 1, 1, 1, 1, 1, 1, 1, 1]),
     "packed": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1,
                    segments=[[("pad", 3), 100, 1, 1, ("pad", 5), 120, 70],
                              [64, 64, ("pad", 2), 170]]),
