@@ -236,8 +236,10 @@ struct ConvThread {
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
             const float rs = rsqrtf(ss[j] + 1e-6f);
+            const u64 rs2 = pk2(rs, rs);
 #pragma unroll
-            for (int c = 0; c < kVec; ++c) out[j][c] *= rs;
+            for (int c = 0; c < kVec; c += 2)
+              upk2(mul2(pk2(out[j][c], out[j][c + 1]), rs2), out[j][c], out[j][c + 1]);
           }
         }
 #pragma unroll
