@@ -235,7 +235,7 @@ class ClockSampler:
             except ValueError:
                 return None
         inside = [r for r in mine if ts(r) is not None and any(a <= ts(r) <= b for a, b in self.windows)]
-        window = "timed"
+        window = "timed regions of every leg"
         if not inside:
             inside, window = mine, "timed+warmup (timed region shorter than the sampling period)"
         if not inside:
@@ -409,8 +409,8 @@ def run_ours(args, dist):
                           output_final_state=True, out=o, final_state_out=fs, workspace=ws,
                           impl=args.kda_impl, v_tile=args.v_tile, stream=stream)
 
-        t_conv, _ = time_steps(conv, args.steps, args.warmup, stream, flush, dist)
-        t_full, _ = time_steps(full, args.steps, args.warmup, stream, flush, dist)
+        t_conv, _ = time_steps(conv, args.steps, args.warmup, stream, flush, dist, clocks)
+        t_full, _ = time_steps(full, args.steps, args.warmup, stream, flush, dist, clocks)
         conv_ms = dist.max(statistics.mean(t_conv))
         full_ms = dist.max(statistics.mean(t_full))
         esz = d["q"].element_size()
@@ -447,7 +447,7 @@ def run_ours(args, dist):
                           d_final=d_f, workspace=ws, stream=stream)
 
         steps = min(args.steps, 20)
-        times, _ = time_steps(step, steps, args.warmup, stream, flush, dist)
+        times, _ = time_steps(step, steps, args.warmup, stream, flush, dist, clocks)
         ms = dist.max(statistics.mean(times))
         th = w.token_heads
         esz = d["q"].element_size()
@@ -489,7 +489,7 @@ def run_ours(args, dist):
 
     clocks.start()
     head = measure(args.workload, with_e2e=not args.no_e2e, clocks_=clocks)
-    packed = (measure(PACKED, with_e2e=False)
+    packed = (measure(PACKED, with_e2e=False, clocks_=clocks)
               if args.workload == HEADLINE and not args.no_packed else None)
     prologue = (measure_prologue(PROLOGUE)
                 if args.workload == HEADLINE and not args.no_prologue else None)
