@@ -28,7 +28,7 @@ section "2026-09-29 representative-shape forward A/B").  No dataset is used.
 from __future__ import annotations
 
 import dataclasses
-from typing import List, Optional
+from typing import Optional
 
 import torch
 import torch.nn.functional as F

@@ -6,7 +6,6 @@ fp32 state the previous range left; each head group's forward runs the same
 kernels on the same per-head data) plus oracle parity."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 

@@ -2,7 +2,6 @@
 oracle on the same seeded inputs, element by element, for the five
 workloads of the pages and for edge cases of the packed format.
 """
-import numpy as np
 import pytest
 import torch
 
