@@ -31,7 +31,9 @@
 namespace {
 
 constexpr int kMaxGroups = 2;
-constexpr int kMaxRanges = 8;
+constexpr int kUniformRanges = 8;
+constexpr int kMaxRanges = kUniformRanges + 1;   // the last one may be split in two
+constexpr int kTailTokens = 256;
 constexpr int kMaxDevices = 64;
 static_assert(kMaxGroups <= kMaxRanges, "the head groups use the range events");
 
@@ -42,15 +44,28 @@ static_assert(kMaxGroups <= kMaxRanges, "the head groups use the range events");
 // shape), so the compute keeps up.  Smaller ranges shorten the unhidden
 // tail (the last range's compute and copy back) but add copies, each with
 // a fixed cost of about 2 us: on that shape 4, 8, 16 and 32 ranges measured
-// 1.97, 1.95, 2.02 and 2.15 ms end to end.
+// 1.97, 1.95, 2.02 and 2.15 ms end to end.  The last range, whose compute
+// and copy back are the unhidden tail, is split off into its own last
+// kTailTokens or so tokens (on a chunk boundary) when it is long enough.
 struct RangePlan {
-  int ranges = 1, R = 1;  // number of ranges, tokens per range (but the last)
+  int ranges = 1, R = 1;          // number of ranges, longest range
+  int start[kMaxRanges + 1] = {};  // range r is tokens [start[r], start[r + 1])
 };
 RangePlan plan_ranges(int T) {
   RangePlan rp;
-  const int per16 = ((T + kMaxRanges - 1) / kMaxRanges + kda::kChunk - 1) / kda::kChunk * kda::kChunk;
-  rp.R = std::max(512, per16);
+  const int per = ((T + kUniformRanges - 1) / kUniformRanges + kda::kChunk - 1) /
+                  kda::kChunk * kda::kChunk;
+  rp.R = std::max(512, per);
   rp.ranges = (T + rp.R - 1) / rp.R;
+  for (int r = 0; r < rp.ranges; ++r) rp.start[r] = r * rp.R;
+  rp.start[rp.ranges] = T;
+  // the split point stays on a 64-token chunk boundary of the whole sequence
+  const int split = (T - kTailTokens) / kda::kChunk * kda::kChunk;
+  if (split - rp.start[rp.ranges - 1] >= kTailTokens) {
+    rp.start[rp.ranges + 1] = T;
+    rp.start[rp.ranges] = split;
+    ++rp.ranges;
+  }
   return rp;
 }
 
@@ -191,7 +206,7 @@ kda_status enqueue_time_pipeline(const kda_shape *s, const void *q, const void *
   if (!ok(cudaMemcpyAsync(dev + L.beta_full, beta, B * T * H * 4, cudaMemcpyHostToDevice, cin)))
     return KDA_ERR_CUDA;
   for (int r = 0; r < rp.ranges; ++r) {
-    const size_t t0 = (size_t)r * rp.R, tr = std::min((size_t)rp.R, T - t0);
+    const size_t t0 = (size_t)rp.start[r], tr = (size_t)(rp.start[r + 1] - rp.start[r]);
     // device copy of range r: [B, tr, H, d] at the offset of its first token
     auto at = [&](size_t region, size_t d, size_t esz) {
       return dev + region + B * t0 * H * d * esz;

@@ -48,6 +48,7 @@ HOST_CASES = {
     "b2_bf16_h4_t1600_s0": dict(B=2, T=1600, H=4, K=128, V=128, dtype="bf16", init_state_std=0.1),
     "b3_bf16_h2_t1100": dict(B=3, T=1100, H=2, K=128, V=128, dtype="bf16"),
     "b2_fp32_h2_t1030_d64_s0": dict(B=2, T=1030, H=2, K=64, V=64, dtype="f32", init_state_std=0.1),
+    "b1_fp32_h1_t8200_d32_s0": dict(B=1, T=8200, H=1, K=32, V=32, dtype="f32", init_state_std=0.1),
 }
 
 
