@@ -270,7 +270,8 @@ KDA_API kda_status kda_clear_device_status(void *workspace, kda_stream_t stream)
  * The call copies the inputs in, runs the forward and copies o and
  * final_state back, with the copies overlapped with the compute.  Without
  * segment ids it pipelines over time: the tokens are split into ranges of
- * a multiple of 64 tokens (at least 512, at most 8 ranges), each range's
+ * a multiple of 64 tokens (at least 512, at most 8, the last one split off
+ * into its final 256 or so tokens when long enough), each range's
  * forward enters with the exact fp32 state the previous one left, and the
  * copies in, the forwards and the copies out run on three internal streams,
  * so the result is bitwise that of kda_chunk_fwd on the whole input.  With
