@@ -469,11 +469,11 @@ def run_ours(args, dist):
         return res
 
     def packed_launches(w):
-        """Kernels one packed forward launches: segment runs, chunk
-        coordinates, prep, recurrence (+ the fused kernel AUTO enqueues
+        """Kernels one packed forward launches: segment runs (with the chunk
+        coordinates), prep, recurrence (+ the fused kernel AUTO enqueues
         gated on an overflow of the split items); 2 on the one-kernel paths."""
         if kernel_impl(w) == "split":
-            return 5 if args.kda_impl == "auto" else 4
+            return 4 if args.kda_impl == "auto" else 3
         return 2
 
     def kernel_impl(w):

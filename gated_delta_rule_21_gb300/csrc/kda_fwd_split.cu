@@ -142,10 +142,12 @@ __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
 struct ChunkTable {
   const int32_t *run_chunk_base;     // [B*T] or nullptr (no segment ids)
   const int32_t *chunk_row_offsets;  // [B+1]
-  const int2 *coords;                // [B*T]: {b*T + first token, tokens} per chunk
+  const int2 *coords;                // [B*T]: {b*T + first token, tokens}, row b's
+                                     // chunks from b*T on
   const uint32_t *total_chunks;      // device count
   uint32_t capacity;                 // chunk items the workspace holds
   int n_chunks_row;                  // chunks per row without segment ids
+  int n_rows;                        // B
   int report_overflow;               // set KDA_DEVICE_WORKSPACE on overflow
 };
 
@@ -162,8 +164,13 @@ __device__ __forceinline__ void chunk_of(const ChunkTable &ct, int T, uint32_t k
     end = T;
     return;
   }
-  const int2 e = ct.coords[k];
-  b = e.x / T;
+  int lo = 0, hi = ct.n_rows;  // the row: chunk_row_offsets[lo] <= k < [lo + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)ct.chunk_row_offsets[mid] <= k) lo = mid; else hi = mid;
+  }
+  const int2 e = ct.coords[(size_t)lo * T + (k - (uint32_t)ct.chunk_row_offsets[lo])];
+  b = lo;
   t0 = e.x - b * T;
   end = t0 + e.y;
 }
@@ -1044,6 +1051,7 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   ChunkTable ct;
   ct.report_overflow = with_fallback ? 0 : 1;
   ct.n_chunks_row = (p.T + C - 1) / C;
+  ct.n_rows = p.B;
   ct.capacity = (uint32_t)((workspace_bytes - ioff) / ((size_t)p.H * ITEM_BYTES));
   if (has_seg) {
     ct.run_chunk_base = reinterpret_cast<const int32_t *>(ws + ws_bytes(p.B, p.T, true));

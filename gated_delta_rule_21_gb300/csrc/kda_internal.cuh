@@ -45,8 +45,8 @@ inline size_t ws_bytes(int B, int T, bool has_seg) {
 // The split path with segment ids appends, after ws_bytes(B, T, true):
 //   int32 run_chunk_base[B*T] (first chunk of run i of row b, within the row),
 //   int32 chunk_row_offsets[B+1] (prefix of chunk counts over rows),
-//   int2 chunk_coords[B*T] ({b*T + first token, tokens} of every chunk, in
-//   chunk order; a row of T tokens has at most T chunks),
+//   int2 chunk_coords[B*T] ({b*T + first token, tokens} of every chunk; row
+//   b's chunks in order from b*T on, a row of T tokens having at most T),
 // then its per-chunk items.
 inline size_t ws_chunk_coords_offset(int B, int T) {
   return ws_bytes(B, T, true) + align_up(sizeof(int32_t) * (size_t)B * T, 256) +

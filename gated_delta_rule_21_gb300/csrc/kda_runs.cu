@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads)
                         int o_elem_bytes, const float *initial_state,
                         float *final_state, WsHeader *hdr,
                         int32_t *row_offsets, int2 *runs,
-                        int32_t *run_chunk_base, int32_t *chunk_row_offsets) {
+                        int32_t *run_chunk_base, int32_t *chunk_row_offsets, int2 *coords) {
   __shared__ unsigned long long sm_scan[32];
   __shared__ int sm_pad[kTile];
   __shared__ int sm_is_last;
@@ -137,21 +137,31 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // Chunks of 64 tokens per run and their prefix inside the row (for the
-  // split path, whose work items are (run, chunk, head)).
+  // split path, whose work items are (run, chunk, head)), and each chunk's
+  // tokens {b*T + first token, tokens} at coords[b*T + chunk within the row]
+  // (a row has at most T chunks).
   int n_chunks_row = 0;
   if (run_chunk_base) {
     __syncthreads();  // this row's run records are written
     for (int base = 0; base < n_runs; base += blockDim.x) {
       const int i = base + threadIdx.x;
       int cnt = 0;
+      int2 r = make_int2(0, 0);
       if (i < n_runs) {
-        const int2 r = rrow[i];
+        r = rrow[i];
         cnt = (r.y - r.x + kChunk - 1) / kChunk;
       }
       unsigned long long tot;
       const unsigned long long ex =
           block_excl_scan64((unsigned long long)cnt, &tot, sm_scan);
-      if (i < n_runs) run_chunk_base[(size_t)b * T + i] = n_chunks_row + (int)ex;
+      if (i < n_runs) {
+        const int lb = n_chunks_row + (int)ex;
+        run_chunk_base[(size_t)b * T + i] = lb;
+        int2 *crow = coords + (size_t)b * T + lb;
+        const int y0 = b * T + r.x;
+        for (int j = 0; j < cnt; ++j)
+          crow[j] = make_int2(y0 + j * kChunk, min(kChunk, r.y - r.x - j * kChunk));
+      }
       n_chunks_row += (int)tot;
     }
   }
@@ -201,24 +211,6 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Every chunk of every run, in chunk order: {b*T + first token, tokens}, so
-// that the split path's per-chunk work finds its tokens with one load.  One
-// thread per (row, run index).
-__global__ void __launch_bounds__(256)
-    chunk_coords_kernel(int B, int T, const int32_t *__restrict__ row_offsets,
-                        const int2 *__restrict__ runs, const int32_t *__restrict__ run_chunk_base,
-                        const int32_t *__restrict__ chunk_row_offsets, int2 *coords) {
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)B * T) return;
-  const int b = (int)(idx / (size_t)T), i = (int)(idx % (size_t)T);
-  if (i >= row_offsets[b + 1] - row_offsets[b]) return;
-  const int2 r = runs[idx];
-  const int k0 = chunk_row_offsets[b] + run_chunk_base[idx];
-  const int y0 = b * T + r.x;
-  for (int j = 0, t = 0; t < r.y - r.x; ++j, t += kChunk)
-    coords[k0 + j] = make_int2(y0 + t, min(kChunk, r.y - r.x - t));
-}
-
 }  // namespace
 
 cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
@@ -232,20 +224,16 @@ cudaError_t launch_segment_runs(int B, int T, int H, int K, int V,
   int2 *runs =
       reinterpret_cast<int2 *>(ws + sizeof(WsHeader) + ws_row_offsets_bytes(B));
   int32_t *chunk_base = nullptr, *chunk_rows = nullptr;
+  int2 *coords = nullptr;
   if (with_chunks) {
+    coords = reinterpret_cast<int2 *>(ws + ws_chunk_coords_offset(B, T));
     chunk_base = reinterpret_cast<int32_t *>(ws + ws_bytes(B, T, true));
     chunk_rows = reinterpret_cast<int32_t *>(ws + ws_bytes(B, T, true) +
                                              align_up(sizeof(int32_t) * (size_t)B * T, 256));
   }
   segment_runs_kernel<<<B, kThreads, 0, stream>>>(
       B, T, H, K, V, segment_ids, static_cast<char *>(o), o_is_bf16 ? 2 : 4,
-      initial_state, final_state, hdr, row_offsets, runs, chunk_base, chunk_rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !with_chunks) return e;
-  int2 *coords = reinterpret_cast<int2 *>(ws + ws_chunk_coords_offset(B, T));
-  const size_t n = (size_t)B * T;
-  chunk_coords_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
-      B, T, row_offsets, runs, chunk_base, chunk_rows, coords);
+      initial_state, final_state, hdr, row_offsets, runs, chunk_base, chunk_rows, coords);
   return cudaGetLastError();
 }
 
