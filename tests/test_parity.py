@@ -53,6 +53,9 @@ EDGE = {
                             segments=[[90], [("pad", 96)]]),
     "repeated_id_after_pad": dict(B=1, T=160, H=1, K=128, V=128, init_state_std=0.1,
                                   segments=[50, ("pad", 3), 100]),
+    "padding_rows_between": dict(B=4, T=96, H=2, K=128, V=128, init_state_std=0.1,
+                                 segments=[[("pad", 96)], [40, ("pad", 6), 50],
+                                           [("pad", 96)], [96]]),
 }
 
 
@@ -204,3 +207,32 @@ def test_split_value_tiles(name, v_tile):
     o_ref, fs_ref = run_oracle(x)
     assert_parity(o, o_ref, True, f"{name} v_tile {v_tile} o")
     assert_parity(fs, fs_ref, True, f"{name} v_tile {v_tile} final_state")
+
+
+PACKED_EDGE = ["len1_segments", "boundary_at_64", "long_run_and_pads", "all_padding_row",
+               "repeated_id_after_pad", "padding_rows_between"]
+
+
+@pytest.mark.parametrize("case", PACKED_EDGE)
+def test_split_packed_edge_cases(case):
+    """The packed edge cases on the split path, whose work items come from a
+    per-row chunk table: rows without a run before, between and after rows
+    with runs, runs of one token, run boundaries on chunk edges."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.custom_workload(name=case, **EDGE[case])
+    skip_unless_supported(w, "split")
+    x = ki.make_inputs(w, seed=1)
+    seg = x["segment_ids"]
+    if case == "repeated_id_after_pad":
+        seg[seg == 2] = 1
+    prev = torch.cat([torch.zeros_like(seg[:, :1]), seg[:, :-1]], 1)
+    max_runs = int(((seg != 0) & (seg != prev)).sum(1).max())
+    ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, torch.bfloat16, True, impl="split",
+                             max_runs_per_row=max(max_runs, 1))
+    o, fs = run_gpu(x, impl="split", workspace=ws)
+    assert kda.read_device_status(ws) == 0
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, f"{case} o")
+    assert_parity(fs, fs_ref, True, f"{case} final_state")
+    pad = (seg == 0).numpy()
+    assert torch.all(o.cpu()[torch.from_numpy(pad)] == 0)
