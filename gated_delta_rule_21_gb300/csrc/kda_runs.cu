@@ -11,9 +11,12 @@
 //
 // One CTA per row.  Besides the run list it writes o = 0 for padding tokens
 // (the forward kernels never visit them) and, for a row with no run,
-// final_state = initial_state (or zeros).  The last CTA to finish turns the
-// per-row counts into a prefix (row_offsets) and the total run count, and
-// returns the completion counter to zero so the workspace stays reusable.
+// final_state = initial_state (or zeros).  For the split path it also splits
+// the row's runs into 64-token chunks: each run's first chunk within the row
+// and, per chunk, its first token and length (the row's chunk table).  The
+// last CTA to finish turns the per-row counts into prefixes (row_offsets, and
+// the chunk counts' prefix) and the totals, and returns the completion
+// counter to zero so the workspace stays reusable.
 #include "kda_internal.cuh"
 
 namespace kda {
