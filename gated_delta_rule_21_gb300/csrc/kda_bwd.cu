@@ -28,6 +28,7 @@
 // shared memory, added up every 2 tokens.  This is the first path on the
 // CUDA cores (no tensor cores).
 #include "kda_internal.cuh"
+#include "kda_f32x2.cuh"
 
 namespace kda {
 namespace {
@@ -131,31 +132,67 @@ struct BwdCta {
     }
   }
 
-  // One forward token on S (the staged token tau).
+  // One forward token on S (the staged token tau).  With an even number of
+  // keys per lane, keys lane + 64p and lane + 64p + 32 go through the packed
+  // f32x2 FMA pipe as one pair.
   __device__ void fwd_token(int tau) {
     float kk[KPL], ee[KPL], pr[kCPW];
     load_k_e(tau, kk, ee);
+    const float bt = sm[L::BETA + tau];
+    if constexpr (KPL % 2 == 0) {
+      constexpr int NP = KPL / 2;
+      u64 k2[NP], pr2[kCPW];
 #pragma unroll
-    for (int m = 0; m < kCPW; ++m) pr[m] = 0.f;
+      for (int m = 0; m < kCPW; ++m) pr2[m] = pk2(0.f, 0.f);
 #pragma unroll
-    for (int n = 0; n < KPL; ++n)
+      for (int q = 0; q < NP; ++q) {
+        k2[q] = pk2(kk[2 * q], kk[2 * q + 1]);
+        const u64 e2 = pk2(ee[2 * q], ee[2 * q + 1]);
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m) {
+          const u64 s2 = mul2(pk2(S[2 * q][m], S[2 * q + 1][m]), e2);
+          pr2[m] = fma2(s2, k2[q], pr2[m]);
+          upk2(s2, S[2 * q][m], S[2 * q + 1][m]);
+        }
+      }
 #pragma unroll
       for (int m = 0; m < kCPW; ++m) {
-        S[n][m] *= ee[n];
-        pr[m] = fmaf(S[n][m], kk[n], pr[m]);
+        float a, b;
+        upk2(pr2[m], a, b);
+        pr[m] = a + b;
       }
-    warp_sums(pr);
-    const float bt = sm[L::BETA + tau];
+      warp_sums(pr);
+      const u64 bt2 = pk2(bt, bt);
 #pragma unroll
-    for (int m = 0; m < kCPW; ++m) {
-      const float r = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+      for (int m = 0; m < kCPW; ++m) {
+        const float r = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+        const u64 r2 = pk2(r, r);
 #pragma unroll
-      for (int n = 0; n < KPL; ++n) S[n][m] = fmaf(bt * kk[n], r, S[n][m]);
+        for (int q = 0; q < NP; ++q)
+          upk2(fma2(mul2(bt2, k2[q]), r2, pk2(S[2 * q][m], S[2 * q + 1][m])), S[2 * q][m],
+               S[2 * q + 1][m]);
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) pr[m] = 0.f;
+#pragma unroll
+      for (int n = 0; n < KPL; ++n)
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m) {
+          S[n][m] *= ee[n];
+          pr[m] = fmaf(S[n][m], kk[n], pr[m]);
+        }
+      warp_sums(pr);
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        const float r = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+#pragma unroll
+        for (int n = 0; n < KPL; ++n) S[n][m] = fmaf(bt * kk[n], r, S[n][m]);
+      }
     }
   }
-  // One backward token (the staged token tau, its entering state in BLK);
-  // the per-warp column sums go to slot `slot` of PQ/PK/PG/PB.
-  __device__ void bwd_token(int tau, int slot, size_t th, int vt) {
+  // One backward token with one key per lane (K = 32), scalar fp32.
+  __device__ void bwd_token_scalar(int tau, int slot, size_t th, int vt) {
     float kk[KPL], ee[KPL], qq[KPL];
     load_k_e(tau, kk, ee);
 #pragma unroll
@@ -212,6 +249,97 @@ struct BwdCta {
     for (int m = 1; m < kCPW; ++m)
       if (lane == m) drl = dr[m];
     if (lane < kCPW) p.dv[th * p.V + vt * kVT + c0 + lane] = drl;
+  }
+
+  // One backward token (the staged token tau, its entering state in BLK);
+  // the per-warp column sums go to slot `slot` of PQ/PK/PG/PB.  With an even
+  // number of keys per lane, keys lane + 64p and lane + 64p + 32 are one
+  // f32x2 pair, so the per-key values and the state pairs feed the packed
+  // FMA pipe and only the per-column scalars are broadcast.
+  __device__ void bwd_token(int tau, int slot, size_t th, int vt) {
+    if constexpr (KPL % 2 != 0) {
+      bwd_token_scalar(tau, slot, th, vt);
+    } else {
+      constexpr int NP = KPL / 2;
+      const float *bk = sm + L::BLK + (size_t)tau * kVT * K;
+      const float bt = sm[L::BETA + tau];
+      const u64 bt2 = pk2(bt, bt), sc2 = pk2(p.scale, p.scale);
+      u64 k2[NP], e2[NP], Sp2[NP][kCPW], dS2[NP][kCPW], dov2[kCPW], pr2[kCPW], pa2[kCPW];
+      float dov[kCPW];
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        dov[m] = sm[L::DO + tau * kVT + c0 + m];
+        dov2[m] = pk2(dov[m], dov[m]);
+        pr2[m] = pk2(0.f, 0.f);
+        pa2[m] = pk2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        const int i0 = tau * K + lane + 64 * q;
+        k2[q] = pk2(sm[L::KK + i0], sm[L::KK + i0 + 32]);
+        e2[q] = pk2(sm[L::E + i0], sm[L::E + i0 + 32]);
+        const u64 sq2 = mul2(sc2, pk2(sm[L::Q + i0], sm[L::Q + i0 + 32]));
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m) {
+          const float *col = bk + (c0 + m) * K + lane + 64 * q;
+          Sp2[q][m] = mul2(pk2(col[0], col[32]), e2[q]);
+          pr2[m] = fma2(Sp2[q][m], k2[q], pr2[m]);
+          // o_t = scale S_t^T q_t
+          dS2[q][m] = fma2(sq2, dov2[m], pk2(dS[2 * q][m], dS[2 * q + 1][m]));
+          pa2[m] = fma2(dS2[q][m], k2[q], pa2[m]);
+        }
+      }
+      float pr[kCPW], pa[kCPW];
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        float a, b;
+        upk2(pr2[m], a, b);
+        pr[m] = a + b;
+        upk2(pa2[m], a, b);
+        pa[m] = a + b;
+      }
+      warp_sums(pr);
+      warp_sums(pa);
+      float r[kCPW], dr[kCPW], db = 0.f;
+      u64 r2[kCPW], ndr2[kCPW], btr2[kCPW];
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) {
+        r[m] = sm[L::VV + tau * kVT + c0 + m] - pr[m];
+        dr[m] = bt * pa[m];
+        db = fmaf(pa[m], r[m], db);
+        r2[m] = pk2(r[m], r[m]);
+        ndr2[m] = pk2(-dr[m], -dr[m]);
+        btr2[m] = pk2(bt * r[m], bt * r[m]);
+      }
+      float* const pq = sm + L::PQ + (slot * kWarps + warp) * K;
+      float* const pk = sm + L::PK + (slot * kWarps + warp) * K;
+      float* const pg = sm + L::PG + (slot * kWarps + warp) * K;
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        const u64 btk2 = mul2(bt2, k2[q]);
+        u64 aq2 = pk2(0.f, 0.f), ak2 = pk2(0.f, 0.f), ag2 = pk2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < kCPW; ++m) {
+          const u64 st2 = fma2(btk2, r2[m], Sp2[q][m]);             // S_t
+          aq2 = fma2(st2, dov2[m], aq2);
+          ak2 = fma2(dS2[q][m], btr2[m], ak2);                       // beta dS r
+          ak2 = fma2(Sp2[q][m], ndr2[m], ak2);                       // - S' dr
+          const u64 dsp2 = fma2(k2[q], ndr2[m], dS2[q][m]);          // dS'
+          ag2 = fma2(Sp2[q][m], dsp2, ag2);
+          upk2(mul2(e2[q], dsp2), dS[2 * q][m], dS[2 * q + 1][m]);   // gradient of S_{t-1}
+        }
+        const int i = lane + 64 * q;
+        upk2(mul2(sc2, aq2), pq[i], pq[i + 32]);
+        upk2(ak2, pk[i], pk[i + 32]);
+        upk2(ag2, pg[i], pg[i + 32]);
+      }
+      if (lane == 0) sm[L::PB + slot * kWarps + warp] = db;
+      float drl = dr[0];
+#pragma unroll
+      for (int m = 1; m < kCPW; ++m)
+        if (lane == m) drl = dr[m];
+      if (lane < kCPW) p.dv[th * p.V + vt * kVT + c0 + lane] = drl;
+    }
   }
 
   // The column sums of `count` tokens (slot s = token t_hi - s), over the

@@ -35,6 +35,7 @@
 //   * A head of K channels is K/8 adjacent lanes, so the L2 norm of q and k
 //     is a shuffle reduction inside the warp, done for 3 tokens at a time.
 #include "kda_internal.cuh"
+#include "kda_f32x2.cuh"
 
 namespace kda {
 namespace {
@@ -84,32 +85,6 @@ __device__ __forceinline__ float sfu_rcp(float x) {
   return y;
 }
 
-// Two fp32 lanes in one 64-bit register pair, for the packed f32x2
-// arithmetic of the FMA pipe.
-typedef unsigned long long u64;
-__device__ __forceinline__ u64 pk2(float a, float b) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk2(u64 r, float &a, float &b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-  u64 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
-  u64 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ u64 add2(u64 a, u64 b) {
-  u64 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 // 8 channels of one staged row (shared layout [row][16-byte piece][thread]).
 __device__ __forceinline__ void lds8(const unsigned char *row, int tid, const __nv_bfloat16 *,
                                      float (&f)[kVec]) {
