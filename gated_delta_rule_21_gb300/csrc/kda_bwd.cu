@@ -21,7 +21,8 @@
 // every 8th token (global scratch, per CTA); then, block by block from the
 // end, the block is replayed from its checkpoint with the states kept in
 // shared memory and walked backwards.  512 threads: warp w owns the tile's
-// value columns 2w, 2w + 1 for all keys (lane l: keys l, l + 32, ...).
+// value columns 2w, 2w + 1 for all keys (lane l: the K / 32 keys from
+// (K / 32) l on).
 // The value columns are independent in the recurrence, so each warp's chain
 // needs only in-warp sums over keys and no block barrier per token; the
 // sums over value columns (dq, dk, dg, dbeta) are per-warp partials in
@@ -69,8 +70,36 @@ __device__ __forceinline__ void warp_sums(float (&x)[N]) {
   }
 }
 
-// One CTA's walk of one unit.  Lane l of warp w holds keys l, l + 32, ...
-// (K / 32 of them) for the warp's kCPW value columns.  The state
+// N consecutive floats (N = 1, 2 or 4; src and dst 4N-byte aligned) in one
+// load or store.
+template <int N>
+__device__ __forceinline__ void ld_vec(const float *src, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const float4 x = *reinterpret_cast<const float4 *>(src);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if constexpr (N == 2) {
+    const float2 x = *reinterpret_cast<const float2 *>(src);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = src[i];
+  }
+}
+template <int N>
+__device__ __forceinline__ void st_vec(float *dst, const float (&v)[N]) {
+  if constexpr (N == 4) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (N == 2) {
+    *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) dst[i] = v[i];
+  }
+}
+
+// One CTA's walk of one unit.  Lane l of warp w holds the K / 32 consecutive
+// keys KPL l .. KPL l + KPL - 1 (one vector load or store of each per-key
+// row) for the warp's kCPW value columns.  The state
 // recurrence is independent per value column, so a warp's chain needs only
 // in-warp sums over keys; the sums over value columns (dq, dk, dg, dbeta)
 // are per-warp partials in shared memory, added up every kFlush tokens.
@@ -82,6 +111,8 @@ struct BwdCta {
   float *sm;
   int warp, lane, c0;
   float S[KPL][kCPW], dS[KPL][kCPW];
+
+  __device__ int key0() const { return lane * KPL; }   // this lane's first key
 
   __device__ BwdCta(const BwdParams &p_, float *sm_) : p(p_), sm(sm_) {
     warp = threadIdx.x >> 5;
@@ -125,16 +156,13 @@ struct BwdCta {
   }
 
   __device__ void load_k_e(int tau, float (&kk)[KPL], float (&ee)[KPL]) const {
-#pragma unroll
-    for (int n = 0; n < KPL; ++n) {
-      kk[n] = sm[L::KK + tau * K + lane + 32 * n];
-      ee[n] = sm[L::E + tau * K + lane + 32 * n];
-    }
+    ld_vec(sm + L::KK + tau * K + key0(), kk);
+    ld_vec(sm + L::E + tau * K + key0(), ee);
   }
 
   // One forward token on S (the staged token tau).  With an even number of
-  // keys per lane, keys lane + 64p and lane + 64p + 32 go through the packed
-  // f32x2 FMA pipe as one pair.
+  // keys per lane, neighbouring keys go through the packed f32x2 FMA pipe as
+  // one pair.
   __device__ void fwd_token(int tau) {
     float kk[KPL], ee[KPL], pr[kCPW];
     load_k_e(tau, kk, ee);
@@ -196,7 +224,7 @@ struct BwdCta {
     float kk[KPL], ee[KPL], qq[KPL];
     load_k_e(tau, kk, ee);
 #pragma unroll
-    for (int n = 0; n < KPL; ++n) qq[n] = sm[L::Q + tau * K + lane + 32 * n];
+    for (int n = 0; n < KPL; ++n) qq[n] = sm[L::Q + tau * K + key0() + n];
     const float *bk = sm + L::BLK + (size_t)tau * kVT * K;
     const float bt = sm[L::BETA + tau];
     float dov[kCPW], Sp[KPL][kCPW], pr[kCPW], pa[kCPW];
@@ -210,7 +238,7 @@ struct BwdCta {
     for (int n = 0; n < KPL; ++n)
 #pragma unroll
       for (int m = 0; m < kCPW; ++m) {
-        Sp[n][m] = bk[(c0 + m) * K + lane + 32 * n] * ee[n];
+        Sp[n][m] = bk[(c0 + m) * K + key0() + n] * ee[n];
         pr[m] = fmaf(Sp[n][m], kk[n], pr[m]);
         dS[n][m] = fmaf(p.scale * qq[n], dov[m], dS[n][m]);   // o_t = scale S_t^T q_t
         pa[m] = fmaf(dS[n][m], kk[n], pa[m]);
@@ -239,9 +267,9 @@ struct BwdCta {
         ag = fmaf(Sp[n][m], dsp, ag);
         dS[n][m] = ee[n] * dsp;                                     // gradient of S_{t-1}
       }
-      pq[lane + 32 * n] = p.scale * aq;
-      pk[lane + 32 * n] = ak;
-      pg[lane + 32 * n] = ag;
+      pq[key0() + n] = p.scale * aq;
+      pk[key0() + n] = ak;
+      pg[key0() + n] = ag;
     }
     if (lane == 0) sm[L::PB + slot * kWarps + warp] = db;
     float drl = dr[0];
@@ -253,9 +281,9 @@ struct BwdCta {
 
   // One backward token (the staged token tau, its entering state in BLK);
   // the per-warp column sums go to slot `slot` of PQ/PK/PG/PB.  With an even
-  // number of keys per lane, keys lane + 64p and lane + 64p + 32 are one
-  // f32x2 pair, so the per-key values and the state pairs feed the packed
-  // FMA pipe and only the per-column scalars are broadcast.
+  // number of keys per lane, neighbouring keys are one f32x2 pair, so the
+  // per-key values and the state pairs feed the packed FMA pipe and only the
+  // per-column scalars are broadcast.
   __device__ void bwd_token(int tau, int slot, size_t th, int vt) {
     if constexpr (KPL % 2 != 0) {
       bwd_token_scalar(tau, slot, th, vt);
@@ -273,16 +301,20 @@ struct BwdCta {
         pr2[m] = pk2(0.f, 0.f);
         pa2[m] = pk2(0.f, 0.f);
       }
+      float kk[KPL], ee[KPL], qq[KPL], sp[kCPW][KPL];
+      ld_vec(sm + L::KK + tau * K + key0(), kk);
+      ld_vec(sm + L::E + tau * K + key0(), ee);
+      ld_vec(sm + L::Q + tau * K + key0(), qq);
+#pragma unroll
+      for (int m = 0; m < kCPW; ++m) ld_vec(bk + (c0 + m) * K + key0(), sp[m]);
 #pragma unroll
       for (int q = 0; q < NP; ++q) {
-        const int i0 = tau * K + lane + 64 * q;
-        k2[q] = pk2(sm[L::KK + i0], sm[L::KK + i0 + 32]);
-        e2[q] = pk2(sm[L::E + i0], sm[L::E + i0 + 32]);
-        const u64 sq2 = mul2(sc2, pk2(sm[L::Q + i0], sm[L::Q + i0 + 32]));
+        k2[q] = pk2(kk[2 * q], kk[2 * q + 1]);
+        e2[q] = pk2(ee[2 * q], ee[2 * q + 1]);
+        const u64 sq2 = mul2(sc2, pk2(qq[2 * q], qq[2 * q + 1]));
 #pragma unroll
         for (int m = 0; m < kCPW; ++m) {
-          const float *col = bk + (c0 + m) * K + lane + 64 * q;
-          Sp2[q][m] = mul2(pk2(col[0], col[32]), e2[q]);
+          Sp2[q][m] = mul2(pk2(sp[m][2 * q], sp[m][2 * q + 1]), e2[q]);
           pr2[m] = fma2(Sp2[q][m], k2[q], pr2[m]);
           // o_t = scale S_t^T q_t
           dS2[q][m] = fma2(sq2, dov2[m], pk2(dS[2 * q][m], dS[2 * q + 1][m]));
@@ -311,9 +343,7 @@ struct BwdCta {
         ndr2[m] = pk2(-dr[m], -dr[m]);
         btr2[m] = pk2(bt * r[m], bt * r[m]);
       }
-      float* const pq = sm + L::PQ + (slot * kWarps + warp) * K;
-      float* const pk = sm + L::PK + (slot * kWarps + warp) * K;
-      float* const pg = sm + L::PG + (slot * kWarps + warp) * K;
+      float aq[KPL], ak[KPL], ag[KPL];
 #pragma unroll
       for (int q = 0; q < NP; ++q) {
         const u64 btk2 = mul2(bt2, k2[q]);
@@ -328,11 +358,13 @@ struct BwdCta {
           ag2 = fma2(Sp2[q][m], dsp2, ag2);
           upk2(mul2(e2[q], dsp2), dS[2 * q][m], dS[2 * q + 1][m]);   // gradient of S_{t-1}
         }
-        const int i = lane + 64 * q;
-        upk2(mul2(sc2, aq2), pq[i], pq[i + 32]);
-        upk2(ak2, pk[i], pk[i + 32]);
-        upk2(ag2, pg[i], pg[i + 32]);
+        upk2(mul2(sc2, aq2), aq[2 * q], aq[2 * q + 1]);
+        upk2(ak2, ak[2 * q], ak[2 * q + 1]);
+        upk2(ag2, ag[2 * q], ag[2 * q + 1]);
       }
+      st_vec(sm + L::PQ + (slot * kWarps + warp) * K + key0(), aq);
+      st_vec(sm + L::PK + (slot * kWarps + warp) * K + key0(), ak);
+      st_vec(sm + L::PG + (slot * kWarps + warp) * K + key0(), ag);
       if (lane == 0) sm[L::PB + slot * kWarps + warp] = db;
       float drl = dr[0];
 #pragma unroll
@@ -381,15 +413,17 @@ struct BwdCta {
 #pragma unroll
       for (int m = 0; m < kCPW; ++m)
         S[n][m] = (u.first && p.initial_state)
-                      ? p.initial_state[st0 + (size_t)(lane + 32 * n) * p.V + m] : 0.f;
+                      ? p.initial_state[st0 + (size_t)(key0() + n) * p.V + m] : 0.f;
     // forward over the run, keeping S at every kCKB-th token
     for (int c = 0; c < nck; ++c) {
       const int t0 = u.start + c * kCKB, n = min(kCKB, u.end - t0);
 #pragma unroll
-      for (int kn = 0; kn < KPL; ++kn)
+      for (int m = 0; m < kCPW; ++m) {
+        float t[KPL];
 #pragma unroll
-        for (int m = 0; m < kCPW; ++m)
-          ck[((size_t)c * kVT + c0 + m) * K + lane + 32 * kn] = S[kn][m];
+        for (int kn = 0; kn < KPL; ++kn) t[kn] = S[kn][m];
+        st_vec(ck + ((size_t)c * kVT + c0 + m) * K + key0(), t);
+      }
       stage(b, h, vt, t0, n, false);
       __syncthreads();
       for (int tau = 0; tau < n; ++tau) fwd_token(tau);
@@ -401,21 +435,27 @@ struct BwdCta {
 #pragma unroll
       for (int m = 0; m < kCPW; ++m)
         dS[n][m] = (u.last && p.d_final)
-                       ? p.d_final[st0 + (size_t)(lane + 32 * n) * p.V + m] : 0.f;
+                       ? p.d_final[st0 + (size_t)(key0() + n) * p.V + m] : 0.f;
     for (int c = nck - 1; c >= 0; --c) {
       const int t0 = u.start + c * kCKB, n = min(kCKB, u.end - t0);
 #pragma unroll
-      for (int kn = 0; kn < KPL; ++kn)
+      for (int m = 0; m < kCPW; ++m) {
+        float t[KPL];
+        ld_vec(ck + ((size_t)c * kVT + c0 + m) * K + key0(), t);
 #pragma unroll
-        for (int m = 0; m < kCPW; ++m) S[kn][m] = ck[((size_t)c * kVT + c0 + m) * K + lane + 32 * kn];
+        for (int kn = 0; kn < KPL; ++kn) S[kn][m] = t[kn];
+      }
       stage(b, h, vt, t0, n, true);
       __syncthreads();
       for (int tau = 0; tau < n; ++tau) {   // replay: the state entering each token
         float *bk = sm + L::BLK + (size_t)tau * kVT * K;
 #pragma unroll
-        for (int kn = 0; kn < KPL; ++kn)
+        for (int m = 0; m < kCPW; ++m) {
+          float t[KPL];
 #pragma unroll
-          for (int m = 0; m < kCPW; ++m) bk[(c0 + m) * K + lane + 32 * kn] = S[kn][m];
+          for (int kn = 0; kn < KPL; ++kn) t[kn] = S[kn][m];
+          st_vec(bk + (c0 + m) * K + key0(), t);
+        }
         if (tau + 1 < n) fwd_token(tau);
       }
       for (int hi = n - 1; hi >= 0; hi -= kFlush) {   // groups of kFlush tokens
@@ -430,14 +470,14 @@ struct BwdCta {
       for (int n = 0; n < KPL; ++n)
 #pragma unroll
         for (int m = 0; m < kCPW; ++m)
-          p.d_initial[st0 + (size_t)(lane + 32 * n) * p.V + m] = dS[n][m];
+          p.d_initial[st0 + (size_t)(key0() + n) * p.V + m] = dS[n][m];
     }
   }
 };
 
 template <typename TI, int K>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_simt_kernel(const BwdParams p) {
-  extern __shared__ float bwd_sm[];
+  extern __shared__ __align__(16) float bwd_sm[];
   BwdCta<TI, K> cta(p, bwd_sm);
   const uint32_t n_units = total_units(p.runs, p.B, p.H, p.n_vtiles);
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
