@@ -236,3 +236,21 @@ def test_split_packed_edge_cases(case):
     assert_parity(fs, fs_ref, True, f"{case} final_state")
     pad = (seg == 0).numpy()
     assert torch.all(o.cpu()[torch.from_numpy(pad)] == 0)
+
+
+@pytest.mark.parametrize("name", ["packed_bf16_h8_t1024_4seg", "packed_bf16_h32_t8192_25seg"])
+def test_packed_in_benchmark_configuration(name):
+    """The packed workloads through AUTO with a workspace sized for their runs
+    per row, the configuration the benchmark times (the split path), against
+    the oracle on every output."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.WORKLOADS[name]
+    skip_unless_supported(w, "split")
+    x = ki.make_inputs(w, seed=0)
+    ws = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, torch.bfloat16, True, impl="auto",
+                             max_runs_per_row=len(w.segments))
+    o, fs = run_gpu(x, workspace=ws)
+    assert kda.read_device_status(ws) == 0
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, f"{name} o")
+    assert_parity(fs, fs_ref, True, f"{name} final_state")
