@@ -71,6 +71,9 @@ CASES = {
                              [64, 64, ("pad", 2), 170]]),
     "all_padding_row": dict(B=2, T=96, H=2, K=64, V=64, dtype="f32", init_state_std=0.1,
                             segments=[[90], [("pad", 96)]]),
+    "padding_rows_between": dict(B=4, T=96, H=2, K=128, V=128, init_state_std=0.1,
+                                 segments=[[("pad", 96)], [40, ("pad", 6), 50],
+                                           [("pad", 96)], [96]]),
 }
 
 
