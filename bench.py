@@ -570,10 +570,18 @@ def cpu_baseline(w, seed, budget_s=10.0):
         runs += 1
     per_run = t_total / runs
     tokens_equiv = w.B * w.T * heads / w.H
+    # and on one thread, the whole B1 H8 T1024 fixed workload
+    w1 = ki.WORKLOADS["fixed_bf16_h8_t1024"]
+    a1, s1, seg1, scale1 = oracle_sample(w1, seed, w1.H)
+    t = time.perf_counter()
+    oracle.kda_forward(*a1, scale1, initial_state=s1, segment_ids=seg1, threads=1)
+    t1 = time.perf_counter() - t
     return {"value": tokens_equiv / per_run, "unit": "tokens/s", "cores": min(cores, w.B * heads),
-            "kind": "oracle",
+            "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{heads} of {w.H} heads x {w.B * w.T} tokens (fp64 token recurrence), "
-                      f"{runs} runs, {t_total:.1f} s; tokens/s scaled by heads/H"}
+                      f"{runs} runs, {t_total:.1f} s; tokens/s scaled by heads/H",
+            "one_thread": {"workload": w1.name, "ms": round(t1 * 1e3, 1),
+                           "value": w1.B * w1.T / t1, "unit": "tokens/s", "threads": 1}}
 
 
 def cpu_baseline_backward(w, seed, budget_s=5.0):

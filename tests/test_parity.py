@@ -254,3 +254,41 @@ def test_packed_in_benchmark_configuration(name):
     o_ref, fs_ref = run_oracle(x)
     assert_parity(o, o_ref, True, f"{name} o")
     assert_parity(fs, fs_ref, True, f"{name} final_state")
+
+
+def _bf16_order_key(t):
+    """bf16 bit patterns as integers ordered like the values (+0 and -0 equal)."""
+    import numpy as np
+    u = t.contiguous().view(torch.int16).numpy().astype(np.int32) & 0xFFFF
+    mag = u & 0x7FFF
+    return np.where(u & 0x8000, -mag, mag)
+
+
+@pytest.mark.parametrize("name", ["fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg"])
+def test_bf16_ulp_distance_report(name, capsys):
+    """Diagnostic: the distance in bf16 ULPs between the kernel's o and the
+    fp64 oracle rounded to bf16 (via fp32), over outputs with |o| at least
+    1e-3 of the largest (near zero a ULP means nothing).  The only bound
+    asserted follows from the rel-L2 tolerance of 1e-2: a relative error of
+    1e-2 is at most about 5 ULPs of bf16 (8 significand bits), so the median
+    must not exceed that."""
+    import numpy as np
+    w = ki.WORKLOADS[name]
+    x = ki.make_inputs(w, seed=0)
+    o, _ = run_gpu(x)
+    o_ref, _ = run_oracle(x)
+    ref = torch.from_numpy(np.asarray(o_ref)).to(torch.float32).to(torch.bfloat16)
+    d_all = np.abs(_bf16_order_key(o.cpu()) - _bf16_order_key(ref))
+    mag = np.abs(np.asarray(o_ref))
+    # a distance across zero counts every binade in between, so the maximum
+    # over small outputs says little; |o| >= 0.1 max is the well-scaled part
+    for frac in (1e-3, 1e-1):
+        d = d_all[mag >= frac * mag.max()]
+        p50, p99, mx = np.percentile(d, 50), np.percentile(d, 99), d.max()
+        exact = float(np.mean(d == 0))
+        with capsys.disabled():
+            print(f"\n{name}: bf16 ULP distance of o over the {d.size} outputs with |o| >= "
+                  f"{frac:g} max: median {p50:.0f}, p99 {p99:.0f}, max {mx}, "
+                  f"exact {100 * exact:.1f} %")
+        if frac == 1e-3:
+            assert p50 <= 5
