@@ -103,6 +103,10 @@ def lib():
         L.kda_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
                                     vp, vp, vp, vp, u64, vp]
         L.kda_chunk_bwd.restype = i
+        L.kda_chunk_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp]
+        L.kda_chunk_fwd_noalloc.restype = i
+        L.kda_chunk_fwd_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.kda_chunk_fwd_noalloc_status.restype = i
         L.kda_selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
         L.kda_selftest_wait_timeout.restype = i
         _lib = L
@@ -131,7 +135,9 @@ def make_shape(B, T, H, K, V, dtype) -> kda_shape:
 
 def workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
                    impl=None) -> int:
-    """Workspace bytes: the minimum (impl None) or what ``impl`` needs."""
+    """Workspace bytes: what the fastest kernel needs (impl None, the C
+    default query) or what ``impl`` needs ("simt" gives the smallest size
+    any path accepts)."""
     s = make_shape(B, T, H, K, V, dtype)
     if impl is None:
         return int(lib().kda_chunk_fwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))

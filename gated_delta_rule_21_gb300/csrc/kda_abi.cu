@@ -29,6 +29,8 @@ bool aligned(const void *p, uintptr_t a) {
 
 bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
 
+}  // namespace
+
 kda_status check_shape(const kda_shape *s) {
   if (!s) return KDA_ERR_INVALID_ARG;
   if (s->B < 1 || s->T < 1 || s->H < 1) return KDA_ERR_INVALID_ARG;
@@ -39,6 +41,8 @@ kda_status check_shape(const kda_shape *s) {
   if ((long long)s->B * s->T * s->H * d >= (1ll << 31)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
+
+namespace {
 
 // Runs per row the default split workspace is sized for (runs of 64 tokens
 // on average).
@@ -74,8 +78,8 @@ const char *kda_status_string(kda_status st) {
 int kda_version(void) { return KDA_VERSION; }
 
 size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids) {
-  if (check_shape(s) != KDA_OK) return 0;
-  return ws_bytes(s->B, s->T, has_segment_ids != 0);
+  // The size AUTO needs for its fastest kernel on this shape.
+  return kda_chunk_fwd_workspace_size_for(s, has_segment_ids, KDA_IMPL_AUTO);
 }
 
 size_t kda_chunk_fwd_workspace_size_for(const kda_shape *s, int has_segment_ids,

@@ -41,9 +41,11 @@ constexpr int VD = 128;
 constexpr int VT = 32;
 
 // ---- one workspace item (per row, chunk, head) ----------------------------
-constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: K-major, 128 rows, Kd 128
+// Each region is already in the shared-memory operand layout the recurrence
+// kernel's MMAs read, so a stage is a plain bulk copy of the item.
+constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: MN-major, 128 rows x Kd 128 channels
 constexpr uint32_t I_AQK = 32768;     // A_qk: K-major, 64 rows, Kd 64
-constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: MN-major, 128 x Kd 64
+constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: K-major, 128 channels x Kd 64 rows
 constexpr uint32_t I_U = 57344;       // u bf16 [vt][r][32]
 constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
 constexpr uint32_t ITEM_BYTES = 74240;     // 72.5 KiB, 256-byte aligned
@@ -54,67 +56,57 @@ constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
 // CTA's serial phases (the block solve, the MMA round trips) overlap the
 // other's.  To fit two CTAs, the intra-chunk operands are built in two
 // halves of 64 key channels (the A products accumulate over both halves on
-// the tensor cores).  Shared memory (offsets from a 1 KiB-aligned base):
-//   RAW   q, k (64 rows x 64 channels bf16) and g (64 x 64 fp32) of one
-//         channel half, TMA 128-byte swizzle (16-byte unit u of row r at
-//         u ^ (r % 8)), so that row- and column-wise reads are conflict free;
-//   X, Y  [K e1 ; Q e1] (128 rows) and Y_0..Y_3 (160 rows), Kd 64 each;
-//   RHST  [K e^G | V]^T, MN-major 256 x Kd 64 (v lands here by TMA);
-//   solver fp32 buffers, aliased over RAW + X + Y once the A products are
-//   in TMEM.
+// the tensor cores).
+//
+// Elementwise work (gate cumsum, decay factors, operand tiles) is done by
+// channel owners: thread (c, b) holds key channel c of the half for the 16
+// rows of sub-block b, so the cumsum runs down its own registers, every
+// per-(block, channel) factor is a per-thread constant, and each operand is
+// written in the layout that keeps a channel's 8 consecutive rows in one
+// 16-byte chunk: MN-major X, Y (A products) and Q e^G (item), K-major
+// (K e^G)^T (the w product) and (K e^{G_C-G})^T (item).  w is produced
+// transposed, w^T = (K e^G)^T (T diag(beta))^T, so its TMEM lanes are
+// channels too and its rows leave TMEM as MN-major 16-byte chunks.
+//
+// Shared memory (offsets from a 1 KiB-aligned base):
+//   RAW   q, k (64 rows x 64 channels bf16, 128 B per row) and g (two
+//         64 x 32 fp32 boxes, 128 B per row) of one channel half, no swizzle:
+//         a warp reads 32 consecutive channels of one row;
+//   X, Y  [K e1 ; Q e1] (128 rows) and Y_0..Y_3 (160 rows), MN-major, Kd 64;
+//   KT    (K e^G)^T, K-major, 128 channels x Kd 64 rows (both halves);
+//   TB    T diag(beta), K-major, 64 rows x Kd 64 (the w product's B operand,
+//         and the u product's A operand, whose rows 64..127 read V: ignored);
+//   V     v, MN-major, 128 columns x Kd 64 rows (TMA);
+//   solver fp32 buffers, aliased over RAW + X once the A products are in
+//   TMEM.
 constexpr int PT = 256;                       // threads
 constexpr int KH = 64;                        // key channels per half
 constexpr uint32_t P_RAW_Q = 0, P_RAW_K = 8192, P_RAW_G = 16384;
 constexpr uint32_t P_RAW_TX = 8192 * 2 + 16384;
-constexpr uint32_t P_V_TX = 16384;
 constexpr uint32_t P_X = 32768;               // 128 x Kd 64
 constexpr uint32_t P_Y = P_X + 16384;         // Y_0..Y_3, 160 rows x Kd 64
-constexpr uint32_t P_RHST = P_Y + 20480;      // 256 x Kd 64, MN-major
-constexpr uint32_t P_MISC = P_RHST + 32768;
+constexpr uint32_t P_KT = P_Y + 20480;        // 128 x Kd 64, K-major
+constexpr uint32_t P_TB = P_KT + 16384;       // 64 x Kd 64, K-major
+constexpr uint32_t P_V = P_TB + 8192;         // 128 x Kd 64, MN-major
+constexpr uint32_t P_V_TX = 16384;
+constexpr uint32_t P_MISC = P_V + 16384;
 constexpr uint32_t P_BETA = P_MISC;           // 64 fp32
-constexpr uint32_t P_DBLK = P_MISC + 256;     // 4 x 128 fp32: e^{block sum of g}
-constexpr uint32_t P_BSUM = P_DBLK + 2048;    // 4 x 64 fp32 block sums (one half)
-constexpr uint32_t P_FAC = P_BSUM + 1024;     // factor table, 4 x 7 x 64 fp32
-constexpr uint32_t P_BAR = P_FAC + 7168;      // raw, mma, v
+constexpr uint32_t P_BSUM = P_BETA + 256;     // 4 x 64 fp32: log2e x block sums of g (one half)
+constexpr uint32_t P_BAR = P_BSUM + 1024;     // raw, mma, v
 constexpr uint32_t P_SLOT = P_BAR + 24;
 constexpr uint32_t P_ABORT = P_SLOT + 4;
-constexpr uint32_t P_SMEM = P_ABORT + 20;
+constexpr uint32_t P_SMEM = P_ABORT + 12;
 constexpr uint32_t P_ALLOC = P_SMEM + 1024;
 constexpr int LDF = C + 4;
 constexpr uint32_t P_AKK = 0;                      // fp32 64 x 68 (beta A_kk)
 constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68 (T)
-constexpr uint32_t P_TB = P_TF + 64 * LDF * 4;     // T diag(beta) bf16, K-major rows 0..63
-constexpr uint32_t P_SCR = P_TB + 8192;            // 10 blocks of 16 x LDS fp32
+constexpr uint32_t P_SCR = P_TF + 64 * LDF * 4;    // 10 blocks of 16 x LDS fp32
 constexpr int LDS = 20;                            // padded: conflict-free rows
-static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_RHST && P_TB + 16384 <= P_RHST,
-              "solver buffers and the 128-row T operand (rows 64..127 ignored) stay below RHST");
-static_assert(P_RHST % 1024 == 0 && P_X % 1024 == 0, "operand alignment");
-// Per-(block, channel) factors of one channel half, built with the cumsum and
-// read by the operand build: prod_{i<b} D_i, prod_{i>b} D_i, 1/D_b, D_{b+1},
-// D_{b+1} D_{b+2}, and (log2e times) G before block b and at its last row.
-enum { F_PRE, F_SUF, F_RD, F_X2, F_X3, F_PL, F_EL, kFac };
-static_assert(kNumSub * kFac * KH * 4 == 7168, "factor table size");
+static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_Y, "solver buffers stay in RAW + X");
+static_assert(P_TB + 16384 <= P_V + 16384, "the u product's 128-row A operand stays in smem");
+static_assert(P_X % 1024 == 0 && P_Y % 1024 == 0 && P_KT % 1024 == 0 && P_V % 1024 == 0,
+              "operand alignment");
 static_assert(2 * (P_ALLOC + 1024) <= 233472, "two prep CTAs fit one SM");
-
-// Byte offsets of element (row r, channel c of the half) in the raw tiles.
-__device__ __forceinline__ uint32_t kq_off(int r, int c) {
-  return (uint32_t)(r * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
-}
-__device__ __forceinline__ uint32_t g_off(int r, int c) {
-  return (uint32_t)((c >> 5) * 8192 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
-}
-__device__ __forceinline__ void ld_f32x8s(const float *p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4 *>(p);
-  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void ld_f32x8(const unsigned char *tile, int r, int c8, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4 *>(tile + g_off(r, c8));
-  const float4 b = *reinterpret_cast<const float4 *>(tile + g_off(r, c8 + 4));
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 
 // Y_0..Y_3 are stored back to back (row groups of 8), so together they form
 // one 160-row B operand: a single N = 160 MMA gives X Y_b^T for every b at
@@ -216,6 +208,18 @@ __device__ __forceinline__ void blk_prod(float *dst, int ldd, const float *X, in
   }
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+
+// 8 fp32 values (consecutive rows of one channel) as one 16-byte bf16 chunk.
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                    pack_bf16(v[6], v[7]));
+}
+__device__ __forceinline__ uint4 pack8s(const float (&v)[8], float s) {
+  return make_uint4(pack_bf16(v[0] * s, v[1] * s), pack_bf16(v[2] * s, v[3] * s),
+                    pack_bf16(v[4] * s, v[5] * s), pack_bf16(v[6] * s, v[7] * s));
+}
+
 __global__ void __launch_bounds__(PT, 2)
     fwd_prep_kernel(const FwdParams p, unsigned char *items, const ChunkTable ct,
                     const __grid_constant__ CUtensorMap tm_q,
@@ -227,17 +231,21 @@ __global__ void __launch_bounds__(PT, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   float *sBeta = reinterpret_cast<float *>(smem + P_BETA);
-  float *sDblk = reinterpret_cast<float *>(smem + P_DBLK);
   float *sBsum = reinterpret_cast<float *>(smem + P_BSUM);
   float *sAkk = reinterpret_cast<float *>(smem + P_AKK);
   float *sT = reinterpret_cast<float *>(smem + P_TF);
   float *sScr = reinterpret_cast<float *>(smem + P_SCR);
-  float *sFac = reinterpret_cast<float *>(smem + P_FAC);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + P_ABORT);
   const uint32_t raw_bar = sb + P_BAR, mma_bar = sb + P_BAR + 8, v_bar = sb + P_BAR + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, sub = warp >> 2;  // 2 warps per TMEM lane quadrant
   const int L = 32 * quad + lane;
+  // Channel owner: channel ec of the half, sub-block eb (rows 16 eb ..).  The
+  // two warps on each scheduler get blocks {0, 3} or {1, 2}, which balances
+  // the Y versions they write (block b writes 4 - b of them).
+  const int ec = 32 * (warp & 1) + lane;
+  const int eb = (warp >> 1) ^ ((warp >> 2) & 1);
+  const int er0 = kSub * eb;
   const int H = p.H, T = p.T;
 
   if (warp == 0) tmem_alloc(sb + P_SLOT, 256);
@@ -291,8 +299,7 @@ __global__ void __launch_bounds__(PT, 2)
   // Both issue functions are called by all 32 lanes of one warp: lane 0
   // arms the barrier, then one box per lane.
   auto issue_raw = [&](const Coords &xc, int half) {  // q, k, g of one channel half
-    const int b = xc.b, t0 = xc.t0, h = xc.h;
-    const int y = b * T + t0, x = h * KD + KH * half;
+    const int y = xc.b * T + xc.t0, x = xc.h * KD + KH * half;
     if (lane == 0) mbar_expect_tx(raw_bar, P_RAW_TX);
     __syncwarp();
     if (lane == 0) tma_load_2d(sb + P_RAW_Q, &tm_q, x, y, raw_bar);
@@ -300,14 +307,13 @@ __global__ void __launch_bounds__(PT, 2)
     else if (lane < 4) tma_load_2d(sb + P_RAW_G + 8192 * (lane - 2), &tm_g, x + 32 * (lane - 2), y, raw_bar);
   };
   // v as 16 column groups of 8, each 64 rows x 16 bytes: the MN-major layout
-  // of the V part of RHST (read by the [w | u] MMA).
+  // of V (read by the u product).
   auto issue_v = [&](const Coords &xc) {
-    const int b = xc.b, t0 = xc.t0, h = xc.h;
-    const int y = b * T + t0;
+    const int y = xc.b * T + xc.t0;
     if (lane == 0) mbar_expect_tx(v_bar, P_V_TX);
     __syncwarp();
     if (lane < VD / 8)
-      tma_load_2d(sb + P_RHST + mn_off(KD + 8 * lane, 0, C), &tm_v, h * VD + 8 * lane, y, v_bar);
+      tma_load_2d(sb + P_V + mn_off(8 * lane, 0, C), &tm_v, xc.h * VD + 8 * lane, y, v_bar);
   };
   auto load_beta = [&](const Coords &xc) -> float {
     const int t = xc.t0 + tid;
@@ -334,151 +340,105 @@ __global__ void __launch_bounds__(PT, 2)
     unsigned char *gi = items + (size_t)item * ITEM_BYTES;
     if (tid < C) sBeta[tid] = beta_next;
 
-    // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform).
-    const int rl = tid & 7, cg = (tid >> 3) & 7, b = tid >> 6;
-    const int cc0 = cg * 8;
     for (int half = 0; half < 2; ++half) {
-      const int ch0 = KH * half + cc0;  // first of this thread's channels (global)
+      const int ch = KH * half + ec;  // this thread's channel (of 128)
       // ---- P17: this half's raw tiles
       wait_raw();
-      __syncthreads();
-      if (*sAbort) goto done;
 
-      // ---- P0: gate cumsum, one thread per (channel, 16-row block b); the
-      //      block factors of (b, channel) go to the factor table ----
+      // ---- P0: gate cumsum down this thread's 16 rows (log2 units; rows
+      //      past the chunk's end add nothing), block sums to smem ----
+      float G[kSub];
       {
-        const int c = tid & 63, q4 = tid >> 6;
-        unsigned char *graw = smem + P_RAW_G;
-        float v[16];
+        const unsigned char *gcol = smem + P_RAW_G + 8192 * (ec >> 5) + 4 * (ec & 31);
+        float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = 16 * q4 + i;
-          v[i] = r < n ? *reinterpret_cast<const float *>(graw + g_off(r, c)) : 0.f;
+        for (int i = 0; i < kSub; ++i) {
+          const int r = er0 + i;
+          const float gv = r < n ? *reinterpret_cast<const float *>(gcol + 128 * r) : 0.f;
+          acc = fmaf(gv, kLog2e, acc);
+          G[i] = acc;
         }
-#pragma unroll
-        for (int i = 1; i < 16; ++i) v[i] += v[i - 1];
-        sBsum[q4 * KH + c] = v[15];
-        sDblk[q4 * KD + KH * half + c] = ex2(v[15] * kLog2e);
-        __syncthreads();
-        float off = 0.f;
-        for (int i = 0; i < q4; ++i) off += sBsum[i * KH + c];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          *reinterpret_cast<float *>(graw + g_off(16 * q4 + i, c)) = v[i] + off;
-        float D[kNumSub];
-#pragma unroll
-        for (int i = 0; i < kNumSub; ++i) D[i] = sDblk[i * KD + KH * half + c];
-        float pre = 1.f, suf = 1.f, Db = 1.f;
-#pragma unroll
-        for (int i = 0; i < kNumSub; ++i) {
-          if (i < q4) pre *= D[i];
-          if (i > q4) suf *= D[i];
-          if (i == q4) Db = D[i];
-        }
-        const float x2 = q4 + 2 < kNumSub ? D[min(q4 + 1, kNumSub - 1)] : 1.f;
-        const float x3 = q4 + 3 < kNumSub ? x2 * D[min(q4 + 2, kNumSub - 1)] : 1.f;
-        float *f = sFac + q4 * kFac * KH + c;
-        f[F_PRE * KH] = pre;
-        f[F_SUF * KH] = suf;
-        f[F_RD * KH] = __frcp_rn(Db);
-        f[F_X2 * KH] = x2;
-        f[F_X3 * KH] = x3;
-        f[F_PL * KH] = off * kLog2e;             // G before the block
-        f[F_EL * KH] = (v[15] + off) * kLog2e;   // G at the block's last row
+        sBsum[eb * KH + ec] = acc;
       }
       __syncthreads();
-
-      // ---- P1: operands of this channel half: X, Y_b (smem, for the MMA),
-      //      beta-free K e^G (RHST), Q e^G and K e^{G_C-G} (the item) ----
-      // Thread -> 8 channels of 2 rows of one 16-row block b (warp-uniform).
+      // ---- P1: block offsets and factors of (block eb, channel ch), then
+      //      this half's operands: X, Y_b, (K e^G)^T (smem, for the MMAs),
+      //      Q e^G and (K e^{G_C-G})^T (the item) ----
+      float bs[kNumSub];
 #pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        const int r = kSub * b + 8 * i2 + rl;
-        const bool valid = r < n;
-        const float *fb = sFac + b * kFac * KH + cc0;
-        float xk[8], xq[8], ke[8];  // k e^{G-P_b}, q e^{G-P_b}, k e^{E_b-G}
-        {
-          float kk[8], qq[8], G[8], Pl[8], El[8];
-          ld_bf16x8(smem + P_RAW_K + kq_off(r, cc0), kk);
-          ld_bf16x8(smem + P_RAW_Q + kq_off(r, cc0), qq);
-          ld_f32x8(smem + P_RAW_G, r, cc0, G);
-          ld_f32x8s(fb + F_PL * KH, Pl);
-          ld_f32x8s(fb + F_EL * KH, El);
+      for (int i = 0; i < kNumSub; ++i) bs[i] = sBsum[i * KH + ec];
+      float P2 = 0.f, GC2 = 0.f;  // G before block eb, G at the chunk's end
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float gl = G[j] * kLog2e;
-            const float e1 = ex2(gl - Pl[j]);
-            const float e2 = ex2(El[j] - gl);
-            const float kv = valid ? kk[j] : 0.f;
-            xk[j] = kv * e1;
-            xq[j] = (valid ? qq[j] : 0.f) * e1;
-            ke[j] = kv * e2;
-          }
-        }
-        // out = base * factor (factor row f of the table, or 1), to bf16
-        auto scaled = [&](const float (&base)[8], int f, uint4 &w) {
-          float fv[8];
-          if (f >= 0) ld_f32x8s(fb + f * KH, fv);
-          else {
+      for (int i = 0; i < kNumSub; ++i) {
+        if (i < eb) P2 += bs[i];
+        GC2 += bs[i];
+      }
+      const float E2 = P2 + bs[eb];   // G at block eb's last row
+      const float E3 = eb + 1 < kNumSub ? E2 + bs[min(eb + 1, kNumSub - 1)] : E2;
+      const float E4 = eb + 2 < kNumSub ? E3 + bs[min(eb + 2, kNumSub - 1)] : E3;
+      const float pre = ex2(P2);        // e^{G before the block}
+      const float suf = ex2(GC2 - E2);  // e^{G_C - E_b}
+      const float rD = ex2(P2 - E2);    // 1 / D_b
+      const float x2 = ex2(E3 - E2);    // D_{b+1}
+      const float x3 = ex2(E4 - E2);    // D_{b+1} D_{b+2}
+      if (eb == 0) reinterpret_cast<float *>(gi + I_GAM)[ch] = ex2(GC2);  // e^{G_C}
+      if (half == 1) wait_mma();  // the half-0 MMA has read X and Y
 #pragma unroll
-            for (int j = 0; j < 8; ++j) fv[j] = 1.f;
-          }
-          w.x = pack_bf16(base[0] * fv[0], base[1] * fv[1]);
-          w.y = pack_bf16(base[2] * fv[2], base[3] * fv[3]);
-          w.z = pack_bf16(base[4] * fv[4], base[5] * fv[5]);
-          w.w = pack_bf16(base[6] * fv[6], base[7] * fv[7]);
-        };
-        uint4 w;
-        scaled(xk, -1, w);
-        *reinterpret_cast<uint4 *>(smem + P_X + op_off(r, cc0, KH)) = w;
-        scaled(xq, -1, w);
-        *reinterpret_cast<uint4 *>(smem + P_X + op_off(64 + r, cc0, KH)) = w;
-        scaled(ke, F_RD, w);
-        *reinterpret_cast<uint4 *>(smem + p_y_off(b) + op_off(r, cc0, KH)) = w;
-        if (b + 1 < kNumSub) {
-          scaled(ke, -1, w);
-          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 1) + op_off(r, cc0, KH)) = w;
+      for (int o = 0; o < 2; ++o) {
+        const int r8 = er0 + 8 * o;  // first of the 8 rows of this chunk
+        float xk[8], xq[8], ke[8];
+        const unsigned char *kcol = smem + P_RAW_K + 2 * ec;
+        const unsigned char *qcol = smem + P_RAW_Q + 2 * ec;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = r8 + i;
+          const bool valid = r < n;
+          const float kv = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(kcol + 128 * r)) : 0.f;
+          const float qv = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(qcol + 128 * r)) : 0.f;
+          const float e1 = ex2(G[8 * o + i]);           // e^{G_r - P_b} in (0, 1]
+          const float e2 = ex2(bs[eb] - G[8 * o + i]);  // e^{E_b - G_r} in (0, 1]
+          xk[i] = kv * e1;
+          xq[i] = qv * e1;
+          ke[i] = kv * e2;
         }
-        if (b + 2 < kNumSub) {
-          scaled(ke, F_X2, w);
-          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 2) + op_off(r, cc0, KH)) = w;
-        }
-        if (b + 3 < kNumSub) {
-          scaled(ke, F_X3, w);
-          *reinterpret_cast<uint4 *>(smem + p_y_off(b + 3) + op_off(r, cc0, KH)) = w;
-        }
-        scaled(xk, F_PRE, w);  // K e^G (beta goes into T's columns)
-        *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(ch0, r, C)) = w;
-        scaled(xq, F_PRE, w);  // Q e^G
-        *reinterpret_cast<uint4 *>(gi + I_WQ + op_off(64 + r, ch0, KD)) = w;
-        scaled(ke, F_SUF, w);  // K e^{G_C - G}
-        *reinterpret_cast<uint4 *>(gi + I_KHT + mn_off(ch0, r, C)) = w;
+        *reinterpret_cast<uint4 *>(smem + P_X + mn_off(r8, ec, KH)) = pack8(xk);
+        *reinterpret_cast<uint4 *>(smem + P_X + mn_off(64 + r8, ec, KH)) = pack8(xq);
+        *reinterpret_cast<uint4 *>(smem + p_y_off(eb) + mn_off(r8, ec, KH)) = pack8s(ke, rD);
+        if (eb + 1 < kNumSub)
+          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 1) + mn_off(r8, ec, KH)) = pack8(ke);
+        if (eb + 2 < kNumSub)
+          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 2) + mn_off(r8, ec, KH)) = pack8s(ke, x2);
+        if (eb + 3 < kNumSub)
+          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 3) + mn_off(r8, ec, KH)) = pack8s(ke, x3);
+        // K e^G (beta goes into T's columns), transposed for the w product
+        *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = pack8s(xk, pre);
+        *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8s(xq, pre);
+        *reinterpret_cast<uint4 *>(gi + I_KHT + op_off(ch, r8, C)) = pack8s(ke, suf);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
+      if (*sAbort) goto done;
 
       // ---- P2: this half's share of the A products on the tensor cores;
-      //      the next half's tiles ----
+      //      the next half's tiles (RAW is free once every thread passed) ----
       if (tid == 0) {
         tc_fence_after();
-        mma_group(tmem, sb + P_X, sb + P_Y, KH, 160, half > 0, 0, 0);
+        mma_group(tmem, sb + P_X, sb + P_Y, KH, 160, half > 0, 1, 1);
         mma_commit(mma_bar);
       }
-      if (half == 0 && warp == 1) issue_raw(cur, 1);  // the raw tiles are consumed
       if (half == 0) {
+        if (warp == 1) issue_raw(cur, 1);
         raw_inflight = true;
         raw_pending = raw_phase;
       }
       if (half == 1 && has_next && tid < C) beta_next = load_beta(nxt);
-      // ---- P16: the A products of this half
-      wait_mma();  // X / Y are free again (and, after half 1, A is in TMEM)
     }
-    fence_proxy_async();
+    // ---- P16: the A products of both halves
+    wait_mma();
     __syncthreads();
     if (*sAbort) goto done;
     tc_fence_after();
-
     // ---- P3: beta A_kk (fp32, strict) to smem; A_qk (inclusive) to the item ----
     {
       const int r = L & 63;
@@ -588,7 +548,7 @@ __global__ void __launch_bounds__(PT, 2)
       __syncthreads();
     }
     // ---- P8: T diag(beta) to bf16 (beta folds into T's columns, so the
-    //      right-hand side is [K e^G | V] as loaded); v of this item landed
+    //      right-hand sides are K e^G and V as loaded) ----
     {
       const int rl8 = tid & 7, jc = (tid >> 3) & 3, r = 8 * (tid >> 5) + rl8;
 #pragma unroll
@@ -603,6 +563,7 @@ __global__ void __launch_bounds__(PT, 2)
         st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
       }
     }
+    // v of this item
     v_inflight = true;
     if (!mbar_wait(v_bar, v_phase)) abort_all();
     else v_inflight = false;
@@ -611,7 +572,7 @@ __global__ void __launch_bounds__(PT, 2)
       const int m = C - n;
       for (int i = tid; i < (VD / 8) * m; i += PT) {
         const int grp = i / m, rr = n + i % m;
-        *reinterpret_cast<uint4 *>(smem + P_RHST + mn_off(KD + 8 * grp, rr, C)) =
+        *reinterpret_cast<uint4 *>(smem + P_V + mn_off(8 * grp, rr, C)) =
             make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -620,59 +581,58 @@ __global__ void __launch_bounds__(PT, 2)
     __syncthreads();
     if (*sAbort) goto done;
 
-    // ---- P5: [w | u] = T diag(beta) [K e^G | V] (N = 256) over the A
-    //      products' TMEM columns (read out in P3); rows 64..127 of the A
-    //      operand are ignored ----
+    // ---- P5: w^T = (K e^G)^T (T diag(beta))^T (TMEM columns 0..63, lanes =
+    //      channels) and u = T diag(beta) V (columns 64..191, lanes 0..63 =
+    //      rows; rows 64..127 of its A operand are ignored) ----
     if (tid == 0) {
       tc_fence_after();
-      mma_group(tmem, sb + P_TB, sb + P_RHST, C, KD + VD, false, 0, 1);
+      mma_group(tmem, sb + P_KT, sb + P_TB, C, C, false, 0, 0);
+      mma_group(tmem + C, sb + P_TB, sb + P_V, C, VD, false, 0, 1);
       mma_commit(mma_bar);
     }
-    wait_mma();
-    __syncthreads();
-    if (*sAbort) goto done;
-    tc_fence_after();
-    if (has_next) {  // RAW, the solver buffers and RHST are free: next item's tiles
+    if (has_next) {  // RAW and the solver buffers are free: next item's q, k, g
       if (warp == 0) issue_raw(nxt, 0);
-      if (warp == 1) issue_v(nxt);
-      raw_inflight = v_inflight = true;
+      raw_inflight = true;
       raw_pending = raw_phase;
+    }
+    wait_mma();
+    if (has_next) {  // V has been read: next item's v
+      if (warp == 1) issue_v(nxt);
+      v_inflight = true;
       v_pending = v_phase;
     }
-    // ---- P9: [w | u] out of TMEM into the item
-    if (quad < 2) {  // lanes 0..63: chunk rows; 2 warps share the 16 column pieces
+    tc_fence_after();
+    // ---- P9: w (rows 0..63 of [w ; Q e^G], MN-major) and u out of TMEM
+    {
+      const int r0 = 32 * sub;  // rows r0 .. r0 + 31 of channel L
+      float v0[16], v1[16];
+      tmem_ld16x2(tq + r0, tq + r0 + 16, v0, v1);
+#pragma unroll
+      for (int o = 0; o < 4; ++o) {
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = (o < 2 ? v0 : v1)[8 * (o & 1) + i];
+        st_g16(gi, I_WQ + mn_off(r0 + 8 * o, L, KD), a);
+      }
+    }
+    if (quad < 2) {  // lanes 0..63: chunk rows; 2 warps share the 8 u pieces
       const int r = L;
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
+      for (int k2 = 0; k2 < 2; ++k2) {
         const int p0 = sub + 4 * k2, p1 = p0 + 2;  // pieces of 16 columns
         float v0[16], v1[16];
-        tmem_ld16x2(tq + 16 * p0, tq + 16 * p1, v0, v1);
+        tmem_ld16x2(tq + C + 16 * p0, tq + C + 16 * p1, v0, v1);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int pc = e ? p1 : p0;
+          const int col = 16 * (e ? p1 : p0), vt = col >> 5, cv = col & 31;
           const float *vv = e ? v1 : v0;
-          if (pc < 8) {  // w columns 16 pc .. 16 pc + 15
-            float a[8], c8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { a[i] = vv[i]; c8[i] = vv[8 + i]; }
-            st_g16(gi, I_WQ + op_off(r, 16 * pc, KD), a);
-            st_g16(gi, I_WQ + op_off(r, 16 * pc + 8, KD), c8);
-          } else {  // u columns 16 (pc - 8) .., bf16
-            const int col = 16 * (pc - 8), vt = col >> 5, cv = col & 31;
-            uint4 *dst = reinterpret_cast<uint4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 2);
-            dst[0] = make_uint4(pack_bf16(vv[0], vv[1]), pack_bf16(vv[2], vv[3]),
-                                pack_bf16(vv[4], vv[5]), pack_bf16(vv[6], vv[7]));
-            dst[1] = make_uint4(pack_bf16(vv[8], vv[9]), pack_bf16(vv[10], vv[11]),
-                                pack_bf16(vv[12], vv[13]), pack_bf16(vv[14], vv[15]));
-          }
+          uint4 *dst = reinterpret_cast<uint4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 2);
+          dst[0] = make_uint4(pack_bf16(vv[0], vv[1]), pack_bf16(vv[2], vv[3]),
+                              pack_bf16(vv[4], vv[5]), pack_bf16(vv[6], vv[7]));
+          dst[1] = make_uint4(pack_bf16(vv[8], vv[9]), pack_bf16(vv[10], vv[11]),
+                              pack_bf16(vv[12], vv[13]), pack_bf16(vv[14], vv[15]));
         }
       }
-    } else {
-      const int c = 64 * sub + (tid & 63);  // warps 2, 3, 6, 7: e^{G_C} per key channel
-      float gam = 1.f;
-#pragma unroll
-      for (int i = 0; i < kNumSub; ++i) gam *= sDblk[i * KD + c];
-      reinterpret_cast<float *>(gi + I_GAM)[c] = gam;
     }
     tc_fence_before();
     __syncthreads();
@@ -692,11 +652,13 @@ done:
 }
 
 // ---- recurrence kernel --------------------------------------------------------
-// One CTA per (run, head, VTR-column value tile), 256 threads: two warps per
-// TMEM lane quadrant, each owning VTR / 2 of the tile's value columns (warp
-// w: quadrant w % 4, columns (VTR / 2) (w / 4) ..).  VTR is 32 or 64; the
-// wider tile halves the item bytes the CTAs pull from L2 per chunk.
-constexpr int RT = 256;
+// One CTA per (run, head, VTR-column value tile), WPQ warps per TMEM lane
+// quadrant, each owning VTR / WPQ of the tile's value columns (warp w:
+// quadrant w % 4, columns (VTR / WPQ) (w / 4) ..).  VTR is 32, 64 or 128;
+// a wider tile pulls each item from L2 fewer times and does more work per
+// MMA instruction at the same MMA latency (an M = 128, K = 16 step takes
+// about as long for N = 32 as for N = 128), so VTR = 128 (one CTA per run
+// and head, 16 warps) reads every item exactly once.
 // One stage mirrors the item's start: [w ; Q e^G] | A_qk | (K e^{G_C-G})^T
 // (one copy), then this unit's u columns (VTR / 32 tiles of 64 x 32 bf16)
 // and e^{G_C}.  A_qk is read as the 128-row A operand starting 64 rows
@@ -707,44 +669,67 @@ static_assert(S_WQ == 0 && S_AQK == 32768 && S_KHT == S_AQK + 8192 && S_U == S_K
               "stage layout");
 template <int VTR, int NST>
 struct RecLayout {
-  static constexpr int NT = VTR / VT;                            // u tiles per unit
+  static constexpr int WPQ = VTR == 128 ? 4 : 2;                // warps per lane quadrant
+  static constexpr int THREADS = 128 * WPQ;
+  static constexpr int CPT = VTR / WPQ;                         // value columns per thread
+  static constexpr int NT = VTR / VT;                           // u tiles per unit
   static constexpr uint32_t S_GAM = S_U + 4096u * NT;
   static constexpr uint32_t S_BYTES = S_GAM + 512;               // copied per stage
   static constexpr uint32_t STAGE = (S_BYTES + 1023) / 1024 * 1024;
   static constexpr uint32_t ST = NST * STAGE;                   // S^T MN-major VTR x Kd 128
   static constexpr uint32_t UT = ST + 256u * VTR;               // U^T MN-major VTR x Kd 64
-  static constexpr uint32_t BAR = UT + 128u * VTR;              // stages, mma
-  static constexpr uint32_t SLOT = BAR + 8 * (NST + 1);
+  static constexpr uint32_t BAR = UT + 128u * VTR;              // stages, d1, s, o
+  static constexpr uint32_t SLOT = BAR + 8 * (NST + 3);
   static constexpr uint32_t ABORT = SLOT + 4;
   static constexpr uint32_t ALLOC = ABORT + 12 + 1024;
   // TMEM: D1 double-buffered (chunk parity) so the o rows of chunk n are read
   // while the first MMA of chunk n + 1 runs; D2 single.
   static constexpr uint32_t TM_D1 = 0, TM_D2 = 2 * VTR;
-  static constexpr uint32_t TM_COLS = 3 * VTR <= 128 ? 128 : 256;
+  static constexpr uint32_t TM_COLS = 3 * VTR <= 128 ? 128 : (3 * VTR <= 256 ? 256 : 512);
+  static_assert(CPT == 16 || CPT == 32, "columns per thread");
   static_assert(ALLOC <= 232448, "rec smem fits");
 };
 
+// Per chunk, three MMA groups, each committed to its own mbarrier:
+//   D1  = [w ; Q e^G] S          (d1 barrier; U = u - D1[0:64] follows)
+//   D2  = (K e^{G_C-G})^T U       (s barrier; the state update follows)
+//   D1 += [* ; A_qk] U            (o barrier; only the o rows wait for it)
+// D2 is issued before the o product, so the state update, and with it the
+// next chunk's first MMA, waits only for the products on the serial chain;
+// the o product runs on the tensor pipe while the CUDA cores update S.
 template <int VTR, int NST>
-__global__ void __launch_bounds__(RT, 1)
+__global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
   using Lay = RecLayout<VTR, NST>;
-  constexpr int CPT = VTR / 2;  // value columns per thread
+  constexpr int CPT = Lay::CPT;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + Lay::ABORT);
-  const uint32_t bar0 = sb + Lay::BAR, mma_bar = sb + Lay::BAR + 8 * NST;
+  const uint32_t bar0 = sb + Lay::BAR;
+  const uint32_t d1_bar = bar0 + 8 * NST, s_bar = d1_bar + 8, o_bar = d1_bar + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, half = warp >> 2;
+  const int quad = warp & 3, grp = warp >> 2;
   const int L = 32 * quad + lane;   // TMEM lane: chunk row (0..63) / o row / key row
-  const int col0 = CPT * half;      // this thread's value columns within the tile
+  const int col0 = CPT * grp;       // this thread's value columns within the tile
   const int H = p.H, T = p.T;
+  // The thread that issues the stage refills: lane 0 of the first warp of
+  // quadrant 2, which waits for the o product (the last reader of a stage).
+  constexpr int kRefillTid = 64;
+#ifndef KDA_REC_PREFETCH
+#define KDA_REC_PREFETCH 2
+#endif
+  // Items are also pulled into L2 this many chunks ahead of their stage
+  // copy, so the copies hit L2 instead of waiting on DRAM.
+  constexpr int kRecPrefetch = KDA_REC_PREFETCH;
 
   if (warp == 0) tmem_alloc(sb + Lay::SLOT, Lay::TM_COLS);
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) mbar_init(bar0 + 8u * i, 1);
-    mbar_init(mma_bar, 1);
+    mbar_init(d1_bar, 1);
+    mbar_init(s_bar, 1);
+    mbar_init(o_bar, 1);
     *sAbort = 0u;
     fence_mbar_init();
   }
@@ -753,10 +738,15 @@ __global__ void __launch_bounds__(RT, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + Lay::SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
-  uint32_t st_phase[NST] = {}, mma_phase = 0;
+  uint32_t st_phase[NST] = {};
   uint32_t st_issued = 0;  // per-stage bit: copy issued and not yet waited
-  bool mma_inflight = false;
-  uint32_t mma_pending = 0;
+  // Completions of each MMA barrier this thread has waited for (the k-th
+  // completion has parity k & 1), and, for the issuing thread 0, the
+  // barrier and completion index of its last commit (drained on abort).
+  uint32_t n_d1 = 0, n_s = 0, n_o = 0;
+  uint32_t c_d1 = 0, c_s = 0, c_o = 0;  // commits issued (thread 0)
+  uint32_t last_bar = 0, last_k = 0;
+  bool committed = false;
   auto abort_all = [&]() {
     *sAbort = 1u;
     set_status(p.status, KDA_DEVICE_TIMEOUT);
@@ -774,12 +764,15 @@ __global__ void __launch_bounds__(RT, 1)
     else st_issued &= ~(1u << s);
     st_phase[s] ^= 1u;
   };
-  auto wait_mma = [&]() {
-    mma_inflight = true;
-    mma_pending = mma_phase;
-    if (!mbar_wait(mma_bar, mma_phase)) abort_all();
-    else mma_inflight = false;
-    mma_phase ^= 1u;
+  auto wait_bar = [&](uint32_t bar, uint32_t &n) {
+    if (!mbar_wait(bar, n & 1u)) abort_all();
+    ++n;
+  };
+  auto commit = [&](uint32_t bar, uint32_t &c) {  // thread 0
+    mma_commit(bar);
+    last_bar = bar;
+    last_k = c++;
+    committed = true;
   };
   // CPT consecutive fp32 TMEM columns of this thread's lane.
   auto tmem_ld_cpt = [&](uint32_t taddr, float (&v)[CPT]) {
@@ -830,8 +823,10 @@ __global__ void __launch_bounds__(RT, 1)
       for (int i = 0; i < CPT; ++i) S[i] = 0.f;
     }
     store_st(S, L);
-    if (tid == 0)
+    if (tid == 0) {
       for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt);
+      for (int c = NST; c < NST + kRecPrefetch && c < n_chunks; ++c) prefetch_l2(item_ptr(c), ITEM_BYTES);
+    }
     st_issued = (1u << (NST < n_chunks ? NST : n_chunks)) - 1u;
     fence_proxy_async();
     wait_stage(0);
@@ -841,8 +836,8 @@ __global__ void __launch_bounds__(RT, 1)
     // ---- P11: D1[0] = [w ; Q e^G] S for chunk 0
     if (tid == 0) {
       tc_fence_after();
-      mma_group(tmem + Lay::TM_D1, sb + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
-      mma_commit(mma_bar);
+      mma_group(tmem + Lay::TM_D1, sb + S_WQ, sb + Lay::ST, KD, VTR, false, 1, 1);
+      commit(d1_bar, c_d1);
     }
 
     int s = 0;  // stage of chunk c
@@ -857,7 +852,7 @@ __global__ void __launch_bounds__(RT, 1)
       // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk (every thread
       //      waits on the barrier itself; an abort is seen after the next
       //      block barrier, which also keeps the phases in step)
-      wait_mma();
+      wait_bar(d1_bar, n_d1);
       tc_fence_after();
 
       // ---- P12: U = u - w S (lanes 0..63)
@@ -880,14 +875,15 @@ __global__ void __launch_bounds__(RT, 1)
       __syncthreads();
       if (*sAbort) goto done;
 
-      // ---- P13: D1 += [* ; A_qk] U ;  D2 = (K e^{G_C-G})^T U
+      // ---- P13: D2 = (K e^{G_C-G})^T U (the chain), then D1 += [* ; A_qk] U
       if (tid == 0) {
         tc_fence_after();
+        mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 0, 1);
+        commit(s_bar, c_s);
         mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
-        mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 1, 1);
-        mma_commit(mma_bar);
+        commit(o_bar, c_o);
       }
-      wait_mma();
+      wait_bar(s_bar, n_s);
       tc_fence_after();
 
       // ---- P14: state update (all lanes = key rows), next chunk's first MMA
@@ -899,25 +895,37 @@ __global__ void __launch_bounds__(RT, 1)
         for (int i = 0; i < CPT; ++i) S[i] = fmaf(gam, S[i], v[i]);
         store_st(S, L);
       }
+      // Refill stage s as early as possible: when the o product (its last
+      // reader) is already done, now; else after the o rows wait for it.
+      bool refilled = false;
+      if (tid == kRefillTid && c + NST < n_chunks && mbar_try_wait(o_bar, n_o & 1u)) {
+        tc_fence_after();
+        issue_stage(s, item_ptr(c + NST), vt);
+        if (c + NST + kRecPrefetch < n_chunks) prefetch_l2(item_ptr(c + NST + kRecPrefetch), ITEM_BYTES);
+        refilled = true;
+      }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
       if (*sAbort) goto done;
-      if (c + NST < n_chunks) {  // stage s is free: its MMAs and reads are done
-        if (tid == 32) issue_stage(s, item_ptr(c + NST), vt);  // beside the MMA issue
-        st_issued |= 1u << s;
-      }
       if (c + 1 < n_chunks) {
         wait_stage(s1);
         if (tid == 0) {
           tc_fence_after();
           mma_group(tmem + Lay::TM_D1 + (uint32_t)VTR * (uint32_t)((c + 1) & 1),
-                    sb + (uint32_t)s1 * Lay::STAGE + S_WQ, sb + Lay::ST, KD, VTR, false, 0, 1);
-          mma_commit(mma_bar);
+                    sb + (uint32_t)s1 * Lay::STAGE + S_WQ, sb + Lay::ST, KD, VTR, false, 1, 1);
+          commit(d1_bar, c_d1);
         }
       }
-      // o rows of this chunk (lanes 64..127) while the next MMA runs
+      // o rows of this chunk (lanes 64..127) while the next MMA runs; the o
+      // product is the last reader of stage s, so the refill follows it
       if (quad >= 2) {
+        wait_bar(o_bar, n_o);
+        tc_fence_after();
+        if (tid == kRefillTid && !refilled && c + NST < n_chunks) {
+          issue_stage(s, item_ptr(c + NST), vt);
+          if (c + NST + kRecPrefetch < n_chunks) prefetch_l2(item_ptr(c + NST + kRecPrefetch), ITEM_BYTES);
+        }
         const int r = L - 64;
         float v[CPT];
         tmem_ld_cpt(tq + d1 + col0, v);
@@ -935,6 +943,7 @@ __global__ void __launch_bounds__(RT, 1)
           }
         }
       }
+      if (c + NST < n_chunks) st_issued |= 1u << s;
       tc_fence_before();
       s = s1;
     }
@@ -949,9 +958,11 @@ __global__ void __launch_bounds__(RT, 1)
   }
 
 done:
+  // Drain this thread's copies and (thread 0) its last MMA commit, each
+  // wait bounded, before TMEM is freed.
   for (int s = 0; s < NST; ++s)
     if (st_issued & (1u << s)) mbar_wait(bar0 + 8u * s, st_phase[s]);
-  if (mma_inflight) mbar_wait(mma_bar, mma_pending);
+  if (tid == 0 && committed) mbar_wait(last_bar, last_k & 1u);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -1008,7 +1019,8 @@ size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per
 }
 
 bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
-  return bf16 && K == KD && V == VD && (v_tile == 0 || v_tile == 32 || v_tile == 64);
+  return bf16 && K == KD && V == VD &&
+         (v_tile == 0 || v_tile == 32 || v_tile == 64 || v_tile == 128);
 }
 
 // Two stages in flight: a third only lengthens the copies' latency (more
@@ -1027,7 +1039,7 @@ cudaError_t launch_rec(const FwdParams &p, const unsigned char *items, const Chu
   const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
                                : (long)p.B * p.H * p.n_vtiles;
   const int g2 = (int)(n_units < sms ? n_units : sms);
-  fwd_rec_kernel<VTR, NST><<<g2 > 0 ? g2 : 1, RT, Lay::ALLOC, stream>>>(p, items, ct);
+  fwd_rec_kernel<VTR, NST><<<g2 > 0 ? g2 : 1, Lay::THREADS, Lay::ALLOC, stream>>>(p, items, ct);
   return cudaGetLastError();
 }
 }  // namespace
@@ -1067,7 +1079,9 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   }
   const uint64_t rows = (uint64_t)p.B * p.T;
   CUtensorMap mq, mk, mg, mv;
-  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  // q, k, g unswizzled: the prep kernel's channel owners read one row's 32
+  // consecutive channels per warp (128 contiguous bytes of g, 64 of q or k)
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
   if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
       !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
       !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, 32, sw) ||
@@ -1086,8 +1100,9 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = p.v_tile == 32 ? launch_rec<32, kRecStages>(p, items, ct, has_seg, stream)
-                     : launch_rec<64, kRecStages>(p, items, ct, has_seg, stream);
+  e = p.v_tile == 32   ? launch_rec<32, kRecStages>(p, items, ct, has_seg, stream)
+      : p.v_tile == 64 ? launch_rec<64, kRecStages>(p, items, ct, has_seg, stream)
+                       : launch_rec<128, kRecStages>(p, items, ct, has_seg, stream);
   if (e != cudaSuccess || !with_fallback || !has_seg) return e;
   // The fused kernel covers calls whose runs overflow the items (it exits
   // at once when they fit).

@@ -144,6 +144,10 @@ cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
 
 int num_sms();
 
+// Shape validation shared by the forward entry points (KDA_OK, or the code
+// kda_chunk_fwd returns for that shape).
+kda_status check_shape(const kda_shape *s);
+
 // ---- device helpers -------------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) {

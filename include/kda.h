@@ -102,12 +102,17 @@ typedef enum kda_impl {
                                       workspace was sized for (split path) */
 
 /*
- * Bytes of workspace kda_chunk_fwd needs for this shape.  The workspace
- * holds the device status word and, when segment ids are given, the run
- * list (one 8-byte record per run, at most B*T runs) and per-row counts.
- * The workspace must be zero-filled once before its first use (for
- * instance allocated with cudaMemset 0); libkda leaves it reusable.
- * Returns 0 when `s` is NULL or invalid.
+ * Bytes of workspace that let kda_chunk_fwd run its fastest kernel on this
+ * shape (the same as kda_chunk_fwd_workspace_size_for(s, has_segment_ids,
+ * KDA_IMPL_AUTO)).  The workspace holds the device status word, when
+ * segment ids are given the run list (one 8-byte record per run, at most
+ * B*T runs) and per-row counts, and for the tensor-core split path the
+ * per-chunk operands.  Any smaller workspace of at least
+ * kda_chunk_fwd_workspace_size_for(s, has_segment_ids, KDA_IMPL_SIMT) bytes
+ * is accepted too; AUTO then picks a kernel that fits it, which can be
+ * several times slower.  The workspace must be zero-filled once before its
+ * first use (for instance allocated with cudaMemset 0); libkda leaves it
+ * reusable.  Returns 0 when `s` is NULL or invalid.
  */
 KDA_API size_t kda_chunk_fwd_workspace_size(const kda_shape *s, int has_segment_ids);
 
@@ -159,9 +164,11 @@ KDA_API size_t kda_chunk_fwd_workspace_size_packed(const kda_shape *s,
  *   final_state   device float32 [B,H,K,V] or NULL (not requested): the state
  *                 after each row's last non-padding token (initial_state or
  *                 zeros for an all-padding row).
- *   workspace     device, >= kda_chunk_fwd_workspace_size(s, segment_ids
- *                 != NULL) bytes, 256-byte aligned, zero-filled before first
- *                 use.
+ *   workspace     device, 256-byte aligned, zero-filled before first use;
+ *                 kda_chunk_fwd_workspace_size(s, segment_ids != NULL) bytes
+ *                 for the fastest kernel, at least the KDA_IMPL_SIMT size of
+ *                 kda_chunk_fwd_workspace_size_for (KDA_ERR_WORKSPACE when
+ *                 smaller).
  * Returns KDA_OK or an error code; on error nothing has been enqueued.
  */
 KDA_API kda_status kda_chunk_fwd(const kda_shape *s, const void *q, const void *k,
@@ -197,17 +204,22 @@ KDA_API kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const voi
  * lives in a fixed device array of KDA_NOALLOC_SCRATCH_BYTES bytes that the
  * library defines; every GPU that loads the library keeps that memory until
  * the process exits.  The call itself allocates nothing.
- *   - Shapes whose scratch need, kda_chunk_fwd_workspace_size(s,
- *     segment_ids != NULL), exceeds KDA_NOALLOC_SCRATCH_BYTES are rejected
- *     with KDA_ERR_WORKSPACE (with segment ids about B*T > 130000 tokens).
+ *   - Argument errors are the codes kda_chunk_fwd returns for the same
+ *     input.  Shapes whose smallest workspace,
+ *     kda_chunk_fwd_workspace_size_for(s, segment_ids != NULL,
+ *     KDA_IMPL_SIMT), exceeds KDA_NOALLOC_SCRATCH_BYTES are rejected with
+ *     KDA_ERR_WORKSPACE (with segment ids about B*T > 130000 tokens).  The
+ *     kernel is the one AUTO picks for a workspace of that many bytes.
  *   - All calls share the array: calls whose work overlaps on the GPU race
  *     and give wrong results.  Order them on one stream.
- *   - The first call on each device looks up the array's address with that
- *     device current and keeps it; make that first call before any stream
- *     capture begins.
+ *   - The array's address is looked up on the first call in each CUDA
+ *     context of a device, with that device current, and kept for that
+ *     context; after a device reset the next call looks it up again.  Make
+ *     the first call on a device before any stream capture begins.
  *   - Each call clears the array's header on `stream` before its kernels,
- *     so the previous call's counters never carry over.  Device status
- *     bits are not reported by this entry point.
+ *     so the previous call's counters never carry over; the device status
+ *     bits of the last call stay there until the next call, and
+ *     kda_chunk_fwd_noalloc_status reads them.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (1u << 20)
 KDA_API kda_status kda_chunk_fwd_noalloc(
@@ -215,6 +227,15 @@ KDA_API kda_status kda_chunk_fwd_noalloc(
     const float *g, const float *beta, float scale, int chunk_size,
     const float *initial_state, const int32_t *segment_ids, void *o,
     float *final_state, kda_stream_t stream);
+
+/*
+ * Device status of the last kda_chunk_fwd_noalloc call on the current
+ * device (no counterpart on the pages): waits for `stream`, then reads the
+ * status word of the fixed scratch array into *device_bits, with the
+ * return codes of kda_read_device_status.  KDA_ERR_INVALID_ARG for a NULL
+ * device_bits.
+ */
+KDA_API kda_status kda_chunk_fwd_noalloc_status(kda_stream_t stream, uint32_t *device_bits);
 
 /*
  * 1 when `impl` can run shape `s` (KDA_IMPL_AUTO: always, for a valid

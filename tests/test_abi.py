@@ -61,11 +61,32 @@ def test_version_and_status_strings(L):
 
 
 def test_workspace_size_formula(L):
-    assert kda.workspace_size(1, 8192, 32, 128, 128) == 256
-    # header + row offsets (B+1 ints rounded to 256 B) + 8 B per possible run
-    assert kda.workspace_size(2, 1000, 4, 64, 64, has_segment_ids=True) == 256 + 256 + 8 * 2000
+    # the smallest workspace: the header, plus with segment ids the row
+    # offsets (B+1 ints rounded to 256 B) and 8 B per possible run
+    assert kda.workspace_size(1, 8192, 32, 128, 128, impl="simt") == 256
+    assert kda.workspace_size(2, 1000, 4, 64, 64, has_segment_ids=True, impl="simt") == \
+        256 + 256 + 8 * 2000
     s = kda.kda_shape(1, 16, 1, 48, 128, 1)   # unsupported K
     assert L.kda_chunk_fwd_workspace_size(ctypes.byref(s), 0) == 0
+
+
+@pytest.mark.parametrize("shape,seg", [((1, 8192, 32, 128, 128), False),
+                                       ((1, 8192, 32, 128, 128), True),
+                                       ((2, 1000, 4, 64, 64), True),
+                                       ((1, 128, 2, 128, 128), False)])
+def test_default_workspace_size_is_the_fast_path_size(L, shape, seg):
+    # The default query returns what AUTO needs for its fastest kernel: for
+    # bf16 K = V = 128 the split path's size, so a caller that follows the
+    # basic recipe (query, allocate, call) gets the split kernels.
+    B, T, H, K, V = shape
+    d = kda.workspace_size(B, T, H, K, V, has_segment_ids=seg)
+    assert d == kda.workspace_size(B, T, H, K, V, has_segment_ids=seg, impl="auto")
+    split = kda.workspace_size(B, T, H, K, V, has_segment_ids=seg, impl="split")
+    if K == V == 128:
+        assert d == split > kda.workspace_size(B, T, H, K, V, has_segment_ids=seg, impl="simt")
+    else:
+        assert split == 0
+        assert d == kda.workspace_size(B, T, H, K, V, has_segment_ids=seg, impl="simt")
 
 
 FAKE = 0x10000  # a 256-byte aligned address; never dereferenced
@@ -101,6 +122,38 @@ def test_forward_rejects_bad_arguments_without_launching(L, kw, expect):
     assert call_fwd(L, **kw) == expect
 
 
+def call_noalloc(L, shape=(1, 128, 2, 128, 128, 1), q=FAKE, k=FAKE, v=FAKE, g=FAKE,
+                 beta=FAKE, chunk=64, s0=None, seg=None, o=FAKE, fs=None, scale=0.1):
+    s = kda.kda_shape(*shape)
+    vp = ctypes.c_void_p
+    return L.kda_chunk_fwd_noalloc(ctypes.byref(s), vp(q), vp(k), vp(v), vp(g), vp(beta),
+                                   scale, chunk, vp(s0), vp(seg), vp(o), vp(fs), None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(beta=None), 1),
+    (dict(shape=(0, 128, 2, 128, 128, 1)), 1),
+    (dict(shape=(1, 0, 2, 128, 128, 1)), 1),
+    (dict(shape=(1, 128, 2, 128, 128, 7)), 1),
+    (dict(shape=(1, 128, 2, 96, 128, 1)), 2),
+    (dict(chunk=32), 2),
+    (dict(q=FAKE + 2), 3), (dict(g=FAKE + 4), 3), (dict(s0=FAKE + 8), 3),
+    (dict(scale=float("nan")), 1),
+    # the run list of 200000 tokens does not fit the fixed array
+    (dict(shape=(1, 200000, 1, 32, 32, 1), seg=FAKE), 4),
+])
+def test_noalloc_rejects_bad_arguments_like_the_workspace_entry_point(L, kw, expect):
+    assert call_noalloc(L, **kw) == expect
+    if "shape" not in kw or kw["shape"][1] != 200000:
+        # kda_chunk_fwd returns the same code for the same input
+        kw2 = {k: v for k, v in kw.items()}
+        assert call_fwd(L, **kw2) == expect
+
+
+def test_noalloc_status_rejects_null(L):
+    assert L.kda_chunk_fwd_noalloc_status(None, None) == 1
+
+
 def test_conv_rejects_bad_arguments(L):
     s = kda.kda_shape(1, 64, 2, 128, 128, 1)
     vp = ctypes.c_void_p
@@ -120,7 +173,7 @@ def test_impl_available_query(L):
 
 
 def test_workspace_size_for_each_impl(L):
-    base = kda.workspace_size(1, 8192, 32, 128, 128)
+    base = kda.workspace_size(1, 8192, 32, 128, 128, impl="simt")
     split = kda.workspace_size(1, 8192, 32, 128, 128, impl="split")
     assert split == 1024 + 128 * 32 * 74240          # one 72.5 KiB item per chunk-head
     assert kda.workspace_size(1, 8192, 32, 128, 128, impl="auto") == split
@@ -134,7 +187,7 @@ def test_workspace_size_for_each_impl(L):
     assert kda.workspace_size_packed(1, 100, 2, 64, 64, 3) == 0
     assert kda.workspace_size(1, 100, 2, 64, 64, impl="split") == 0
     assert kda.workspace_size(1, 100, 2, 128, 128, torch.float32, impl="auto") == \
-        kda.workspace_size(1, 100, 2, 128, 128, torch.float32)
+        kda.workspace_size(1, 100, 2, 128, 128, torch.float32, impl="simt")
 
 
 def test_split_rejects_small_workspace(L):

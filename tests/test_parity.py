@@ -190,7 +190,7 @@ def test_misaligned_pointer_rejected_on_gpu():
     assert e.value.status == 3
 
 
-@pytest.mark.parametrize("v_tile", [32, 64])
+@pytest.mark.parametrize("v_tile", [32, 64, 128])
 @pytest.mark.parametrize("name", ["fixed_bf16_h8_t1024", "packed_bf16_h8_t1024_4seg"])
 def test_split_value_tiles(name, v_tile):
     """The split path's recurrence with either value-tile width (32 or 64
