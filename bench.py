@@ -161,9 +161,28 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def head_partition(h_total: int, world: int, rank: int):
+    """Heads [h0, h1) that rank ``rank`` of ``world`` owns in a problem of
+    ``h_total`` heads: equal contiguous blocks.  Heads are independent in the
+    recurrence, so a rank computes its block with no data exchange."""
+    if world < 1 or not 0 <= rank < world or h_total % world:
+        raise ValueError(f"cannot split {h_total} heads over {world} ranks")
+    per = h_total // world
+    return rank * per, (rank + 1) * per
+
+
+def head_block_seed(seed: int, h0: int, heads_per_rank: int) -> int:
+    """Seed of the input block of heads [h0, h0 + heads_per_rank): the inputs
+    of the multi-rank problem are drawn block by block, so every rank makes
+    only its own block and the blocks differ."""
+    return seed + h0 // heads_per_rank
+
+
 def whole_job_value(world: int, tokens_per_rank: int, ms_max: float) -> float:
-    """tokens/s of the whole job: each rank processes its own replica, and the
-    job takes as long as its slowest rank."""
+    """Whole-job throughput in tokens/s of an H-head layer (H the heads one
+    rank owns): the problem has world x H heads, every rank runs the forward
+    of its H heads over all tokens, and the job takes as long as its slowest
+    rank; equivalently the sum over ranks of each rank's tokens/s."""
     return world * tokens_per_rank / (ms_max * 1e-3)
 
 
@@ -296,9 +315,13 @@ def run_ours(args, dist):
     clocks = ClockSampler(dist.local_rank)
     hbm_peak, tc_peak, peak_src = measured_peaks()
 
+    def rank_seed(w):
+        h0, _ = head_partition(w.H * dist.world, dist.world, dist.rank)
+        return head_block_seed(args.seed, h0, w.H)
+
     def measure(wname, with_e2e, clocks_=None):
         w = ki.WORKLOADS[wname]
-        x = ki.make_inputs(w, seed=args.seed + dist.rank)
+        x = ki.make_inputs(w, seed=rank_seed(w))
         d = device_inputs(x, dev)
         has_seg = d["segment_ids"] is not None
         o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
@@ -389,7 +412,7 @@ def run_ours(args, dist):
         """The short-conv prologue (conv + SiLU + L2 on q, k) alone and followed
         by the forward, on the packed shape with pre-conv inputs."""
         w = ki.WORKLOADS[wname]
-        x = ki.make_inputs(w, seed=args.seed + dist.rank)
+        x = ki.make_inputs(w, seed=rank_seed(w))
         d = device_inputs(x, dev)
         cw = x["conv_w"].to(dev)
         o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
@@ -432,8 +455,8 @@ def run_ours(args, dist):
         of sum(d_o * o) + sum(d_final * final_state) for seeded upstream
         gradients, workspace allocated once."""
         w = ki.WORKLOADS[wname]
-        x = ki.make_inputs(w, seed=args.seed + dist.rank)
-        u = ki.make_upstream_grads(w, seed=args.seed + dist.rank)
+        x = ki.make_inputs(w, seed=rank_seed(w))
+        u = ki.make_upstream_grads(w, seed=rank_seed(w))
         d = device_inputs(x, dev)
         d_o, d_f = u["d_o"].to(dev), u["d_final"].to(dev)
         has_seg = d["segment_ids"] is not None
@@ -515,6 +538,9 @@ def run_ours(args, dist):
                    "qkv_dtype": w.dtype, "chunk": CHUNK, "initial_state": w.init_state_std is not None,
                    "output_final_state": True, "impl": impl_used,
                    "l2": "flushed: 256 MiB write between timed steps",
+                   "parallelism": (f"heads sharded: {w.H * dist.world} heads, {w.H} per rank "
+                                   f"on {dist.world} ranks, no data exchange"
+                                   if dist.world > 1 else "one GPU"),
                    "ms_median": head["ms_median"], "ms_min": head["ms_min"]},
         "roofline": roofline(head),
         "e2e": head.get("e2e"),

@@ -246,6 +246,10 @@ __global__ void __launch_bounds__(PT, 2)
   const int ec = 32 * (warp & 1) + lane;
   const int eb = (warp >> 1) ^ ((warp >> 2) & 1);
   const int er0 = kSub * eb;
+  // The MMAs are issued by a thread of warp 4 (block 3, the lightest share
+  // of the elementwise work): issuing holds a thread for about the MMA's
+  // execution time.
+  constexpr int kIssuer = 128;
   const int H = p.H, T = p.T;
 
   if (warp == 0) tmem_alloc(sb + P_SLOT, 256);
@@ -298,6 +302,8 @@ __global__ void __launch_bounds__(PT, 2)
   };
   // Both issue functions are called by all 32 lanes of one warp: lane 0
   // arms the barrier, then one box per lane.
+  // Half 0's request also pulls half 1's boxes into L2, so their copy,
+  // issued once half 0's tiles are consumed, does not wait on DRAM.
   auto issue_raw = [&](const Coords &xc, int half) {  // q, k, g of one channel half
     const int y = xc.b * T + xc.t0, x = xc.h * KD + KH * half;
     if (lane == 0) mbar_expect_tx(raw_bar, P_RAW_TX);
@@ -305,6 +311,9 @@ __global__ void __launch_bounds__(PT, 2)
     if (lane == 0) tma_load_2d(sb + P_RAW_Q, &tm_q, x, y, raw_bar);
     else if (lane == 1) tma_load_2d(sb + P_RAW_K, &tm_k, x, y, raw_bar);
     else if (lane < 4) tma_load_2d(sb + P_RAW_G + 8192 * (lane - 2), &tm_g, x + 32 * (lane - 2), y, raw_bar);
+    else if (half == 0 && lane == 4) tma_prefetch_2d(&tm_q, x + KH, y);
+    else if (half == 0 && lane == 5) tma_prefetch_2d(&tm_k, x + KH, y);
+    else if (half == 0 && lane < 8) tma_prefetch_2d(&tm_g, x + KH + 32 * (lane - 6), y);
   };
   // v as 16 column groups of 8, each 64 rows x 16 bytes: the MN-major layout
   // of V (read by the u product).
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(PT, 2)
 
       // ---- P2: this half's share of the A products on the tensor cores;
       //      the next half's tiles (RAW is free once every thread passed) ----
-      if (tid == 0) {
+      if (tid == kIssuer) {
         tc_fence_after();
         mma_group(tmem, sb + P_X, sb + P_Y, KH, 160, half > 0, 1, 1);
         mma_commit(mma_bar);
@@ -584,7 +593,7 @@ __global__ void __launch_bounds__(PT, 2)
     // ---- P5: w^T = (K e^G)^T (T diag(beta))^T (TMEM columns 0..63, lanes =
     //      channels) and u = T diag(beta) V (columns 64..191, lanes 0..63 =
     //      rows; rows 64..127 of its A operand are ignored) ----
-    if (tid == 0) {
+    if (tid == kIssuer) {
       tc_fence_after();
       mma_group(tmem, sb + P_KT, sb + P_TB, C, C, false, 0, 0);
       mma_group(tmem + C, sb + P_TB, sb + P_V, C, VD, false, 0, 1);
@@ -1050,11 +1059,15 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, p_in.v_tile))
     return cudaErrorNotSupported;
   FwdParams p = p_in;
-  // Recurrence value tile: 32 columns when every (run, head, tile) unit runs
-  // at once (one CTA each, no segment ids): the shortest serial chain; 64
-  // otherwise, which halves the units and the item bytes they pull from L2.
+  // Recurrence value tile: without segment ids, the narrowest tile whose
+  // (row, head, tile) units all run at once, one CTA each (32 columns give
+  // the shortest serial chain: the four CTAs of a head share the per-chunk
+  // shared-memory traffic); with segment ids (many short runs) 128 columns,
+  // which reads each item once and does the most work per MMA.
+  const long bh = (long)p.B * p.H, sms = num_sms();
   if (p_in.v_tile != 0) p.v_tile = p_in.v_tile;
-  else p.v_tile = (!has_seg && (long)p.B * p.H * (VD / 32) <= (long)num_sms()) ? 32 : 64;
+  else if (has_seg) p.v_tile = 128;
+  else p.v_tile = bh * 4 <= sms ? 32 : (bh * 2 <= sms ? 64 : 128);
   p.n_vtiles = VD / p.v_tile;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   const size_t ioff = items_offset(p.B, p.T, has_seg);
@@ -1094,7 +1107,6 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   e = cudaFuncSetAttribute(fwd_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  const long sms = num_sms();
   const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
   const int g1 = (int)(n_items < 2 * sms ? n_items : 2 * sms);  // two CTAs per SM
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
