@@ -51,6 +51,7 @@ KERNEL_NAMES = {"simt": "fwd_simt_kernel", "tc": "fwd_tc_kernel",
 HEADLINE = "fixed_bf16_h32_t8192"
 PACKED = "packed_bf16_h32_t8192_25seg"
 PROLOGUE = "packed_bf16_h32_t8192_25seg_conv"   # the packed shape behind the conv prologue
+LONG_FEW_HEADS = "fixed_bf16_h8_t32768"          # long context, few heads: the scan's case
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -491,6 +492,48 @@ def run_ours(args, dist):
             res["cpu_baseline"] = cpu_baseline_backward(w, args.seed, budget_s=args.cpu_seconds / 2)
         return res
 
+    def measure_scan(wname):
+        """The forward as a chunk-parallel state scan (kda_chunk_fwd_scan,
+        automatic segment count) beside the split path, on one workload."""
+        w = ki.WORKLOADS[wname]
+        x = ki.make_inputs(w, seed=rank_seed(w))
+        d = device_inputs(x, dev)
+        o = torch.empty(w.B, w.T, w.H, w.V, dtype=d["q"].dtype, device=dev)
+        fs = torch.empty(w.B, w.H, w.K, w.V, dtype=torch.float32, device=dev)
+        ws_scan = torch.zeros(kda.scan_workspace_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype),
+                              dtype=torch.uint8, device=dev)
+        ws_split = kda.alloc_workspace(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, False, dev,
+                                       impl="split")
+
+        def scan():
+            kda.chunk_fwd_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                               initial_state=d["initial_state"], output_final_state=True,
+                               out=o, final_state_out=fs, workspace=ws_scan, stream=stream)
+
+        def split():
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], output_final_state=True, out=o,
+                          final_state_out=fs, workspace=ws_split, impl="split", stream=stream)
+
+        steps = min(args.steps, 50)
+        t_scan, _ = time_steps(scan, steps, args.warmup, stream, flush, dist, clocks)
+        if kda.read_device_status(ws_scan):
+            raise RuntimeError("device status bits after the scan steps")
+        t_split, _ = time_steps(split, steps, args.warmup, stream, flush, dist, clocks)
+        ms_scan = dist.max(statistics.mean(t_scan))
+        ms_split = dist.max(statistics.mean(t_split))
+        tokens = w.B * w.T
+        return {"workload": w.name, "ms_per_step": ms_scan, "unit": "tokens/s",
+                "value": whole_job_value(dist.world, tokens, ms_scan),
+                "split_ms_per_step": ms_split,
+                "split_value": whole_job_value(dist.world, tokens, ms_split),
+                "segments": kda_scan_segments(w),
+                # prep, map pass, combine, finish pass (+ split: prep, rec)
+                "gpu_launches": steps * (4 + 2)}
+
+    def kda_scan_segments(w):
+        return kda.scan_segments(w.B, w.T, w.H, w.K, w.V)
+
     def packed_launches(w):
         """Kernels one packed forward launches: segment runs (with the chunk
         coordinates), prep, recurrence (+ the fused kernel AUTO enqueues
@@ -515,6 +558,8 @@ def run_ours(args, dist):
               if args.workload == HEADLINE and not args.no_packed else None)
     prologue = (measure_prologue(PROLOGUE)
                 if args.workload == HEADLINE and not args.no_prologue else None)
+    scan = ([measure_scan(n) for n in (HEADLINE, LONG_FEW_HEADS)]
+            if args.workload == HEADLINE and not args.no_scan else None)
     backward = (measure_backward(args.workload)
                 if not args.no_backward and kda.bwd_workspace_size(
                     1, 64, 1, ki.WORKLOADS[args.workload].K, ki.WORKLOADS[args.workload].V) > 0
@@ -560,6 +605,9 @@ def run_ours(args, dist):
     if prologue is not None:
         line["prologue"] = prologue
         line["gpu_launches"] += prologue["gpu_launches"]
+    if scan is not None:
+        line["scan"] = scan
+        line["gpu_launches"] += sum(x["gpu_launches"] for x in scan)
     if backward is not None:
         line["backward"] = backward
         line["gpu_launches"] += backward["gpu_launches"]
@@ -680,6 +728,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--no-packed", action="store_true", help="skip the packed N=25 leg")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
+    ap.add_argument("--no-scan", action="store_true",
+                    help="skip the chunk-parallel scan leg (headline and long-context shapes)")
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip the conv prologue leg (packed N=25 shape)")
     args = ap.parse_args()

@@ -103,6 +103,12 @@ def lib():
         L.kda_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
                                     vp, vp, vp, vp, u64, vp]
         L.kda_chunk_bwd.restype = i
+        L.kda_chunk_fwd_scan_workspace_size.argtypes = [sp, i]
+        L.kda_chunk_fwd_scan_workspace_size.restype = u64
+        L.kda_chunk_fwd_scan_segments.argtypes = [sp, i]
+        L.kda_chunk_fwd_scan_segments.restype = i
+        L.kda_chunk_fwd_scan.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, i, vp, u64, vp]
+        L.kda_chunk_fwd_scan.restype = i
         L.kda_chunk_fwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp]
         L.kda_chunk_fwd_noalloc.restype = i
         L.kda_chunk_fwd_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -237,6 +243,61 @@ def chunk_fwd(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None
         IMPLS[impl], int(v_tile), _stream_ptr(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
+    return o, fs
+
+
+def scan_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, n_segments=0) -> int:
+    """Workspace bytes of chunk_fwd_scan (0 when the shape is not served)."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_scan_workspace_size(ctypes.byref(s), int(n_segments)))
+
+
+def scan_segments(B, T, H, K, V, dtype=torch.bfloat16, n_segments=0) -> int:
+    """Segments per row chunk_fwd_scan uses for this request (0: not served)."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_scan_segments(ctypes.byref(s), int(n_segments)))
+
+
+def chunk_fwd_scan(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None,
+                   output_final_state=False, n_segments=0, out=None, final_state_out=None,
+                   workspace=None, stream=None):
+    """The chunked forward as a chunk-parallel state scan over ``n_segments``
+    segments per row (0: chosen to fill the GPU); rows without segment ids,
+    bf16 with K = V = 128.  Same results as chunk_fwd up to rounding.
+    Returns ``(o, final_state or None)``."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("chunk_fwd_scan needs CUDA tensors")
+    _check(q, "q", (B, T, H, K), dt, dev)
+    _check(k, "k", (B, T, H, K), dt, dev)
+    _check(v, "v", (B, T, H, V), dt, dev)
+    _check(g, "g", (B, T, H, K), torch.float32, dev)
+    _check(beta, "beta", (B, T, H), torch.float32, dev)
+    _check(initial_state, "initial_state", (B, H, K, V), torch.float32, dev)
+    if scale is None:
+        scale = K ** -0.5
+    o = out if out is not None else torch.empty(B, T, H, V, dtype=dt, device=dev)
+    _check(o, "out", (B, T, H, V), dt, dev)
+    fs = None
+    if output_final_state:
+        fs = final_state_out if final_state_out is not None else torch.empty(
+            B, H, K, V, dtype=torch.float32, device=dev)
+        _check(fs, "final_state_out", (B, H, K, V), torch.float32, dev)
+    if workspace is None:
+        n = scan_workspace_size(B, T, H, K, V, dt, n_segments)
+        if n == 0:
+            raise KdaError(2, "kda_chunk_fwd_scan_workspace_size")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_fwd_scan(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        int(chunk_size), _ptr(initial_state), _ptr(o), _ptr(fs), int(n_segments),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_scan")
     return o, fs
 
 

@@ -201,6 +201,50 @@ kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const void *k,
   return from_cuda(e);
 }
 
+int kda_chunk_fwd_scan_segments(const kda_shape *s, int n_segments) {
+  if (kda_chunk_fwd_scan_workspace_size(s, n_segments) == 0) return 0;
+  return scan_segments(s->B, s->T, s->H, n_segments);
+}
+
+size_t kda_chunk_fwd_scan_workspace_size(const kda_shape *s, int n_segments) {
+  if (check_shape(s) != KDA_OK || n_segments < 0 || n_segments == 1) return 0;
+  if (!fwd_split_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16, false, 0)) return 0;
+  if ((s->T + kChunk - 1) / kChunk < 2) return 0;
+  return scan_workspace_bytes(s->B, s->T, s->H, n_segments);
+}
+
+kda_status kda_chunk_fwd_scan(const kda_shape *s, const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, float scale, int chunk_size,
+                              const float *initial_state, void *o, float *final_state,
+                              int n_segments, void *workspace, size_t workspace_bytes,
+                              kda_stream_t stream) {
+  kda_status st = check_shape(s);
+  if (st != KDA_OK) return st;
+  if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+  if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (n_segments < 0 || n_segments == 1) return KDA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return KDA_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, o, initial_state, final_state};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  const size_t need = kda_chunk_fwd_scan_workspace_size(s, n_segments);
+  if (need == 0) return KDA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.scale = scale;
+  p.initial_state = initial_state;
+  p.o = o;
+  p.final_state = final_state;
+  p.status = &reinterpret_cast<WsHeader *>(workspace)->status;
+  const int P = scan_segments(s->B, s->T, s->H, n_segments);
+  return from_cuda(launch_fwd_split(p, workspace, workspace_bytes,
+                                    reinterpret_cast<cudaStream_t>(stream), false, P));
+}
+
 int kda_impl_available(kda_impl impl, const kda_shape *s, int v_tile) {
   if (check_shape(s) != KDA_OK || v_tile < 0) return 0;
   const bool bf16 = s->qkv_dtype == KDA_DTYPE_BF16;

@@ -46,10 +46,18 @@ constexpr int VT = 32;
 constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: MN-major, 128 rows x Kd 128 channels
 constexpr uint32_t I_AQK = 32768;     // A_qk: K-major, 64 rows, Kd 64
 constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: K-major, 128 channels x Kd 64 rows
-constexpr uint32_t I_U = 57344;       // u bf16 [vt][r][32]
+constexpr uint32_t I_U = 57344;       // u bf16, 4 tiles of 32 columns, see u_off
 constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
 constexpr uint32_t ITEM_BYTES = 74240;     // 72.5 KiB, 256-byte aligned
 constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
+
+// Byte offset of u's 8 columns c .. c + 7 (c a multiple of 8 within the
+// 32-column tile vt) of row r: each tile is [column group of 8][row][8]
+// bf16, so the 32 rows a warp reads for one column group are 512
+// contiguous bytes (no bank conflicts), and a tile is one 4 KiB block.
+__device__ __forceinline__ uint32_t u_off(int vt, int c, int r) {
+  return (uint32_t)(vt * 4096 + (c >> 3) * 1024 + r * 16);
+}
 
 // ---- prep kernel --------------------------------------------------------------
 // Two CTAs of 256 threads per SM, each working on its own item, so that one
@@ -635,11 +643,13 @@ __global__ void __launch_bounds__(PT, 2)
         for (int e = 0; e < 2; ++e) {
           const int col = 16 * (e ? p1 : p0), vt = col >> 5, cv = col & 31;
           const float *vv = e ? v1 : v0;
-          uint4 *dst = reinterpret_cast<uint4 *>(gi + I_U + ((size_t)(vt * C + r) * VT + cv) * 2);
-          dst[0] = make_uint4(pack_bf16(vv[0], vv[1]), pack_bf16(vv[2], vv[3]),
-                              pack_bf16(vv[4], vv[5]), pack_bf16(vv[6], vv[7]));
-          dst[1] = make_uint4(pack_bf16(vv[8], vv[9]), pack_bf16(vv[10], vv[11]),
-                              pack_bf16(vv[12], vv[13]), pack_bf16(vv[14], vv[15]));
+          unsigned char *dst = gi + I_U + u_off(vt, cv, r);
+          *reinterpret_cast<uint4 *>(dst) =
+              make_uint4(pack_bf16(vv[0], vv[1]), pack_bf16(vv[2], vv[3]),
+                         pack_bf16(vv[4], vv[5]), pack_bf16(vv[6], vv[7]));
+          *reinterpret_cast<uint4 *>(dst + 1024) =
+              make_uint4(pack_bf16(vv[8], vv[9]), pack_bf16(vv[10], vv[11]),
+                         pack_bf16(vv[12], vv[13]), pack_bf16(vv[14], vv[15]));
         }
       }
     }
@@ -673,6 +683,23 @@ done:
 // and e^{G_C}.  A_qk is read as the 128-row A operand starting 64 rows
 // before it: those rows (the tail of Q e^G) only feed D1 rows 0..63, which
 // are dead once U is formed.
+// Chunk-parallel state scan (rows without segment ids): each row's chunks
+// are cut into n_segs segments of cps chunks.  The chunk form is affine in
+// the state entering a chunk, S' = (diag(e^{G_C}) - (K e^{G_C-G})^T w) S +
+// (K e^{G_C-G})^T u, so a segment maps its entering state to
+// S_end = M S_start + B.  The map pass (MAP = 1) runs the recurrence of
+// segments 0 .. n_segs - 2 on X = [B | M] (K x (V + K)) from [0 | I], with
+// u replaced by [u | 0] and no outputs, and writes X to `maps`
+// [B][n_segs - 1][H][K][V + K]; scan_combine_kernel chains
+// S_start(s + 1) = M_s S_start(s) + B_s into `starts` [B][n_segs][H][K][V];
+// the finish pass (MAP = 0) runs every segment from its S_start, writing o
+// and, for the last segment, the final state.  n_segs = 0: no scan.
+struct ScanParams {
+  int n_segs, cps;
+  float *maps;
+  float *starts;
+};
+
 constexpr uint32_t S_WQ = I_WQ, S_AQK = I_AQK, S_KHT = I_KHT, S_U = I_U;
 static_assert(S_WQ == 0 && S_AQK == 32768 && S_KHT == S_AQK + 8192 && S_U == S_KHT + 16384,
               "stage layout");
@@ -706,11 +733,13 @@ struct RecLayout {
 // D2 is issued before the o product, so the state update, and with it the
 // next chunk's first MMA, waits only for the products on the serial chain;
 // the o product runs on the tensor pipe while the CUDA cores update S.
-template <int VTR, int NST>
+template <int VTR, int NST, int MAP>
 __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
-    fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct) {
+    fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct,
+                   const ScanParams sc) {
   using Lay = RecLayout<VTR, NST>;
   constexpr int CPT = Lay::CPT;
+  constexpr int NVT_V = VD / VTR;  // tiles of V; map tiles past them are M's columns
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -806,34 +835,72 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
 
   float S[CPT];  // S[key row L][col0 .. col0 + CPT - 1], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
-  const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
+  const int seg_units = MAP ? sc.n_segs - 1 : sc.n_segs;
+  const uint32_t n_units =
+      !fits ? 0u
+            : sc.n_segs > 0 ? (uint32_t)seg_units * (uint32_t)p.B * (uint32_t)H * (uint32_t)p.n_vtiles
+                            : total_units(p.runs, p.B, H, p.n_vtiles);
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
-    const int vt = u.vt, h = u.h, b = u.b;
+    int vt, h, b, ustart, uend, seg = 0;
+    bool ufirst, ulast;
+    uint32_t cbase;
+    if (sc.n_segs > 0) {  // (segment, row, head, tile), rows without segment ids
+      uint32_t x = unit;
+      vt = (int)(x % (uint32_t)p.n_vtiles);
+      x /= (uint32_t)p.n_vtiles;
+      h = (int)(x % (uint32_t)H);
+      x /= (uint32_t)H;
+      b = (int)(x % (uint32_t)p.B);
+      seg = (int)(x / (uint32_t)p.B);
+      const int c0 = seg * sc.cps, c1 = min(c0 + sc.cps, ct.n_chunks_row);
+      ustart = c0 * C;
+      uend = min(c1 * C, T);
+      ufirst = seg == 0;
+      ulast = seg == sc.n_segs - 1;
+      cbase = (uint32_t)b * ct.n_chunks_row + (uint32_t)c0;
+    } else {
+      const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
+      vt = u.vt; h = u.h; b = u.b;
+      ustart = u.start; uend = u.end;
+      ufirst = u.first; ulast = u.last;
+      cbase = ct.run_chunk_base
+          ? (uint32_t)(ct.chunk_row_offsets[b] + ct.run_chunk_base[(size_t)b * T + u.run_in_row])
+          : (uint32_t)b * ct.n_chunks_row;
+    }
     const int vc0 = vt * VTR;
-    const int n_chunks = (u.end - u.start + C - 1) / C;
-    const uint32_t cbase = ct.run_chunk_base
-        ? (uint32_t)(ct.chunk_row_offsets[b] + ct.run_chunk_base[(size_t)b * T + u.run_in_row])
-        : (uint32_t)b * ct.n_chunks_row;
+    const int n_chunks = uend > ustart ? (uend - ustart + C - 1) / C : 0;
+    if (n_chunks == 0) continue;
+    // map pass: the tiles of M read no u (its columns of [u | 0] are zero)
+    const bool m_tile = MAP && vt >= NVT_V;
+    const int vt_u = m_tile ? 0 : vt;
     auto item_ptr = [&](int c) {
       return items + ((size_t)(cbase + c) * H + h) * ITEM_BYTES;
     };
-    // state entering the run; S^T operand (MN-major: v contiguous)
-    if (u.first && p.initial_state) {
-      const float4 *src = reinterpret_cast<const float4 *>(
-          p.initial_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0);
+    // state entering the run (or segment); S^T operand (MN-major: v contiguous)
+    const float *s_src = nullptr;
+    if (!MAP) {
+      if (ufirst) s_src = p.initial_state
+          ? p.initial_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0 : nullptr;
+      else if (sc.n_segs > 0)
+        s_src = sc.starts + ((((size_t)b * sc.n_segs + seg) * H + h) * KD + L) * p.V + vc0 + col0;
+    }
+    if (s_src) {
+      const float4 *src = reinterpret_cast<const float4 *>(s_src);
 #pragma unroll
       for (int q4 = 0; q4 < CPT / 4; ++q4) {
         const float4 x = src[q4];
         S[4 * q4] = x.x; S[4 * q4 + 1] = x.y; S[4 * q4 + 2] = x.z; S[4 * q4 + 3] = x.w;
       }
+    } else if (m_tile) {  // identity columns of M
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) S[i] = (L == (vt - NVT_V) * VTR + col0 + i) ? 1.f : 0.f;
     } else {
 #pragma unroll
       for (int i = 0; i < CPT; ++i) S[i] = 0.f;
     }
     store_st(S, L);
     if (tid == 0) {
-      for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt);
+      for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt_u);
       for (int c = NST; c < NST + kRecPrefetch && c < n_chunks; ++c) prefetch_l2(item_ptr(c), ITEM_BYTES);
     }
     st_issued = (1u << (NST < n_chunks ? NST : n_chunks)) - 1u;
@@ -852,8 +919,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     int s = 0;  // stage of chunk c
     for (int c = 0; c < n_chunks; ++c) {
       const int s1 = s + 1 == NST ? 0 : s + 1;  // stage of chunk c + 1
-      const int t0 = u.start + c * C;
-      const int n = min(C, u.end - t0);
+      const int t0 = ustart + c * C;
+      const int n = min(C, uend - t0);
       const size_t tok0 = (size_t)b * T + t0;
       const unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
       const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
@@ -873,7 +940,12 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
         for (int e = 0; e < CPT / 8; ++e) {
           const int col = col0 + 8 * e;
           float uu[8], a[8];
-          ld_bf16x8(stg + S_U + (col >> 5) * 4096 + ((size_t)r * VT + (col & 31)) * 2, uu);
+          if (m_tile) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) uu[i] = 0.f;
+          } else {
+            ld_bf16x8(stg + S_U + u_off(col >> 5, col & 31, r), uu);
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) a[i] = uu[i] - v[8 * e + i];
           st_bf16x8(smem, Lay::UT + mn_off(col, r, C), a);
@@ -889,8 +961,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
         tc_fence_after();
         mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 0, 1);
         commit(s_bar, c_s);
-        mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
-        commit(o_bar, c_o);
+        if (!MAP) mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
+        commit(o_bar, c_o);  // the map pass has no o product: this tracks D2
       }
       wait_bar(s_bar, n_s);
       tc_fence_after();
@@ -909,7 +981,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
       bool refilled = false;
       if (tid == kRefillTid && c + NST < n_chunks && mbar_try_wait(o_bar, n_o & 1u)) {
         tc_fence_after();
-        issue_stage(s, item_ptr(c + NST), vt);
+        issue_stage(s, item_ptr(c + NST), vt_u);
         if (c + NST + kRecPrefetch < n_chunks) prefetch_l2(item_ptr(c + NST + kRecPrefetch), ITEM_BYTES);
         refilled = true;
       }
@@ -932,13 +1004,13 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
         wait_bar(o_bar, n_o);
         tc_fence_after();
         if (tid == kRefillTid && !refilled && c + NST < n_chunks) {
-          issue_stage(s, item_ptr(c + NST), vt);
+          issue_stage(s, item_ptr(c + NST), vt_u);
           if (c + NST + kRecPrefetch < n_chunks) prefetch_l2(item_ptr(c + NST + kRecPrefetch), ITEM_BYTES);
         }
         const int r = L - 64;
         float v[CPT];
-        tmem_ld_cpt(tq + d1 + col0, v);
-        if (r < n) {
+        if (!MAP) tmem_ld_cpt(tq + d1 + col0, v);
+        if (!MAP && r < n) {
           uint4 *dst = reinterpret_cast<uint4 *>(
               static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0 + col0);
 #pragma unroll
@@ -956,9 +1028,14 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
       tc_fence_before();
       s = s1;
     }
-    if (u.last && p.final_state) {
-      float4 *dst = reinterpret_cast<float4 *>(
-          p.final_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0);
+    float *s_dst = nullptr;
+    if (MAP)
+      s_dst = sc.maps + ((((size_t)b * (sc.n_segs - 1) + seg) * H + h) * KD + L) * (VD + KD) +
+              vc0 + col0;
+    else if (ulast && p.final_state)
+      s_dst = p.final_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0;
+    if (s_dst) {
+      float4 *dst = reinterpret_cast<float4 *>(s_dst);
 #pragma unroll
       for (int q4 = 0; q4 < CPT / 4; ++q4)
         dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
@@ -977,6 +1054,68 @@ done:
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::TM_COLS);
+  }
+}
+
+// S_start(s + 1) = M_s S_start(s) + B_s for s = 0 .. n_segs - 2, in fp32:
+// one CTA per (row, head, 32 columns of S), each thread a 4 x 4 register
+// tile (rows 4 kq .., columns 4 cq ..); S_start(0) is the initial state (or
+// zero).  M_s is staged in shared memory with a padded row (129 floats), so
+// the 4 rows a thread reads per step are in distinct banks.
+constexpr int kCombLd = KD + 1;
+constexpr uint32_t kCombSmem = (uint32_t)(KD * kCombLd + KD * 32) * 4;
+__global__ void __launch_bounds__(256)
+    scan_combine_kernel(const FwdParams p, const ScanParams sc) {
+  extern __shared__ float csm[];
+  float *sM = csm;                  // M_s [KD][kCombLd]
+  float *sS = csm + KD * kCombLd;   // S_start(s)[:, tile] [KD][32]
+  const int tile = blockIdx.x % (VD / 32), bh = blockIdx.x / (VD / 32);
+  const int h = bh % p.H, b = bh / p.H;
+  const int tid = threadIdx.x, kq = tid >> 3, cq = tid & 7;
+  for (int i = tid; i < KD * 32; i += 256) {
+    const int kk = i >> 5, cc = i & 31;
+    sS[i] = p.initial_state
+                ? p.initial_state[(((size_t)b * p.H + h) * KD + kk) * VD + 32 * tile + cc]
+                : 0.f;
+  }
+  for (int s = 0; s + 1 < sc.n_segs; ++s) {
+    const float *map = sc.maps + (((size_t)b * (sc.n_segs - 1) + s) * p.H + h) * KD * (VD + KD);
+    __syncthreads();  // sS of this step written, sM of the last step read
+    for (int i = tid; i < KD * KD / 4; i += 256) {  // M_s = map[:, VD:]
+      const int kk = i / (KD / 4), m4 = i % (KD / 4);
+      const float4 x = *reinterpret_cast<const float4 *>(map + (size_t)kk * (VD + KD) + VD + 4 * m4);
+      float *d = sM + kk * kCombLd + 4 * m4;
+      d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {  // B_s
+      const float4 x = *reinterpret_cast<const float4 *>(
+          map + (size_t)(4 * kq + r) * (VD + KD) + 32 * tile + 4 * cq);
+      acc[r][0] = x.x; acc[r][1] = x.y; acc[r][2] = x.z; acc[r][3] = x.w;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int m = 0; m < KD; ++m) {
+      const float4 sv = *reinterpret_cast<const float4 *>(sS + m * 32 + 4 * cq);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float mv = sM[(4 * kq + r) * kCombLd + m];
+        acc[r][0] = fmaf(mv, sv.x, acc[r][0]);
+        acc[r][1] = fmaf(mv, sv.y, acc[r][1]);
+        acc[r][2] = fmaf(mv, sv.z, acc[r][2]);
+        acc[r][3] = fmaf(mv, sv.w, acc[r][3]);
+      }
+    }
+    __syncthreads();  // every thread has read sS
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float4 x = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      *reinterpret_cast<float4 *>(sS + (4 * kq + r) * 32 + 4 * cq) = x;
+      *reinterpret_cast<float4 *>(
+          sc.starts + ((((size_t)b * sc.n_segs + s + 1) * p.H + h) * KD + 4 * kq + r) * VD +
+          32 * tile + 4 * cq) = x;
+    }
   }
 }
 
@@ -1027,6 +1166,26 @@ size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per
   return items_offset(B, T, has_seg) + chunks * H * ITEM_BYTES;
 }
 
+int scan_segments(int B, int T, int H, int n_segs) {
+  const int nc = (T + C - 1) / C;
+  if (n_segs == 0) {  // fill the GPU with the finish pass's 32-column units
+    const long units = (long)B * H * (VD / 32);
+    n_segs = (int)(num_sms() / (units > 0 ? units : 1));
+  }
+  if (n_segs < 2) n_segs = 2;
+  if (n_segs > nc) n_segs = nc;
+  const int cps = (nc + n_segs - 1) / n_segs;
+  return (nc + cps - 1) / cps;  // segments that hold at least one chunk
+}
+
+size_t scan_workspace_bytes(int B, int T, int H, int n_segs) {
+  const int P = scan_segments(B, T, H, n_segs);
+  if (P < 2) return 0;
+  const size_t maps = (size_t)(P - 1) * B * H * KD * (VD + KD) * 4;
+  const size_t starts = (size_t)P * B * H * KD * VD * 4;
+  return align_up(split_workspace_bytes(B, T, H, false, 0), 256) + align_up(maps, 256) + starts;
+}
+
 bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
   return bf16 && K == KD && V == VD &&
          (v_tile == 0 || v_tile == 32 || v_tile == 64 || v_tile == 128);
@@ -1036,28 +1195,47 @@ bool fwd_split_supported(int K, int V, bool bf16, bool, int v_tile) {
 // bytes queued at the same L2 -> SM throughput) and measured slower.
 constexpr int kRecStages = 2;
 namespace {
-template <int VTR, int NST>
+template <int VTR, int NST, int MAP>
 cudaError_t launch_rec(const FwdParams &p, const unsigned char *items, const ChunkTable &ct,
-                       bool has_seg, cudaStream_t stream) {
+                       bool has_seg, const ScanParams &sc, cudaStream_t stream) {
   using Lay = RecLayout<VTR, NST>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_rec_kernel<VTR, NST>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_rec_kernel<VTR, NST, MAP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Lay::ALLOC);
   if (e != cudaSuccess) return e;
   const long sms = num_sms();
-  const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles
-                               : (long)p.B * p.H * p.n_vtiles;
+  const long rows = sc.n_segs > 0 ? (long)p.B * (MAP ? sc.n_segs - 1 : sc.n_segs) : (long)p.B;
+  const long n_units = has_seg ? (long)p.B * p.T * p.H * p.n_vtiles : rows * p.H * p.n_vtiles;
   const int g2 = (int)(n_units < sms ? n_units : sms);
-  fwd_rec_kernel<VTR, NST><<<g2 > 0 ? g2 : 1, Lay::THREADS, Lay::ALLOC, stream>>>(p, items, ct);
+  fwd_rec_kernel<VTR, NST, MAP><<<g2 > 0 ? g2 : 1, Lay::THREADS, Lay::ALLOC, stream>>>(p, items,
+                                                                                         ct, sc);
   return cudaGetLastError();
+}
+
+template <int MAP>
+cudaError_t launch_rec_tile(const FwdParams &p, const unsigned char *items, const ChunkTable &ct,
+                            bool has_seg, const ScanParams &sc, cudaStream_t stream) {
+  return p.v_tile == 32   ? launch_rec<32, kRecStages, MAP>(p, items, ct, has_seg, sc, stream)
+         : p.v_tile == 64 ? launch_rec<64, kRecStages, MAP>(p, items, ct, has_seg, sc, stream)
+                          : launch_rec<128, kRecStages, MAP>(p, items, ct, has_seg, sc, stream);
+}
+
+// Narrowest value tile (32, 64 or 128 columns) whose `units` per tile
+// count, times the tiles of `cols` columns, fits one CTA per SM.
+int fit_tile(long units, int cols) {
+  const long sms = num_sms();
+  if (units * (cols / 32) <= sms) return 32;
+  if (units * (cols / 64) <= sms) return 64;
+  return 128;
 }
 }  // namespace
 
 cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream, bool with_fallback) {
+                             cudaStream_t stream, bool with_fallback, int scan_segs) {
   const bool has_seg = p_in.runs.runs != nullptr;
   if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, p_in.v_tile))
     return cudaErrorNotSupported;
+  if (scan_segs < 0 || (scan_segs > 0 && has_seg)) return cudaErrorNotSupported;
   FwdParams p = p_in;
   // Recurrence value tile: without segment ids, the narrowest tile whose
   // (row, head, tile) units all run at once, one CTA each (32 columns give
@@ -1112,9 +1290,32 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = p.v_tile == 32   ? launch_rec<32, kRecStages>(p, items, ct, has_seg, stream)
-      : p.v_tile == 64 ? launch_rec<64, kRecStages>(p, items, ct, has_seg, stream)
-                       : launch_rec<128, kRecStages>(p, items, ct, has_seg, stream);
+  ScanParams sc = {0, 0, nullptr, nullptr};
+  if (scan_segs > 0) {
+    // chunk-parallel scan: map pass, combine, finish pass (see ScanParams)
+    const int nc = ct.n_chunks_row;
+    sc.n_segs = scan_segments(p.B, p.T, p.H, scan_segs);
+    sc.cps = (nc + sc.n_segs - 1) / sc.n_segs;
+    const size_t items_end = align_up(split_workspace_bytes(p.B, p.T, p.H, false, 0), 256);
+    const size_t maps_bytes = align_up((size_t)(sc.n_segs - 1) * p.B * p.H * KD * (VD + KD) * 4, 256);
+    if (workspace_bytes < scan_workspace_bytes(p.B, p.T, p.H, scan_segs)) return cudaErrorInvalidValue;
+    sc.maps = reinterpret_cast<float *>(ws + items_end);
+    sc.starts = reinterpret_cast<float *>(ws + items_end + maps_bytes);
+    FwdParams pm = p;
+    pm.v_tile = fit_tile((long)p.B * p.H * (sc.n_segs - 1), VD + KD);
+    pm.n_vtiles = (VD + KD) / pm.v_tile;
+    e = launch_rec_tile<1>(pm, items, ct, false, sc, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kCombSmem);
+    if (e != cudaSuccess) return e;
+    scan_combine_kernel<<<p.B * p.H * (VD / 32), 256, kCombSmem, stream>>>(p, sc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p_in.v_tile == 0) p.v_tile = fit_tile((long)p.B * p.H * sc.n_segs, VD);
+    p.n_vtiles = VD / p.v_tile;
+  }
+  e = launch_rec_tile<0>(p, items, ct, has_seg, sc, stream);
   if (e != cudaSuccess || !with_fallback || !has_seg) return e;
   // The fused kernel covers calls whose runs overflow the items (it exits
   // at once when they fit).

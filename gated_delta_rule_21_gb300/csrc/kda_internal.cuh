@@ -113,9 +113,14 @@ size_t split_workspace_bytes(int B, int T, int H, bool has_seg = false,
                              int max_runs_per_row = 0);
 bool fwd_split_supported(int K, int V, bool bf16, bool has_seg, int v_tile);
 // with_fallback (AUTO): with segment ids, also enqueue the fused kernel,
-// gated to run only when the runs overflow the split items.
+// gated to run only when the runs overflow the split items.  scan_segs > 0
+// (rows without segment ids only): the recurrence as a chunk-parallel scan
+// over that many segments per row (scan_segments() rounds the request; 0 in
+// scan_segments picks the count that fills the GPU).
 cudaError_t launch_fwd_split(const FwdParams &p, void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream, bool with_fallback = false);
+                             cudaStream_t stream, bool with_fallback = false, int scan_segs = 0);
+int scan_segments(int B, int T, int H, int n_segs);
+size_t scan_workspace_bytes(int B, int T, int H, int n_segs);
 
 // Backward (kda_bwd.cu).  Per-tile partial sums of dq, dk, dg ([n_vtiles]
 // x [B*T*H*K]) and dbeta ([n_vtiles] x [B*T*H]) are summed into the outputs

@@ -195,6 +195,41 @@ KDA_API kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const voi
                             kda_stream_t stream);
 
 /*
+ * The chunked forward computed as a chunk-parallel state scan, for rows
+ * without segment ids (the single-GPU counterpart of the state chain of the
+ * pages' context parallelism: page "feat(kda): integrate KDA attention with
+ * tokamax backend and CP support", section "Implementation Details").  Each
+ * row's 64-token chunks are cut into n_segments contiguous segments.  The
+ * chunk form is affine in the state entering a chunk, so each segment but
+ * the last maps its entering state S to M S + B (M: K x K, B: K x V, both
+ * computed in parallel over segments, rows and heads), the segments'
+ * entering states are chained from initial_state in fp32, and then every
+ * segment's chunks run in parallel from their entering state.  It trades
+ * about three times the state-recurrence work for a chain n_segments times
+ * shorter, which pays when few (row, head) pairs leave SMs idle and T is
+ * long.  Arguments, layouts and results are those of kda_chunk_fwd with
+ * segment_ids = NULL (up to rounding: the maps are rounded like the state).
+ *   n_segments  0 (choose: enough segments to fill the GPU's SMs with the
+ *               final pass, at least 2) or >= 2; capped at ceil(T/64) and
+ *               rounded so every segment holds at least one chunk.
+ *   workspace   device, kda_chunk_fwd_scan_workspace_size(s, n_segments)
+ *               bytes, 256-byte aligned, zero-filled before first use.
+ * bf16 q/k/v with K = V = 128 and T > 64 only (KDA_ERR_UNSUPPORTED
+ * otherwise; the workspace query then returns 0); KDA_ERR_INVALID_ARG for
+ * n_segments < 0 or == 1.  Asynchronous on `stream`.
+ */
+KDA_API size_t kda_chunk_fwd_scan_workspace_size(const kda_shape *s, int n_segments);
+/* The segment count kda_chunk_fwd_scan uses for this request (0 when the
+ * shape or the request is not served). */
+KDA_API int kda_chunk_fwd_scan_segments(const kda_shape *s, int n_segments);
+KDA_API kda_status kda_chunk_fwd_scan(const kda_shape *s, const void *q, const void *k,
+                                      const void *v, const float *g, const float *beta,
+                                      float scale, int chunk_size, const float *initial_state,
+                                      void *o, float *final_state, int n_segments,
+                                      void *workspace, size_t workspace_bytes,
+                                      kda_stream_t stream);
+
+/*
  * kda_chunk_fwd without a workspace argument, for callers that cannot
  * allocate device memory (no counterpart on the pages: it exists only for
  * such callers).  A plugin inside a host application may be handed nothing

@@ -73,6 +73,13 @@ WORKLOADS = {
     "packed_bf16_h32_t8192_25seg_conv": Workload(
         "packed_bf16_h32_t8192_25seg_conv", B=1, T=8192, H=32, K=128, V=128,
         segments=tuple([328] * 17 + [327] * 8), prologue=True),
+    # not one of the pages' workloads: a long context with few heads (the
+    # same token-heads as B1 H32 T8192), where one state chain per
+    # (row, head, value tile) leaves most SMs idle; timed for the
+    # chunk-parallel state scan
+    "fixed_bf16_h8_t32768": Workload(
+        "fixed_bf16_h8_t32768", B=1, T=32768, H=8, K=128, V=128,
+        init_state_std=0.1),
 }
 
 
