@@ -83,7 +83,12 @@ typedef enum kda_impl {
                          large enough, else TC, else SIMT.  With segment
                          ids and the split path it always computes the
                          result: runs that overflow the split workspace are
-                         served by the fused TC kernel on the device.       */
+                         served by the fused TC kernel on the device.
+                         Without segment ids, when at least 3 segments of
+                         16 or more chunks fill the SMs (few rows x heads,
+                         long T) and the workspace holds the scan's
+                         buffers, SPLIT runs as the chunk-parallel scan of
+                         kda_chunk_fwd_scan.                                */
   KDA_IMPL_SIMT = 1,  /* fp32 CUDA-core kernel (every supported shape)      */
   KDA_IMPL_TC = 2,    /* fused tcgen05 / TMA kernel: bf16, K = V = 128      */
   KDA_IMPL_SPLIT = 3  /* tcgen05 in two kernels (parallel per-chunk prep,

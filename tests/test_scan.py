@@ -130,3 +130,32 @@ def test_scan_in_benchmark_configuration():
     o_ref, fs_ref = run_oracle(x)
     assert_parity(o, o_ref, True, "B1 H32 T8192 scan o")
     assert_parity(fs, fs_ref, True, "B1 H32 T8192 scan final_state")
+
+
+@pytest.mark.gpu
+def test_auto_workspace_covers_the_scan_on_long_few_head_rows(kda):
+    """AUTO's default workspace is the scan's on long rows with few heads
+    (there it runs the scan), the split path's elsewhere.  The choice counts
+    the SMs of the current device, so this needs one."""
+    long_ = kda.workspace_size(1, 32768, 8, 128, 128)
+    assert long_ == kda.scan_workspace_size(1, 32768, 8, 128, 128) > \
+        kda.workspace_size(1, 32768, 8, 128, 128, impl="split")
+    assert kda.workspace_size(1, 8192, 32, 128, 128) == \
+        kda.workspace_size(1, 8192, 32, 128, 128, impl="split")
+    assert kda.workspace_size(1, 1024, 8, 128, 128) == \
+        kda.workspace_size(1, 1024, 8, 128, 128, impl="split")       # short rows
+
+
+@pytest.mark.gpu
+def test_auto_on_long_few_head_rows_matches_oracle():
+    """kda_chunk_fwd (AUTO) on B1 H8 T32768, which it runs as the scan."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.WORKLOADS["fixed_bf16_h8_t32768"]
+    x = ki.make_inputs(w, seed=4)
+    d = {n: to_dev(x[n]) for n in ("q", "k", "v", "g", "beta", "initial_state")}
+    o, fs = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], output_final_state=True)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = run_oracle(x)
+    assert_parity(o, o_ref, True, "B1 H8 T32768 auto o")
+    assert_parity(fs, fs_ref, True, "B1 H8 T32768 auto final_state")
