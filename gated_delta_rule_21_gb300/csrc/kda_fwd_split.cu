@@ -28,6 +28,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
+#include "kda_f32x2.cuh"
 #include "kda_internal.cuh"
 #include "kda_tc_common.cuh"
 
@@ -227,6 +230,21 @@ __device__ __forceinline__ uint4 pack8s(const float (&v)[8], float s) {
   return make_uint4(pack_bf16(v[0] * s, v[1] * s), pack_bf16(v[2] * s, v[3] * s),
                     pack_bf16(v[4] * s, v[5] * s), pack_bf16(v[6] * s, v[7] * s));
 }
+// The same from 4 packed f32x2 row pairs (scaled on the FMA pipe two lanes
+// at a time: each lane is the scalar fp32 product).
+__device__ __forceinline__ uint32_t pack_bf16x2(u64 v) {
+  float a, b;
+  upk2(v, a, b);
+  return pack_bf16(a, b);
+}
+__device__ __forceinline__ uint4 pack8x2(const u64 (&v)[4]) {
+  return make_uint4(pack_bf16x2(v[0]), pack_bf16x2(v[1]), pack_bf16x2(v[2]), pack_bf16x2(v[3]));
+}
+__device__ __forceinline__ uint4 pack8x2s(const u64 (&v)[4], float s) {
+  const u64 s2 = pk2(s, s);
+  return make_uint4(pack_bf16x2(mul2(v[0], s2)), pack_bf16x2(mul2(v[1], s2)),
+                    pack_bf16x2(mul2(v[2], s2)), pack_bf16x2(mul2(v[3], s2)));
+}
 
 __global__ void __launch_bounds__(PT, 2)
     fwd_prep_kernel(const FwdParams p, unsigned char *items, const ChunkTable ct,
@@ -364,19 +382,25 @@ __global__ void __launch_bounds__(PT, 2)
 
       // ---- P0: gate cumsum down this thread's 16 rows (log2 units; rows
       //      past the chunk's end add nothing), block sums to smem ----
+      // A full chunk (every item but a run's last) takes code with no
+      // per-row tests: `full` is a compile-time constant in each branch.
+      const bool full_chunk = n == C;
       float G[kSub];
-      {
+      auto cumsum = [&](auto full) {
         const unsigned char *gcol = smem + P_RAW_G + 8192 * (ec >> 5) + 4 * (ec & 31);
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < kSub; ++i) {
           const int r = er0 + i;
-          const float gv = r < n ? *reinterpret_cast<const float *>(gcol + 128 * r) : 0.f;
+          const float gv = (decltype(full)::value || r < n)
+                               ? *reinterpret_cast<const float *>(gcol + 128 * r) : 0.f;
           acc = fmaf(gv, kLog2e, acc);
           G[i] = acc;
         }
         sBsum[eb * KH + ec] = acc;
-      }
+      };
+      if (full_chunk) cumsum(std::true_type{});
+      else cumsum(std::false_type{});
       __syncthreads();
       // ---- P1: block offsets and factors of (block eb, channel ch), then
       //      this half's operands: X, Y_b, (K e^G)^T (smem, for the MMAs),
@@ -400,38 +424,49 @@ __global__ void __launch_bounds__(PT, 2)
       const float x3 = ex2(E4 - E2);    // D_{b+1} D_{b+2}
       if (eb == 0) reinterpret_cast<float *>(gi + I_GAM)[ch] = ex2(GC2);  // e^{G_C}
       if (half == 1) wait_mma();  // the half-0 MMA has read X and Y
+      auto operands = [&](auto full) {
 #pragma unroll
-      for (int o = 0; o < 2; ++o) {
-        const int r8 = er0 + 8 * o;  // first of the 8 rows of this chunk
-        float xk[8], xq[8], ke[8];
-        const unsigned char *kcol = smem + P_RAW_K + 2 * ec;
-        const unsigned char *qcol = smem + P_RAW_Q + 2 * ec;
+        for (int o = 0; o < 2; ++o) {
+          const int r8 = er0 + 8 * o;  // first of the 8 rows of this chunk
+          // pairs of consecutive rows in packed f32x2 registers
+          u64 xk[4], xq[4], ke[4];
+          const unsigned char *kcol = smem + P_RAW_K + 2 * ec;
+          const unsigned char *qcol = smem + P_RAW_Q + 2 * ec;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = r8 + i;
-          const bool valid = r < n;
-          const float kv = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(kcol + 128 * r)) : 0.f;
-          const float qv = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(qcol + 128 * r)) : 0.f;
-          const float e1 = ex2(G[8 * o + i]);           // e^{G_r - P_b} in (0, 1]
-          const float e2 = ex2(bs[eb] - G[8 * o + i]);  // e^{E_b - G_r} in (0, 1]
-          xk[i] = kv * e1;
-          xq[i] = qv * e1;
-          ke[i] = kv * e2;
+          for (int i = 0; i < 8; i += 2) {
+            float kv[2], qv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int r = r8 + i + e;
+              const bool valid = decltype(full)::value || r < n;
+              kv[e] = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(kcol + 128 * r)) : 0.f;
+              qv[e] = valid ? bf16_lo(*reinterpret_cast<const unsigned short *>(qcol + 128 * r)) : 0.f;
+            }
+            const float g0 = G[8 * o + i], g1 = G[8 * o + i + 1];
+            const u64 e1 = pk2(ex2(g0), ex2(g1));                  // e^{G_r - P_b} in (0, 1]
+            const u64 e2 = pk2(ex2(bs[eb] - g0), ex2(bs[eb] - g1));  // e^{E_b - G_r} in (0, 1]
+            const u64 k2 = pk2(kv[0], kv[1]);
+            xk[i / 2] = mul2(k2, e1);
+            xq[i / 2] = mul2(pk2(qv[0], qv[1]), e1);
+            ke[i / 2] = mul2(k2, e2);
+          }
+          *reinterpret_cast<uint4 *>(smem + P_X + mn_off(r8, ec, KH)) = pack8x2(xk);
+          *reinterpret_cast<uint4 *>(smem + P_X + mn_off(64 + r8, ec, KH)) = pack8x2(xq);
+          *reinterpret_cast<uint4 *>(smem + p_y_off(eb) + mn_off(r8, ec, KH)) = pack8x2s(ke, rD);
+          if (eb + 1 < kNumSub)
+            *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 1) + mn_off(r8, ec, KH)) = pack8x2(ke);
+          if (eb + 2 < kNumSub)
+            *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 2) + mn_off(r8, ec, KH)) = pack8x2s(ke, x2);
+          if (eb + 3 < kNumSub)
+            *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 3) + mn_off(r8, ec, KH)) = pack8x2s(ke, x3);
+          // K e^G (beta goes into T's columns), transposed for the w product
+          *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = pack8x2s(xk, pre);
+          *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8x2s(xq, pre);
+          *reinterpret_cast<uint4 *>(gi + I_KHT + op_off(ch, r8, C)) = pack8x2s(ke, suf);
         }
-        *reinterpret_cast<uint4 *>(smem + P_X + mn_off(r8, ec, KH)) = pack8(xk);
-        *reinterpret_cast<uint4 *>(smem + P_X + mn_off(64 + r8, ec, KH)) = pack8(xq);
-        *reinterpret_cast<uint4 *>(smem + p_y_off(eb) + mn_off(r8, ec, KH)) = pack8s(ke, rD);
-        if (eb + 1 < kNumSub)
-          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 1) + mn_off(r8, ec, KH)) = pack8(ke);
-        if (eb + 2 < kNumSub)
-          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 2) + mn_off(r8, ec, KH)) = pack8s(ke, x2);
-        if (eb + 3 < kNumSub)
-          *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 3) + mn_off(r8, ec, KH)) = pack8s(ke, x3);
-        // K e^G (beta goes into T's columns), transposed for the w product
-        *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = pack8s(xk, pre);
-        *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8s(xq, pre);
-        *reinterpret_cast<uint4 *>(gi + I_KHT + op_off(ch, r8, C)) = pack8s(ke, suf);
-      }
+      };
+      if (full_chunk) operands(std::true_type{});
+      else operands(std::false_type{});
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
