@@ -103,7 +103,7 @@ def measured_peaks():
 
 def kernel_source_digest(impl_name: str) -> str:
     fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu",
-             "conv": "kda_conv.cu", "bwd": "kda_bwd.cu"}[impl_name]
+             "conv": "kda_conv.cu", "bwd": "kda_bwd.cu", "bwd_tc": "kda_bwd_tc.cu"}[impl_name]
     path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -461,6 +461,10 @@ def run_ours(args, dist):
         d = device_inputs(x, dev)
         d_o, d_f = u["d_o"].to(dev), u["d_final"].to(dev)
         has_seg = d["segment_ids"] is not None
+        # AUTO: the tensor-core backward where it applies (bf16, K = V = 128,
+        # no segment ids), else the CUDA-core one
+        tc = kda.bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg,
+                                    impl="tc") > 0
         ws = torch.zeros(kda.bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype, has_seg),
                          dtype=torch.uint8, device=dev)
 
@@ -469,7 +473,7 @@ def run_ours(args, dist):
                           initial_state=d["initial_state"], segment_ids=d["segment_ids"],
                           d_final=d_f, workspace=ws, stream=stream)
 
-        steps = min(args.steps, 20)
+        steps = args.steps if tc else min(args.steps, 20)
         times, _ = time_steps(step, steps, args.warmup, stream, flush, dist, clocks)
         ms = dist.max(statistics.mean(times))
         th = w.token_heads
@@ -483,11 +487,15 @@ def run_ours(args, dist):
                "value": whole_job_value(dist.world, w.B * w.T, ms), "steps": steps,
                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                             "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                            "traffic": profiled_traffic("bwd", w.name),
+                            "traffic": profiled_traffic("bwd_tc" if tc else "bwd", w.name),
                             "algorithmic_bytes": nbytes,
-                            "kernel": "bwd_simt_kernel + bwd_reduce_kernel"},
-               # (runs +) the backward kernel + the reduction
-               "gpu_launches": steps * (3 if has_seg else 2)}
+                            "kernel": ("fwd_prep_kernel + fwd_rec_kernel (save) + "
+                                       "bwd_chain_kernel + bwd_grad_kernel") if tc
+                            else "bwd_simt_kernel + bwd_reduce_kernel"},
+               "impl": "tc" if tc else "simt",
+               # tensor cores: prep, recurrence (save), chain, gradients;
+               # CUDA cores: (runs +) the backward kernel + the reduction
+               "gpu_launches": steps * (4 if tc else (3 if has_seg else 2))}
         if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline_backward(w, args.seed, budget_s=args.cpu_seconds / 2)
         return res

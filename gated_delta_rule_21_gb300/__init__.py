@@ -103,6 +103,11 @@ def lib():
         L.kda_chunk_bwd.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
                                     vp, vp, vp, vp, u64, vp]
         L.kda_chunk_bwd.restype = i
+        L.kda_chunk_bwd_workspace_size_for.argtypes = [sp, i, i]
+        L.kda_chunk_bwd_workspace_size_for.restype = u64
+        L.kda_chunk_bwd_ex.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, vp, vp, vp, u64, i, vp]
+        L.kda_chunk_bwd_ex.restype = i
         L.kda_chunk_fwd_scan_workspace_size.argtypes = [sp, i]
         L.kda_chunk_fwd_scan_workspace_size.restype = u64
         L.kda_chunk_fwd_scan_segments.argtypes = [sp, i]
@@ -301,19 +306,26 @@ def chunk_fwd_scan(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state
     return o, fs
 
 
-def bwd_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
-    """Workspace bytes of chunk_bwd for this shape (0 when unsupported)."""
+def bwd_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False,
+                       impl=None) -> int:
+    """Workspace bytes of chunk_bwd for this shape (0 when unsupported):
+    the AUTO choice (impl None) or what ``impl`` ("auto", "simt", "tc")
+    needs."""
     s = make_shape(B, T, H, K, V, dtype)
-    return int(lib().kda_chunk_bwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+    if impl is None:
+        return int(lib().kda_chunk_bwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+    return int(lib().kda_chunk_bwd_workspace_size_for(ctypes.byref(s), int(bool(has_segment_ids)),
+                                                      IMPLS[impl]))
 
 
 def chunk_bwd(q, k, v, g, beta, d_o, scale=None, chunk_size=CHUNK, initial_state=None,
               segment_ids=None, d_final=None, want_d_initial=True, workspace=None,
-              stream=None):
+              stream=None, impl="auto"):
     """Gradient of chunk_fwd on the GPU: given ``d_o`` [B,T,H,V] (dtype of q)
     and ``d_final`` [B,H,K,V] fp32 or None, returns fp32 ``(dq, dk, dv, dg,
     dbeta, d_initial or None)`` of ``sum(d_o * o) + sum(d_final *
-    final_state)``.  Inputs as chunk_fwd."""
+    final_state)``.  Inputs as chunk_fwd; ``impl``: "auto" (the tensor cores
+    where they apply), "tc" or "simt"."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     dev = q.device
@@ -337,18 +349,19 @@ def chunk_bwd(q, k, v, g, beta, d_o, scale=None, chunk_size=CHUNK, initial_state
     dbeta = torch.empty(B, T, H, **f32)
     d_init = torch.empty(B, H, K, V, **f32) if want_d_initial else None
     if workspace is None:
-        n = bwd_workspace_size(B, T, H, K, V, dt, segment_ids is not None)
+        n = bwd_workspace_size(B, T, H, K, V, dt, segment_ids is not None, impl)
         if n == 0:
             raise KdaError(2, "kda_chunk_bwd_workspace_size")
         workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
     s = make_shape(B, T, H, K, V, dt)
-    st = lib().kda_chunk_bwd(
+    st = lib().kda_chunk_bwd_ex(
         ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
         int(chunk_size), _ptr(initial_state), _ptr(segment_ids), _ptr(d_o), _ptr(d_final),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(d_init), _ptr(workspace),
-        int(workspace.numel() * workspace.element_size()), _stream_ptr(stream, dev))
+        int(workspace.numel() * workspace.element_size()), IMPLS[impl],
+        _stream_ptr(stream, dev))
     if st != KDA_OK:
-        raise KdaError(st, "kda_chunk_bwd")
+        raise KdaError(st, "kda_chunk_bwd_ex")
     return dq, dk, dv, dg, dbeta, d_init
 
 

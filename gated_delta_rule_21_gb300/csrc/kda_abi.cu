@@ -335,10 +335,24 @@ kda_status kda_clear_device_status(void *workspace, kda_stream_t stream) {
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids) {
+size_t kda_chunk_bwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
+                                        kda_impl impl) {
   if (check_shape(s) != KDA_OK || !bwd_supported(s->K, s->V)) return 0;
-  return align_up(ws_bytes(s->B, s->T, has_segment_ids != 0), 256) +
-         bwd_scratch_bytes(s->B, s->T, s->H, s->K, s->V);
+  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16,
+                                      has_segment_ids != 0);
+  const size_t simt = align_up(ws_bytes(s->B, s->T, has_segment_ids != 0), 256) +
+                      bwd_scratch_bytes(s->B, s->T, s->H, s->K, s->V);
+  switch (impl) {
+    case KDA_IMPL_SIMT: return simt;
+    case KDA_IMPL_TC:
+    case KDA_IMPL_SPLIT: return tc_ok ? bwd_tc_workspace_bytes(s->B, s->T, s->H) : 0;
+    case KDA_IMPL_AUTO: return tc_ok ? bwd_tc_workspace_bytes(s->B, s->T, s->H) : simt;
+  }
+  return 0;
+}
+
+size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids) {
+  return kda_chunk_bwd_workspace_size_for(s, has_segment_ids, KDA_IMPL_AUTO);
 }
 
 kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const void *v,
@@ -347,6 +361,18 @@ kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const
                          const void *d_o, const float *d_final, float *dq, float *dk,
                          float *dv, float *dg, float *dbeta, float *d_initial,
                          void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+  return kda_chunk_bwd_ex(s, q, k, v, g, beta, scale, chunk_size, initial_state, segment_ids,
+                          d_o, d_final, dq, dk, dv, dg, dbeta, d_initial, workspace,
+                          workspace_bytes, KDA_IMPL_AUTO, stream);
+}
+
+kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, float scale, int chunk_size,
+                            const float *initial_state, const int32_t *segment_ids,
+                            const void *d_o, const float *d_final, float *dq, float *dk,
+                            float *dv, float *dg, float *dbeta, float *d_initial,
+                            void *workspace, size_t workspace_bytes, kda_impl impl,
+                            kda_stream_t stream) {
   kda_status st = check_shape(s);
   if (st != KDA_OK) return st;
   if (!bwd_supported(s->K, s->V)) return KDA_ERR_UNSUPPORTED;
@@ -354,12 +380,20 @@ kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const
     return KDA_ERR_INVALID_ARG;
   if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
   if (!(scale == scale)) return KDA_ERR_INVALID_ARG;
+  if (impl != KDA_IMPL_AUTO && impl != KDA_IMPL_SIMT && impl != KDA_IMPL_TC &&
+      impl != KDA_IMPL_SPLIT)
+    return KDA_ERR_INVALID_ARG;
   const void *ptrs[] = {q, k, v, g, beta, d_o, initial_state, d_final, segment_ids,
                         dq, dk, dv, dg, dbeta, d_initial};
   for (const void *ptr : ptrs)
     if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
   const bool has_seg = segment_ids != nullptr;
-  const size_t need = kda_chunk_bwd_workspace_size(s, has_seg ? 1 : 0);
+  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16, has_seg);
+  if ((impl == KDA_IMPL_TC || impl == KDA_IMPL_SPLIT) && !tc_ok) return KDA_ERR_UNSUPPORTED;
+  const bool use_tc = impl == KDA_IMPL_TC || impl == KDA_IMPL_SPLIT ||
+                      (impl == KDA_IMPL_AUTO && tc_ok);
+  const size_t need = kda_chunk_bwd_workspace_size_for(s, has_seg ? 1 : 0,
+                                                       use_tc ? KDA_IMPL_TC : KDA_IMPL_SIMT);
   if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
 
@@ -393,6 +427,9 @@ kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const
     p.runs.total_runs = &reinterpret_cast<WsHeader *>(ws)->total_runs;
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc)
+    return from_cuda(launch_bwd_tc(p, workspace, workspace_bytes, dq, dk, dg, dbeta,
+                                   &reinterpret_cast<WsHeader *>(ws)->status, cs));
   if (has_seg) {
     // Runs; dv = 0 on padding; d_initial = d_final (or 0) for rows without a run.
     cudaError_t e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, dv, 0,

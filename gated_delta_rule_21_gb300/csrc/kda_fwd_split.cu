@@ -32,35 +32,13 @@
 
 #include "kda_f32x2.cuh"
 #include "kda_internal.cuh"
+#include "kda_split.cuh"
 #include "kda_tc_common.cuh"
 
 namespace kda {
+using namespace split;
 namespace {
 using namespace tc;
-
-constexpr int C = kChunk;
-constexpr int KD = 128;
-constexpr int VD = 128;
-constexpr int VT = 32;
-
-// ---- one workspace item (per row, chunk, head) ----------------------------
-// Each region is already in the shared-memory operand layout the recurrence
-// kernel's MMAs read, so a stage is a plain bulk copy of the item.
-constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: MN-major, 128 rows x Kd 128 channels
-constexpr uint32_t I_AQK = 32768;     // A_qk: K-major, 64 rows, Kd 64
-constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: K-major, 128 channels x Kd 64 rows
-constexpr uint32_t I_U = 57344;       // u bf16, 4 tiles of 32 columns, see u_off
-constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
-constexpr uint32_t ITEM_BYTES = 74240;     // 72.5 KiB, 256-byte aligned
-constexpr size_t WS_ITEMS_OFF = 1024;      // after the workspace header
-
-// Byte offset of u's 8 columns c .. c + 7 (c a multiple of 8 within the
-// 32-column tile vt) of row r: each tile is [column group of 8][row][8]
-// bf16, so the 32 rows a warp reads for one column group are 512
-// contiguous bytes (no bank conflicts), and a tile is one 4 KiB block.
-__device__ __forceinline__ uint32_t u_off(int vt, int c, int r) {
-  return (uint32_t)(vt * 4096 + (c >> 3) * 1024 + r * 16);
-}
 
 // ---- prep kernel --------------------------------------------------------------
 // Two CTAs of 256 threads per SM, each working on its own item, so that one
@@ -138,55 +116,6 @@ __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
     pp = i < 3 ? i : i - 3;
   }
 }
-
-// Chunk items: with segment ids, chunk k of the concatenated runs of all rows
-// (run i of row b owns chunks chunk_row_offsets[b] + run_chunk_base[b*T+i] ..);
-// without them, row b owns chunks b*n_chunks ... (b+1)*n_chunks - 1.
-struct ChunkTable {
-  const int32_t *run_chunk_base;     // [B*T] or nullptr (no segment ids)
-  const int32_t *chunk_row_offsets;  // [B+1]
-  const int2 *coords;                // [B*T]: {b*T + first token, tokens}, row b's
-                                     // chunks from b*T on
-  const uint32_t *total_chunks;      // device count
-  uint32_t capacity;                 // chunk items the workspace holds
-  int n_chunks_row;                  // chunks per row without segment ids
-  int n_rows;                        // B
-  int report_overflow;               // set KDA_DEVICE_WORKSPACE on overflow
-};
-
-__device__ __forceinline__ uint32_t total_chunk_count(const ChunkTable &ct, int B) {
-  return ct.run_chunk_base ? *ct.total_chunks : (uint32_t)B * ct.n_chunks_row;
-}
-
-// First token and end of chunk k, and its row.
-__device__ __forceinline__ void chunk_of(const ChunkTable &ct, int T, uint32_t k, int &b,
-                                         int &t0, int &end) {
-  if (!ct.run_chunk_base) {
-    b = (int)(k / (uint32_t)ct.n_chunks_row);
-    t0 = (int)(k % (uint32_t)ct.n_chunks_row) * C;
-    end = T;
-    return;
-  }
-  int lo = 0, hi = ct.n_rows;  // the row: chunk_row_offsets[lo] <= k < [lo + 1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((uint32_t)ct.chunk_row_offsets[mid] <= k) lo = mid; else hi = mid;
-  }
-  const int2 e = ct.coords[(size_t)lo * T + (k - (uint32_t)ct.chunk_row_offsets[lo])];
-  b = lo;
-  t0 = e.x - b * T;
-  end = t0 + e.y;
-}
-
-__device__ __forceinline__ void st_g16(unsigned char *g, uint32_t off, const float (&v)[8]) {
-  uint4 w;
-  w.x = pack_bf16(v[0], v[1]);
-  w.y = pack_bf16(v[2], v[3]);
-  w.z = pack_bf16(v[4], v[5]);
-  w.w = pack_bf16(v[6], v[7]);
-  *reinterpret_cast<uint4 *>(g + off) = w;
-}
-
 
 // One 16 x 16 block product on the CUDA cores by one warp (e = lane: rows
 // e / 4 and e / 4 + 8, four columns each): dst = sgn X Y + add_sgn add.
@@ -311,6 +240,8 @@ __global__ void __launch_bounds__(PT, 2)
     mma_phase ^= 1u;
   };
 
+  // Items for the backward also carry T, A_kk and K e^G.
+  const bool bwd_items = ct.item_stride == ITEM_BYTES_BWD;
   const uint32_t n_chunk_items = total_chunk_count(ct, p.B);
   if (n_chunk_items > ct.capacity && ct.report_overflow && tid == 0 && blockIdx.x == 0)
     set_status(p.status, KDA_DEVICE_WORKSPACE);  // the items cannot hold every chunk
@@ -372,7 +303,7 @@ __global__ void __launch_bounds__(PT, 2)
     const uint32_t next = item + gridDim.x;
     const bool has_next = next < n_items;
     const Coords nxt = has_next ? item_coords(next) : cur;
-    unsigned char *gi = items + (size_t)item * ITEM_BYTES;
+    unsigned char *gi = items + (size_t)item * ct.item_stride;
     if (tid < C) sBeta[tid] = beta_next;
 
     for (int half = 0; half < 2; ++half) {
@@ -460,7 +391,11 @@ __global__ void __launch_bounds__(PT, 2)
           if (eb + 3 < kNumSub)
             *reinterpret_cast<uint4 *>(smem + p_y_off(eb + 3) + mn_off(r8, ec, KH)) = pack8x2s(ke, x3);
           // K e^G (beta goes into T's columns), transposed for the w product
-          *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = pack8x2s(xk, pre);
+          {
+            const uint4 kt = pack8x2s(xk, pre);
+            *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = kt;
+            if (bwd_items) *reinterpret_cast<uint4 *>(gi + I_KT + op_off(ch, r8, C)) = kt;
+          }
           *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8x2s(xq, pre);
           *reinterpret_cast<uint4 *>(gi + I_KHT + op_off(ch, r8, C)) = pack8x2s(ke, suf);
         }
@@ -517,13 +452,15 @@ __global__ void __launch_bounds__(PT, 2)
           if (!is_q) {
             const float br = sBeta[r];
             float4 *dst = reinterpret_cast<float4 *>(sAkk + r * LDF + j0);
+            float4 *raw = reinterpret_cast<float4 *>(gi + I_AKK + (r * C + j0) * 4);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               float a[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                a[i] = (j0 + 4 * q4 + i < r) ? br * v[e][4 * q4 + i] : 0.f;
-              dst[q4] = make_float4(a[0], a[1], a[2], a[3]);
+                a[i] = (j0 + 4 * q4 + i < r) ? v[e][4 * q4 + i] : 0.f;
+              if (bwd_items) raw[q4] = make_float4(a[0], a[1], a[2], a[3]);
+              dst[q4] = make_float4(br * a[0], br * a[1], br * a[2], br * a[3]);
             }
           } else {
             float a0[8], a1[8];
@@ -610,6 +547,11 @@ __global__ void __launch_bounds__(PT, 2)
         const float4 a = src[0], b4 = src[1];
         float t8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
         const bool upper = (j8 >> 4) > (r >> 4);
+        if (bwd_items) {  // T itself, for the backward
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = upper ? 0.f : t8[i];
+          st_g16(gi, I_T + op_off(r, j8, C), t8);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) t8[i] = upper ? 0.f : t8[i] * sBeta[j8 + i];
         st_bf16x8(smem, P_TB + op_off(r, j8, C), t8);
@@ -733,6 +675,9 @@ struct ScanParams {
   int n_segs, cps;
   float *maps;
   float *starts;
+  // Save pass for the backward (MODE = 2): per (chunk, head), at the item's
+  // index, SV_BYTES holding the state entering the chunk and U (bf16).
+  unsigned char *save;
 };
 
 constexpr uint32_t S_WQ = I_WQ, S_AQK = I_AQK, S_KHT = I_KHT, S_U = I_U;
@@ -768,7 +713,10 @@ struct RecLayout {
 // D2 is issued before the o product, so the state update, and with it the
 // next chunk's first MMA, waits only for the products on the serial chain;
 // the o product runs on the tensor pipe while the CUDA cores update S.
-template <int VTR, int NST, int MAP>
+// MODE 0: the forward; 1: the scan's map pass (see ScanParams); 2: the
+// backward's save pass (no outputs; each chunk's entering state and U are
+// written to sc.save).
+template <int VTR, int NST, int MODE>
 __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct,
                    const ScanParams sc) {
@@ -870,6 +818,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
 
   float S[CPT];  // S[key row L][col0 .. col0 + CPT - 1], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
+  constexpr bool MAP = MODE == 1, SAVE = MODE == 2;
   const int seg_units = MAP ? sc.n_segs - 1 : sc.n_segs;
   const uint32_t n_units =
       !fits ? 0u
@@ -909,7 +858,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     const bool m_tile = MAP && vt >= NVT_V;
     const int vt_u = m_tile ? 0 : vt;
     auto item_ptr = [&](int c) {
-      return items + ((size_t)(cbase + c) * H + h) * ITEM_BYTES;
+      return items + ((size_t)(cbase + c) * H + h) * ct.item_stride;
     };
     // state entering the run (or segment); S^T operand (MN-major: v contiguous)
     const float *s_src = nullptr;
@@ -960,6 +909,16 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
       const unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
       const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
       const uint32_t d1 = Lay::TM_D1 + (uint32_t)VTR * (uint32_t)(c & 1);
+      unsigned char *sv = SAVE ? sc.save + ((size_t)(cbase + c) * H + h) * SV_BYTES : nullptr;
+      if (SAVE) {  // the state entering this chunk
+#pragma unroll
+        for (int e = 0; e < CPT / 8; ++e) {
+          float t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = S[8 * e + i];
+          st_g16(sv, SV_S + op_off(L, vc0 + col0 + 8 * e, KD), t8);
+        }
+      }
       // ---- P10: wait for D1 = [w ; Q e^G] S of this chunk (every thread
       //      waits on the barrier itself; an abort is seen after the next
       //      block barrier, which also keeps the phases in step)
@@ -984,6 +943,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) a[i] = uu[i] - v[8 * e + i];
           st_bf16x8(smem, Lay::UT + mn_off(col, r, C), a);
+          if (SAVE) st_g16(sv, SV_U + op_off(r, vc0 + col, KD), a);
         }
       }
       fence_proxy_async();
@@ -996,8 +956,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
         tc_fence_after();
         mma_group(tmem + Lay::TM_D2, sstg + S_KHT, sb + Lay::UT, C, VTR, false, 0, 1);
         commit(s_bar, c_s);
-        if (!MAP) mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
-        commit(o_bar, c_o);  // the map pass has no o product: this tracks D2
+        if (MODE == 0) mma_group(tmem + d1, sstg + S_AQK - 8192, sb + Lay::UT, C, VTR, true, 0, 1);
+        commit(o_bar, c_o);  // without the o product this tracks D2
       }
       wait_bar(s_bar, n_s);
       tc_fence_after();
@@ -1044,8 +1004,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
         }
         const int r = L - 64;
         float v[CPT];
-        if (!MAP) tmem_ld_cpt(tq + d1 + col0, v);
-        if (!MAP && r < n) {
+        if (MODE == 0) tmem_ld_cpt(tq + d1 + col0, v);
+        if (MODE == 0 && r < n) {
           uint4 *dst = reinterpret_cast<uint4 *>(
               static_cast<__nv_bfloat16 *>(p.o) + ((tok0 + r) * H + h) * p.V + vc0 + col0);
 #pragma unroll
@@ -1067,7 +1027,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     if (MAP)
       s_dst = sc.maps + ((((size_t)b * (sc.n_segs - 1) + seg) * H + h) * KD + L) * (VD + KD) +
               vc0 + col0;
-    else if (ulast && p.final_state)
+    else if (!SAVE && ulast && p.final_state)
       s_dst = p.final_state + (((size_t)b * H + h) * KD + L) * p.V + vc0 + col0;
     if (s_dst) {
       float4 *dst = reinterpret_cast<float4 *>(s_dst);
@@ -1169,8 +1129,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
-              uint64_t cols, uint64_t rows, uint32_t box_cols, CUtensorMapSwizzle swz) {
+}  // namespace
+
+bool split::make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                     uint64_t cols, uint64_t rows, uint32_t box_cols, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -1183,16 +1145,12 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
          CUDA_SUCCESS;
 }
 
-}  // namespace
-
-namespace {
 // Byte offset of the first item: after the header (no segment ids) or after
 // the run list and the chunk tables (segment ids).
-size_t items_offset(int B, int T, bool has_seg) {
+size_t split::items_offset(int B, int T, bool has_seg) {
   return has_seg ? align_up(ws_bytes(B, T, true) + ws_chunk_tables_bytes(B, T), 1024)
                  : WS_ITEMS_OFF;
 }
-}  // namespace
 
 size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row) {
   const size_t nc = ((size_t)T + C - 1) / C;
@@ -1263,6 +1221,59 @@ int fit_tile(long units, int cols) {
   if (units * (cols / 64) <= sms) return 64;
   return 128;
 }
+
+// The prep kernel over every item of `ct` (two CTAs per SM).
+cudaError_t launch_prep(const FwdParams &p, unsigned char *items, const ChunkTable &ct,
+                        cudaStream_t stream) {
+  const uint64_t rows = (uint64_t)p.B * p.T;
+  CUtensorMap mq, mk, mg, mv;
+  // q, k, g unswizzled: the prep kernel's channel owners read one row's 32
+  // consecutive channels per warp (128 contiguous bytes of g, 64 of q or k)
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
+      !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
+      !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, 32, sw) ||
+      !make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * VD, rows, 8,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const long sms = num_sms();
+  cudaError_t e = cudaFuncSetAttribute(fwd_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_ALLOC);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fwd_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
+  const int g1 = (int)(n_items < 2 * sms ? n_items : 2 * sms);  // two CTAs per SM
+  fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+// The chunk table of a call: items from `ioff` on, `stride` bytes each.
+ChunkTable make_table(const FwdParams &p, unsigned char *ws, size_t ioff, size_t bytes,
+                      uint32_t stride, bool has_seg, bool with_fallback) {
+  ChunkTable ct;
+  ct.report_overflow = with_fallback ? 0 : 1;
+  ct.n_chunks_row = (p.T + C - 1) / C;
+  ct.n_rows = p.B;
+  ct.item_stride = stride;
+  ct.capacity = (uint32_t)((bytes - ioff) / ((size_t)p.H * stride));
+  if (has_seg) {
+    ct.run_chunk_base = reinterpret_cast<const int32_t *>(ws + ws_bytes(p.B, p.T, true));
+    ct.chunk_row_offsets = reinterpret_cast<const int32_t *>(
+        ws + ws_bytes(p.B, p.T, true) + align_up(sizeof(int32_t) * (size_t)p.B * p.T, 256));
+    ct.total_chunks = &reinterpret_cast<const WsHeader *>(ws)->total_chunks;
+    ct.coords = reinterpret_cast<const int2 *>(ws + ws_chunk_coords_offset(p.B, p.T));
+  } else {
+    ct.run_chunk_base = nullptr;
+    ct.chunk_row_offsets = nullptr;
+    ct.coords = nullptr;
+    ct.total_chunks = nullptr;
+  }
+  return ct;
+}
 }  // namespace
 
 cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t workspace_bytes,
@@ -1286,46 +1297,10 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   const size_t ioff = items_offset(p.B, p.T, has_seg);
   if (workspace_bytes < ioff + (size_t)p.H * ITEM_BYTES) return cudaErrorInvalidValue;
   unsigned char *items = ws + ioff;
-  ChunkTable ct;
-  ct.report_overflow = with_fallback ? 0 : 1;
-  ct.n_chunks_row = (p.T + C - 1) / C;
-  ct.n_rows = p.B;
-  ct.capacity = (uint32_t)((workspace_bytes - ioff) / ((size_t)p.H * ITEM_BYTES));
-  if (has_seg) {
-    ct.run_chunk_base = reinterpret_cast<const int32_t *>(ws + ws_bytes(p.B, p.T, true));
-    ct.chunk_row_offsets = reinterpret_cast<const int32_t *>(
-        ws + ws_bytes(p.B, p.T, true) + align_up(sizeof(int32_t) * (size_t)p.B * p.T, 256));
-    ct.total_chunks = &reinterpret_cast<const WsHeader *>(ws)->total_chunks;
-    ct.coords = reinterpret_cast<const int2 *>(ws + ws_chunk_coords_offset(p.B, p.T));
-  } else {
-    ct.run_chunk_base = nullptr;
-    ct.chunk_row_offsets = nullptr;
-    ct.coords = nullptr;
-    ct.total_chunks = nullptr;
-  }
-  const uint64_t rows = (uint64_t)p.B * p.T;
-  CUtensorMap mq, mk, mg, mv;
-  // q, k, g unswizzled: the prep kernel's channel owners read one row's 32
-  // consecutive channels per warp (128 contiguous bytes of g, 64 of q or k)
-  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
-      !make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * KD, rows, 64, sw) ||
-      !make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)p.H * KD, rows, 32, sw) ||
-      !make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.H * VD, rows, 8,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_prep_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_ALLOC);
+  const ChunkTable ct = make_table(p, ws, ioff, workspace_bytes, ITEM_BYTES, has_seg, with_fallback);
+  cudaError_t e = launch_prep(p, items, ct, stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fwd_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  const long n_items = (long)ct.capacity * p.H;  // upper bound of the real count
-  const int g1 = (int)(n_items < 2 * sms ? n_items : 2 * sms);  // two CTAs per SM
-  fwd_prep_kernel<<<g1 > 0 ? g1 : 1, PT, P_ALLOC, stream>>>(p, items, ct, mq, mk, mg, mv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ScanParams sc = {0, 0, nullptr, nullptr};
+  ScanParams sc = {0, 0, nullptr, nullptr, nullptr};
   if (scan_segs > 0) {
     // chunk-parallel scan: map pass, combine, finish pass (see ScanParams)
     const int nc = ct.n_chunks_row;
@@ -1358,6 +1333,42 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
   pf.gate_chunks = ct.total_chunks;
   pf.gate_capacity = ct.capacity;
   return launch_fwd_tc(pf, stream);
+}
+
+// ---- the forward pass the tensor-core backward starts from ------------------
+size_t split::bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg) {
+  if (has_seg) return 0;  // rows without segment ids only
+  const size_t chunks = (size_t)B * (((size_t)T + C - 1) / C);
+  return items_offset(B, T, false) + chunks * H * ((size_t)ITEM_BYTES_BWD + SV_BYTES);
+}
+
+// Items of ITEM_BYTES_BWD (the forward's, plus T, A_kk and K e^G), then the
+// recurrence in its save mode: the state entering every chunk and U, no o
+// and no final state.
+cudaError_t split::launch_fwd_for_bwd(const FwdParams &p_in, void *workspace,
+                                      size_t workspace_bytes, BwdLayout *out,
+                                      cudaStream_t stream) {
+  if (p_in.runs.runs != nullptr || !fwd_split_supported(p_in.K, p_in.V, true, false, 0))
+    return cudaErrorNotSupported;
+  const size_t need = bwd_tc_workspace_bytes(p_in.B, p_in.T, p_in.H, false);
+  if (workspace_bytes < need) return cudaErrorInvalidValue;
+  FwdParams p = p_in;
+  p.v_tile = fit_tile((long)p.B * p.H, VD);
+  p.n_vtiles = VD / p.v_tile;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  const size_t ioff = items_offset(p.B, p.T, false);
+  const size_t n_items = (size_t)p.B * ((p.T + C - 1) / C) * p.H;
+  const size_t items_end = ioff + n_items * ITEM_BYTES_BWD;
+  BwdLayout lay;
+  lay.items = ws + ioff;
+  lay.saves = ws + items_end;
+  lay.ct = make_table(p, ws, ioff, items_end, ITEM_BYTES_BWD, false, false);
+  cudaError_t e = launch_prep(p, lay.items, lay.ct, stream);
+  if (e != cudaSuccess) return e;
+  const ScanParams sc = {0, 0, nullptr, nullptr, lay.saves};
+  e = launch_rec_tile<2>(p, lay.items, lay.ct, false, sc, stream);
+  if (e == cudaSuccess && out) *out = lay;
+  return e;
 }
 
 }  // namespace kda

@@ -199,6 +199,51 @@ __device__ __forceinline__ void mma_group(uint32_t d_tmem, uint32_t a_addr,
   }
 }
 
+// An operand in shared memory with explicit strides, for layouts other than
+// the two above: `lbo` is the byte stride between core matrices along K and
+// `sbo` between groups of 8 rows (K-major) or 8 MN elements (MN-major).  A
+// K-major tile stored with op_off(row, k, Kd), read with lbo = Kd*16,
+// sbo = 128 and the transpose bit, is the operand whose MN index is `k`
+// and whose K index is `row` (its transpose); the 64-row TMA boxes of 8
+// columns ([column group][row][8]) are a K-major operand over rows with
+// lbo = 1024, sbo = 128.
+struct Opnd {
+  uint32_t addr, lbo, sbo;
+};
+
+__device__ __forceinline__ uint64_t smem_desc_ls(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// D (M = 128, N columns) (+)= A B^T over `ksteps` steps of K = 16; each step
+// moves both operands two core matrices along K.  ta / tb: MN-major.
+__device__ __forceinline__ void mma_k(uint32_t d_tmem, Opnd a, int ta, Opnd b, int tb,
+                                      int ksteps, int N, bool accumulate) {
+  const uint32_t id = idesc_bf16(128, N, ta, tb);
+  for (int s = 0; s < ksteps; ++s)
+    mma_bf16(d_tmem, smem_desc_ls(a.addr + 2u * a.lbo * (uint32_t)s, a.lbo, a.sbo),
+             smem_desc_ls(b.addr + 2u * b.lbo * (uint32_t)s, b.lbo, b.sbo), id,
+             (accumulate || s > 0) ? 1u : 0u);
+}
+
+// 8 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -237,6 +282,17 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t t0, uint32_t t1, float (&v)
   for (int i = 0; i < 16; ++i) {
     v[i] = __uint_as_float(r[i]);
     w[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  float a[16], b[16];
+  tmem_ld16x2(taddr, taddr + 16, a, b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = a[i];
+    v[16 + i] = b[i];
   }
 }
 

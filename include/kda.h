@@ -376,13 +376,24 @@ KDA_API kda_status kda_chunk_fwd_host(const kda_shape *s, const void *q, const v
  *   d_initial  [B,H,K,V] or NULL (not wanted): the gradient with respect to
  *              the initial state (a zero one when initial_state is NULL).
  * Padding tokens get zero gradients; a row without a run passes d_final to
- * d_initial.  Supports K and V in {32, 64, 128}.  The first
- * implementation runs on the CUDA cores in fp32: it recomputes the states
- * from checkpoints every 8 tokens and walks each (run, head, 32-column value
- * tile) backwards.  workspace: kda_chunk_bwd_workspace_size bytes,
- * 256-byte aligned, zero-filled before first use, reusable; it holds the
- * run list, the checkpoints and per-tile partial sums.  Errors as
- * kda_chunk_fwd; the call is asynchronous on `stream`.
+ * d_initial.  Supports K and V in {32, 64, 128}.
+ * Two implementations; kda_chunk_bwd runs KDA_IMPL_AUTO (see _ex):
+ *   tensor cores (KDA_IMPL_TC; KDA_IMPL_SPLIT names the same path): bf16
+ *     q/k/v/d_o, K = V = 128, segment_ids NULL.  The chunked backward: the
+ *     forward's per-chunk prep and its recurrence, which saves the state
+ *     entering every chunk and U; the reverse chain of the state gradient
+ *     (which saves dS' and dU per chunk); and a per-chunk kernel that forms
+ *     every gradient of the chunk's tokens on tcgen05.  Workspace: the
+ *     chunk items and saves, 208.5 KiB per (chunk, head) plus 1 KiB
+ *     (874 MB for B=1, T=8192, H=32).
+ *   CUDA cores (KDA_IMPL_SIMT): every supported shape, fp32.  It recomputes
+ *     the states from checkpoints every 8 tokens and walks each (run, head,
+ *     32-column value tile) backwards; its workspace holds the run list, the
+ *     checkpoints and per-tile partial sums.
+ * workspace: kda_chunk_bwd_workspace_size bytes (the AUTO choice), 256-byte
+ * aligned, zero-filled before first use, reusable; its first word is the
+ * device status word.  Errors as kda_chunk_fwd; the call is asynchronous
+ * on `stream`.
  */
 KDA_API size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids);
 KDA_API kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k,
@@ -392,6 +403,30 @@ KDA_API kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *
                                  const float *d_final, float *dq, float *dk, float *dv,
                                  float *dg, float *dbeta, float *d_initial, void *workspace,
                                  size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Workspace bytes kda_chunk_bwd_ex needs for `impl`: KDA_IMPL_AUTO the
+ * tensor-core size where that path applies, else the CUDA-core size;
+ * KDA_IMPL_TC / KDA_IMPL_SPLIT 0 where the tensor-core path does not apply;
+ * 0 for an invalid or unsupported shape.
+ */
+KDA_API size_t kda_chunk_bwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
+                                                kda_impl impl);
+/*
+ * kda_chunk_bwd with an explicit implementation: KDA_IMPL_AUTO (tensor
+ * cores where they apply, else CUDA cores), KDA_IMPL_SIMT, or KDA_IMPL_TC /
+ * KDA_IMPL_SPLIT (KDA_ERR_UNSUPPORTED where the tensor-core path does not
+ * apply); another value is KDA_ERR_INVALID_ARG.  The workspace must hold
+ * kda_chunk_bwd_workspace_size_for(s, segment_ids != NULL, impl) bytes.
+ */
+KDA_API kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    float scale, int chunk_size, const float *initial_state,
+                                    const int32_t *segment_ids, const void *d_o,
+                                    const float *d_final, float *dq, float *dk, float *dv,
+                                    float *dg, float *dbeta, float *d_initial,
+                                    void *workspace, size_t workspace_bytes, kda_impl impl,
+                                    kda_stream_t stream);
 
 /*
  * Test hook for failure detection (no counterpart in the pages): enqueues

@@ -203,9 +203,22 @@ def test_status_calls_reject_null(L):
 
 def test_backward_workspace_size_and_argument_checks(L):
     # supported: K in {32, 64, 128}, V a multiple of 32
-    n = kda.bwd_workspace_size(1, 8192, 32, 128, 128)
+    n = kda.bwd_workspace_size(1, 8192, 32, 128, 128, impl="simt")
     nck, n_vt, nK, nB = 8192 // 8, 4, 8192 * 32 * 128, 8192 * 32
     assert n == 256 + 152 * nck * 128 * 32 * 4 + 3 * n_vt * nK * 4 + n_vt * nB * 4
+    # the tensor-core path (AUTO for bf16, K = V = 128, no segment ids): the
+    # header, then per (chunk, head) an item of 112.5 KiB and 96 KiB of saves
+    tc = kda.bwd_workspace_size(1, 8192, 32, 128, 128, impl="tc")
+    assert tc == 1024 + 128 * 32 * (115200 + 98304)
+    assert kda.bwd_workspace_size(1, 8192, 32, 128, 128) == tc
+    assert kda.bwd_workspace_size(1, 8192, 32, 128, 128, impl="auto") == tc
+    assert kda.bwd_workspace_size(1, 100, 2, 128, 128, torch.float32, impl="tc") == 0
+    assert kda.bwd_workspace_size(1, 100, 2, 64, 64, impl="tc") == 0
+    assert kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="tc") == 0
+    assert kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True) == \
+        kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="simt")
+    assert kda.bwd_workspace_size(1, 100, 2, 64, 64) == \
+        kda.bwd_workspace_size(1, 100, 2, 64, 64, impl="simt")
     assert kda.bwd_workspace_size(1, 100, 2, 64, 64, has_segment_ids=True) > \
         kda.bwd_workspace_size(1, 100, 2, 64, 64)
     assert kda.bwd_workspace_size(1, 0, 2, 128, 128) == 0
@@ -230,5 +243,20 @@ def test_backward_workspace_size_and_argument_checks(L):
     assert call(d_o=FAKE + 4) == 3             # misaligned
     assert call(nbytes=nb - 1) == 4            # small workspace
     assert call(ws=FAKE + 16) == 3          # workspace not 256-byte aligned
+    # explicit implementations
+    def call_ex(impl, shape=(1, 64, 2, 128, 128, 1), seg=None, nbytes=None):
+        s2 = kda.kda_shape(*shape)
+        nbx = nb if nbytes is None else nbytes
+        return L.kda_chunk_bwd_ex(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                  vp(FAKE), 0.1, 64, None, None if seg is None else vp(seg),
+                                  vp(FAKE), None, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                  vp(FAKE), None, vp(FAKE), nbx, impl, None)
+    assert call_ex(7) == 1                                      # unknown impl
+    assert call_ex(2, shape=(1, 64, 2, 64, 64, 1)) == 2          # TC: K, V
+    assert call_ex(2, shape=(1, 64, 2, 128, 128, 0)) == 2        # TC: fp32 inputs
+    assert call_ex(2, seg=FAKE) == 2                             # TC: segment ids
+    assert call_ex(2, nbytes=nb - 1) == 4                        # TC: small workspace
+    simt_nb = kda.bwd_workspace_size(1, 64, 2, 128, 128, impl="simt")
+    assert call_ex(1, nbytes=simt_nb - 1) == 4                   # SIMT: its own size
     s48 = kda.kda_shape(1, 64, 2, 128, 48, 1)
     assert L.kda_chunk_bwd_workspace_size(ctypes.byref(s48), 0) == 0

@@ -1,7 +1,8 @@
-"""GPU parity of the backward (kda_chunk_bwd, through the C ABI) against the
-fp64 backward oracle on the same seeded inputs and upstream gradients, for
-every gradient, on fixed and packed shapes, all supported (K, V), and heads
-sampled from the B1 H32 T8192 workload.
+"""GPU parity of the CUDA-core backward (kda_chunk_bwd_ex with KDA_IMPL_SIMT,
+through the C ABI) against the fp64 backward oracle on the same seeded
+inputs and upstream gradients, for every gradient, on fixed and packed
+shapes, all supported (K, V), and heads sampled from the B1 H32 T8192
+workload.  The tensor-core backward has its own file (test_bwd_tc.py).
 
 Tolerance: the kernel computes in fp32 from the same (bf16 or fp32) input
 values the oracle upcasts exactly, so the difference is fp32 rounding only
@@ -22,14 +23,15 @@ pytestmark = pytest.mark.gpu
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "d_initial")
 
 
-def _run_both(w, seed=0, heads=None):
+def _run_both(w, seed=0, heads=None, impl="simt"):
     import gated_delta_rule_21_gb300 as kda
     x = ki.make_inputs(w, seed=seed)
     u = ki.make_upstream_grads(w, seed=seed)
     got = kda.chunk_bwd(to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["g"]),
                         to_dev(x["beta"]), to_dev(u["d_o"]), scale=x["scale"],
                         initial_state=to_dev(x["initial_state"]),
-                        segment_ids=to_dev(x["segment_ids"]), d_final=to_dev(u["d_final"]))
+                        segment_ids=to_dev(x["segment_ids"]), d_final=to_dev(u["d_final"]),
+                        impl=impl)
     torch.cuda.synchronize()
     got = [t.cpu().numpy() for t in got]
     if heads is not None:   # heads are independent problems: the oracle takes a few
@@ -103,12 +105,14 @@ def test_backward_is_deterministic_and_workspace_reusable():
                            segments=[40, 60, 50])
     x = ki.make_inputs(w, seed=5)
     u = ki.make_upstream_grads(w, seed=5)
-    ws = torch.zeros(kda.bwd_workspace_size(1, 150, 2, 128, 128, torch.bfloat16, True),
+    ws = torch.zeros(kda.bwd_workspace_size(1, 150, 2, 128, 128, torch.bfloat16, True,
+                                            impl="simt"),
                      dtype=torch.uint8, device="cuda")
     args = (to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["g"]), to_dev(x["beta"]),
             to_dev(u["d_o"]))
     kw = dict(scale=x["scale"], initial_state=to_dev(x["initial_state"]),
-              segment_ids=to_dev(x["segment_ids"]), d_final=to_dev(u["d_final"]), workspace=ws)
+              segment_ids=to_dev(x["segment_ids"]), d_final=to_dev(u["d_final"]), workspace=ws,
+              impl="simt")
     a = kda.chunk_bwd(*args, **kw)
     b = kda.chunk_bwd(*args, **kw)
     for s, t in zip(a, b):
