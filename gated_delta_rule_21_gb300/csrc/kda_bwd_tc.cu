@@ -327,11 +327,14 @@ constexpr uint32_t DGAM = BETA + 256;    // dgam, 128 fp32
 constexpr uint32_t DB = DGAM + 512;      // dbeta parts [3][64] fp32
 constexpr uint32_t GP = DB + 768;        // dG half sums [2][128] fp32
 constexpr uint32_t GCP = GP + 1024;      // sum_r dK^ K^ halves [2][128] fp32
-constexpr uint32_t BAR = GCP + 1024;     // load, mma
-constexpr uint32_t SLOT = BAR + 16;
+constexpr uint32_t BAR = GCP + 1024;     // load (phase A inputs), load (the rest), mma
+constexpr uint32_t SLOT = BAR + 24;
 constexpr uint32_t ABORT = SLOT + 4;
 constexpr uint32_t ALLOC = ABORT + 12 + 1024;
-constexpr uint32_t LOAD_TX = SV_BYTES + 16384 * 2 + 8192 + 16384 + 32768 + 16384 * 2;
+// two load groups: what the first products and the cumsum read (saves, d_o,
+// g), then what the later phases read (v, T, K e^G, q, k)
+constexpr uint32_t LOAD1_TX = SV_BYTES + 16384 + 32768;
+constexpr uint32_t LOAD2_TX = 16384 + 8192 + 16384 + 16384 * 2;
 // after the first products
 constexpr uint32_t DAQ = 0;              // scale dO U^T (j <= r), op_off(r, j, 64)
 constexpr uint32_t DAK = 8192;           // diag(beta) dL, op_off(r, j, 64)
@@ -351,6 +354,7 @@ constexpr uint32_t OYK = OYQ + 16384;
 __host__ __device__ constexpr uint32_t kk_off(int b) { return 2048u * b * (b + 1); }
 __host__ __device__ constexpr uint32_t w_col(int b) { return 8u * b * (b + 1); }
 static_assert(OYK + 16384 <= GG, "decayed-product operands below G");
+static_assert(64 * 128 * 4 <= OYQ - OKK + 16384 * 2, "dG rows fit over the operands");
 static_assert(DW + 16384 + 1024 <= S_DU, "dw and its transposed view's overrun");
 static_assert(ALLOC <= 232448, "grad smem fits");
 // TMEM columns
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(256, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + ABORT);
-  const uint32_t ld_bar = sb + BAR, mma_bar = sb + BAR + 8;
+  const uint32_t ld_bar = sb + BAR, ld2_bar = sb + BAR + 8, mma_bar = sb + BAR + 16;
   float *sBeta = reinterpret_cast<float *>(smem + BETA);
   float *sDgam = reinterpret_cast<float *>(smem + DGAM);
   float *sDb = reinterpret_cast<float *>(smem + DB);
@@ -391,6 +395,7 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0) tmem_alloc(sb + SLOT, 512);
   if (tid == 0) {
     mbar_init(ld_bar, 1);
+    mbar_init(ld2_bar, 1);
     mbar_init(mma_bar, 1);
     *sAbort = 0u;
     fence_mbar_init();
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
   uint32_t ld_phase = 0, n_mma = 0;
-  bool ld_inflight = false, mma_inflight = false;
+  bool ld_inflight = false, ld2_inflight = false, mma_inflight = false;
   auto abort_all = [&]() {
     *sAbort = 1u;
     set_status(p.status, KDA_DEVICE_TIMEOUT);
@@ -444,43 +449,61 @@ __global__ void __launch_bounds__(256, 1)
     // ---- loads
     if (warp == 0) {
       if (lane == 0) {
-        mbar_expect_tx(ld_bar, LOAD_TX);
+        mbar_expect_tx(ld_bar, LOAD1_TX);
+        mbar_expect_tx(ld2_bar, LOAD2_TX);
         bulk_load(sb + SV, sv, SV_BYTES, ld_bar);
-        bulk_load(sb + TT, gi + I_T, 8192, ld_bar);
-        bulk_load(sb + KT, gi + I_KT, 16384, ld_bar);
       }
       __syncwarp();
       const int y = (int)tok0;
       if (lane < 16) {
         tma_load_2d(sb + DO + 1024u * lane, &maps.d_o, h * VD + 8 * lane, y, ld_bar);
-        tma_load_2d(sb + VV + 1024u * lane, &maps.v, h * VD + 8 * lane, y, ld_bar);
       } else if (lane < 20) {
         const int qd = lane - 16;
         tma_load_2d(sb + GG + 8192u * qd, &maps.g, h * KD + 32 * qd, y, ld_bar);
-      } else if (lane < 22) {
-        const int hf = lane - 20;
-        tma_load_2d(sb + QQ + 8192u * hf, &maps.q, h * KD + 64 * hf, y, ld_bar);
-        tma_load_2d(sb + KK + 8192u * hf, &maps.k, h * KD + 64 * hf, y, ld_bar);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        bulk_load(sb + TT, gi + I_T, 8192, ld2_bar);
+        bulk_load(sb + KT, gi + I_KT, 16384, ld2_bar);
+      }
+      if (lane < 16) {
+        tma_load_2d(sb + VV + 1024u * lane, &maps.v, h * VD + 8 * lane, y, ld2_bar);
+      } else if (lane < 18) {
+        const int hf = lane - 16;
+        tma_load_2d(sb + QQ + 8192u * hf, &maps.q, h * KD + 64 * hf, y, ld2_bar);
+        tma_load_2d(sb + KK + 8192u * hf, &maps.k, h * KD + 64 * hf, y, ld2_bar);
       }
     }
-    ld_inflight = true;
+    ld_inflight = ld2_inflight = true;
     if (tid < C) sBeta[tid] = tid < n ? p.beta[(tok0 + tid) * H + h] : 0.f;
     if (!mbar_wait(ld_bar, ld_phase)) abort_all();
     else ld_inflight = false;
     ld_phase ^= 1u;
+    // the next item's inputs into L2 while this one computes
+    if (warp == 0 && item + gridDim.x < n_items) {
+      const uint32_t nx = item + gridDim.x;
+      const int hn = (int)(nx % (uint32_t)H);
+      const uint32_t cn = nx / (uint32_t)H;
+      const int yn = (int)((size_t)(cn / (uint32_t)nc) * T + (cn % (uint32_t)nc) * C);
+      const unsigned char *svn = p.saves + (size_t)nx * SV_BYTES;
+      const unsigned char *gin = p.items + (size_t)nx * ct.item_stride;
+      if (lane < 6) prefetch_l2(svn + 16384u * lane, 16384);
+      else if (lane == 6) prefetch_l2(gin + I_T, 8192);
+      else if (lane == 7) prefetch_l2(gin + I_KT, 16384);
+      else if (lane == 8) prefetch_l2(gin + I_AKK, 16384);
+      else if (lane < 13) tma_prefetch_2d(&maps.g, hn * KD + 32 * (lane - 9), yn);
+      else if (lane < 15) tma_prefetch_2d(&maps.q, hn * KD + 64 * (lane - 13), yn);
+      else if (lane < 17) tma_prefetch_2d(&maps.k, hn * KD + 64 * (lane - 15), yn);
+      if (lane < 16) {
+        tma_prefetch_2d(&maps.v, hn * VD + 8 * lane, yn);
+        tma_prefetch_2d(&maps.d_o, hn * VD + 8 * lane, yn);
+      }
+    }
     if (n < C) {  // rows past the chunk's end: zero (they may hold the next row)
       const int m = C - n;
       for (int i = tid; i < 16 * m; i += 256) {
         const int grp = i / m, r = n + i % m;
         *reinterpret_cast<uint4 *>(smem + DO + 1024 * grp + 16 * r) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(smem + VV + 1024 * grp + 16 * r) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      for (int i = tid; i < 8 * m; i += 256) {  // q, k: 8 x 16 B per row and half
-        const int r = n + i / 8, part = i % 8;
-        for (int hf = 0; hf < 2; ++hf) {
-          *reinterpret_cast<uint4 *>(smem + QQ + 8192 * hf + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4 *>(smem + KK + 8192 * hf + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
-        }
       }
       for (int i = tid; i < 4 * 8 * m; i += 256) {  // g: 8 x 16 B per row and quarter
         const int qd = i / (8 * m), rem = i % (8 * m), r = n + rem / 8, part = rem % 8;
@@ -549,6 +572,23 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
+    // the later phases' inputs (issued with the first group)
+    if (!mbar_wait(ld2_bar, ld_phase ^ 1u)) abort_all();
+    else ld2_inflight = false;
+    if (n < C) {
+      const int m = C - n;
+      for (int i = tid; i < 16 * m; i += 256) {
+        const int grp = i / m, r = n + i % m;
+        *reinterpret_cast<uint4 *>(smem + VV + 1024 * grp + 16 * r) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int i = tid; i < 8 * m; i += 256) {  // q, k: 8 x 16 B per row and half
+        const int r = n + i / 8, part = i % 8;
+        for (int hf = 0; hf < 2; ++hf) {
+          *reinterpret_cast<uint4 *>(smem + QQ + 8192 * hf + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(smem + KK + 8192 * hf + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
     sync_smem();
     if (*sAbort) goto done;
     // ---- T products
@@ -559,8 +599,8 @@ __global__ void __launch_bounds__(256, 1)
       mma_k(tmem + C_X, Opnd{sb + DW, 1024, 128}, 1, Opnd{sb + KT, 1024, 128}, 1, 8, 64, true);
       // dY_k^T = dw^T T                           lanes = channels
       mma_k(tmem + C_DYK, Opnd{sb + DW, 128, 1024}, 0, Opnd{sb + TT, 1024, 128}, 1, 4, 64, false);
-      // dY_v = T^T dU                              lanes = rows j
-      mma_k(tmem + C_ROW, Opnd{sb + TT, 1024, 128}, 1, Opnd{sb + S_DU, 2048, 128}, 1, 4, 128, false);
+      // dY_v^T = dU^T T                            lanes = value columns v
+      mma_k(tmem + C_ROW, Opnd{sb + S_DU, 2048, 128}, 1, Opnd{sb + TT, 1024, 128}, 1, 4, 64, false);
       mma_commit(mma_bar);
     }
     mma_wait();
@@ -583,20 +623,16 @@ __global__ void __launch_bounds__(256, 1)
           st_bf16x8(smem, DTU + mn_off(j8, r, C), a);
         }
       }
-      // dv = beta dY_v (rows j < n), this thread's 64 columns
+    }
+    {  // dv = beta dY_v: value column L, rows j = 32 hh .. (a warp writes 128
+       // contiguous bytes per row)
+      float v[32];
+      tmem_ld32(tq + C_ROW + 32 * hh, v);
+      float *dst = p.dv + tok0 * H * VD + (size_t)h * VD + L;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tq + C_ROW + 64 * hh + 32 * half, v);
-        if (L < n) {
-          const int j = L;
-          const float bj = sBeta[j];
-          float4 *dst = reinterpret_cast<float4 *>(p.dv + (tok0 + j) * H * VD + (size_t)h * VD +
-                                                   64 * hh + 32 * half);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(bj * v[4 * q4], bj * v[4 * q4 + 1], bj * v[4 * q4 + 2],
-                                  bj * v[4 * q4 + 3]);
-        }
+      for (int k = 0; k < 32; ++k) {
+        const int j = 32 * hh + k;
+        if (j < n) dst[(size_t)j * H * VD] = sBeta[j] * v[k];
       }
     }
     sync_smem();
@@ -640,6 +676,12 @@ __global__ void __launch_bounds__(256, 1)
       mma_k(tmem + C_Y, Opnd{sb + TT, 1024, 128}, 1, Opnd{sb + PP, 128, 1024}, 1, 4, 64, false);
       mma_commit(mma_bar);
     }
+    float4 akk[8];  // A_kk row a = L, this thread's 32 columns (read while the MMA runs)
+    if (quad < 2) {
+      const float4 *src = reinterpret_cast<const float4 *>(gi + I_AKK + (L * C + 32 * hh) * 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) akk[i] = src[i];
+    }
     mma_wait();
     if (*sAbort) goto done;
     if (quad < 2) {
@@ -648,7 +690,6 @@ __global__ void __launch_bounds__(256, 1)
       {
         const int a_ = L;
         const float ba = sBeta[a_];
-        const float4 *akk = reinterpret_cast<const float4 *>(gi + I_AKK + (a_ * C + 32 * hh) * 4);
         float db = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -734,50 +775,75 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int i = 0; i < kNumSub; ++i) E[i] = Gat(16 * i + 15, ch);
       const float GC = E[kNumSub - 1];
-      float dG[32];
+      // dG per row into shared memory ([row][channel] fp32, over the decayed
+      // products' operands, which the MMAs above were the last to read)
+      float *sDG = reinterpret_cast<float *>(smem + OKK);
       float gsum = 0.f, gcp = 0.f;
-      auto bf_at = [&](uint32_t off) -> float {
-        return __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(smem + off) << 16);
-      };
-#pragma unroll
+      // the bf16 values the MMAs read, recomputed bit for bit as the operand
+      // build formed them (same expressions, round to nearest even)
+      auto bfr = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+#pragma unroll 1
       for (int e = 0; e < 4; ++e) {
         const int r8 = 32 * hh + 8 * e;
         const int br = r8 >> 4;
-        float dqt[8], dkh[8], dyk[8], rq[8], rk[8], w[kNumSub][8];
-        tmem_ld8(tq + C_DQT + r8, dqt);
-        tmem_ld8(tq + C_DKH + r8, dkh);
-        tmem_ld8(tq + C_DYK + r8, dyk);
-        tmem_ld8(tq + C_ROW + 32 * br + (r8 & 15), rq);
-        tmem_ld8(tq + C_ROW + 32 * br + 16 + (r8 & 15), rk);
+        // this group's TMEM columns: one batch of loads, one wait
+        uint32_t u_[5 + kNumSub][8];
+        tmem_ld8_nw(tq + C_DQT + r8, u_[0]);
+        tmem_ld8_nw(tq + C_DKH + r8, u_[1]);
+        tmem_ld8_nw(tq + C_DYK + r8, u_[2]);
+        tmem_ld8_nw(tq + C_ROW + 32 * br + (r8 & 15), u_[3]);
+        tmem_ld8_nw(tq + C_ROW + 32 * br + 16 + (r8 & 15), u_[4]);
 #pragma unroll
-        for (int bb = 0; bb < kNumSub; ++bb)
-          if (bb >= br) tmem_ld8(tq + C_W + w_col(bb) + r8, w[bb]);
+        for (int bb = 0; bb < kNumSub; ++bb)  // W_bb holds row r only for bb >= b(r)
+          tmem_ld8_nw(tq + C_W + w_col(bb) + (bb >= br ? r8 : 0), u_[5 + bb]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 5 + kNumSub; ++i) reg_fence8(u_[i]);
+        float dqt[8], dkh[8], dyk[8], rq[8], rk[8], w[kNumSub][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          dqt[k] = __uint_as_float(u_[0][k]);
+          dkh[k] = __uint_as_float(u_[1][k]);
+          dyk[k] = __uint_as_float(u_[2][k]);
+          rq[k] = __uint_as_float(u_[3][k]);
+          rk[k] = __uint_as_float(u_[4][k]);
+#pragma unroll
+          for (int bb = 0; bb < kNumSub; ++bb) w[bb][k] = __uint_as_float(u_[5 + bb][k]);
+        }
         const float Pr = br == 0 ? 0.f : E[br - 1];
         float fac[kNumSub];
 #pragma unroll
         for (int bb = 0; bb < kNumSub; ++bb)
           fac[bb] = bb <= br ? 1.f : ex2(E[bb - 1] - Pr);
+        // per block: 2^{P_b}, 2^{E_b - P_b}, 2^{G_C - E_b} (all <= 1), so that
+        // 2^{G_r} = e1 2^{P_b} and 2^{G_C - G_r} = (ie1 2^{E_b - P_b}) 2^{G_C - E_b}
+        // with every partial product <= 1 (no overflow; underflow only where
+        // the value itself is below the fp32 range)
+        const float ePr = ex2(Pr), fE = ex2(E[br] - Pr), fC = ex2(GC - E[br]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int r = r8 + k;
           const float Gr = Gat(r, ch);
-          const float e1 = ex2(Gr - Pr), ie1 = ex2(Pr - Gr), eG = ex2(Gr), eH = ex2(GC - Gr);
+          const float e1 = ex2(Gr - Pr), ie1 = ex2(Pr - Gr);
+          const float eG = e1 * ePr, eH = (ie1 * fE) * fC;
           const float kr = raw_at(KK, r, ch), qr = raw_at(QQ, r, ch);
-          const float yq = bf_at(OYQ + op_off(ch, r, C)), yk = bf_at(OYK + op_off(ch, r, C));
+          const float yq = bfr(qr * e1), yk = bfr(kr * e1);
+          const float ik = kr * ie1;
           float ccol = 0.f, gcol = 0.f;  // column sums: dk (fp32 factors), dG (the KK values)
 #pragma unroll
           for (int bb = 0; bb < kNumSub; ++bb) {
             if (bb < br) continue;
             ccol = fmaf(w[bb][k], fac[bb], ccol);
-            gcol = fmaf(w[bb][k], bf_at(OKK + kk_off(bb) + op_off(ch, r, 16 * (bb + 1))), gcol);
+            gcol = fmaf(w[bb][k], bfr(ik * fac[bb]), gcol);
           }
           const float dQt = scale * dqt[k] * eG;        // dQ~ e^G
           const float dKt = sBeta[r] * dyk[k] * eG;     // dK~ e^G
           const float dKh = dkh[k] * eH;                // dK^ e^{G_C - G}
           const float dq = e1 * rq[k] + dQt;
           const float dk = e1 * rk[k] + ie1 * ccol + dKt + dKh;
-          dG[8 * e + k] = (yq * rq[k] + yk * rk[k] - gcol) + qr * dQt + kr * (dKt - dKh);
-          gsum += dG[8 * e + k];
+          const float dGr = (yq * rq[k] + yk * rk[k] - gcol) + qr * dQt + kr * (dKt - dKh);
+          sDG[r * KD + ch] = dGr;
+          gsum += dGr;
           gcp = fmaf(kr, dKh, gcp);
           if (r < n) {
             p.dq[((tok0 + r) * H + h) * KD + ch] = dq;
@@ -794,10 +860,10 @@ __global__ void __launch_bounds__(256, 1)
       // rounding of dS' then cancels with them.
       const float dGC = sGcp[ch] + sGcp[128 + ch] + sDgam[ch] * ex2(GC);
       float carry = dGC + (hh == 0 ? sGp[128 + ch] : 0.f);
-#pragma unroll
+#pragma unroll 8
       for (int k = 31; k >= 0; --k) {
-        carry += dG[k];
         const int r = 32 * hh + k;
+        carry += sDG[r * KD + ch];
         if (r < n) p.dg[((tok0 + r) * H + h) * KD + ch] = carry;
       }
       if (tid < n) p.dbeta[(tok0 + tid) * H + h] = sDb[tid] + sDb[64 + tid] + sDb[128 + tid];
@@ -809,6 +875,7 @@ __global__ void __launch_bounds__(256, 1)
 done:
   if (tid == 0) {
     if (ld_inflight) mbar_wait(ld_bar, ld_phase);
+    if (ld2_inflight) mbar_wait(ld2_bar, ld_inflight ? ld_phase : ld_phase ^ 1u);
     if (mma_inflight) mbar_wait(mma_bar, (n_mma - 1) & 1u);
   }
   tc_fence_before();

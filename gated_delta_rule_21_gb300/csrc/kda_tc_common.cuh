@@ -285,6 +285,24 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t t0, uint32_t t1, float (&v)
   }
 }
 
+// 8 consecutive fp32 columns without waiting: a batch of these is followed
+// by one tmem_wait_ld(), then reg_fence8() on each result so no use of the
+// registers is scheduled before the wait.
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void reg_fence8(uint32_t (&r)[8]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]));
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   float a[16], b[16];
