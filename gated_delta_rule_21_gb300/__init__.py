@@ -105,6 +105,8 @@ def lib():
         L.kda_chunk_bwd.restype = i
         L.kda_chunk_bwd_workspace_size_for.argtypes = [sp, i, i]
         L.kda_chunk_bwd_workspace_size_for.restype = u64
+        L.kda_chunk_bwd_workspace_size_packed.argtypes = [sp, i]
+        L.kda_chunk_bwd_workspace_size_packed.restype = u64
         L.kda_chunk_bwd_ex.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, u64, i, vp]
         L.kda_chunk_bwd_ex.restype = i
@@ -316,6 +318,13 @@ def bwd_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=Fals
         return int(lib().kda_chunk_bwd_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
     return int(lib().kda_chunk_bwd_workspace_size_for(ctypes.byref(s), int(bool(has_segment_ids)),
                                                       IMPLS[impl]))
+
+
+def bwd_workspace_size_packed(B, T, H, K, V, max_runs_per_row, dtype=torch.bfloat16) -> int:
+    """Tensor-core backward workspace for inputs with segment ids and at most
+    ``max_runs_per_row`` runs per row (0 when that path does not apply)."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_bwd_workspace_size_packed(ctypes.byref(s), int(max_runs_per_row)))
 
 
 def chunk_bwd(q, k, v, g, beta, d_o, scale=None, chunk_size=CHUNK, initial_state=None,

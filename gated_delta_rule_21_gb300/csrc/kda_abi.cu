@@ -338,17 +338,27 @@ kda_status kda_clear_device_status(void *workspace, kda_stream_t stream) {
 size_t kda_chunk_bwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
                                         kda_impl impl) {
   if (check_shape(s) != KDA_OK || !bwd_supported(s->K, s->V)) return 0;
-  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16,
-                                      has_segment_ids != 0);
-  const size_t simt = align_up(ws_bytes(s->B, s->T, has_segment_ids != 0), 256) +
+  const bool has_seg = has_segment_ids != 0;
+  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16);
+  const size_t simt = align_up(ws_bytes(s->B, s->T, has_seg), 256) +
                       bwd_scratch_bytes(s->B, s->T, s->H, s->K, s->V);
+  // with segment ids: room for ceil(T/64) runs per row beyond the chunks of T
+  const size_t tc = tc_ok ? bwd_tc_workspace_bytes(s->B, s->T, s->H, has_seg,
+                                                   default_runs_bound(s->T))
+                          : 0;
   switch (impl) {
     case KDA_IMPL_SIMT: return simt;
     case KDA_IMPL_TC:
-    case KDA_IMPL_SPLIT: return tc_ok ? bwd_tc_workspace_bytes(s->B, s->T, s->H) : 0;
-    case KDA_IMPL_AUTO: return tc_ok ? bwd_tc_workspace_bytes(s->B, s->T, s->H) : simt;
+    case KDA_IMPL_SPLIT: return tc;
+    case KDA_IMPL_AUTO: return tc_ok ? tc : simt;
   }
   return 0;
+}
+
+size_t kda_chunk_bwd_workspace_size_packed(const kda_shape *s, int max_runs_per_row) {
+  if (check_shape(s) != KDA_OK || max_runs_per_row < 1) return 0;
+  if (!bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16)) return 0;
+  return bwd_tc_workspace_bytes(s->B, s->T, s->H, true, max_runs_per_row);
 }
 
 size_t kda_chunk_bwd_workspace_size(const kda_shape *s, int has_segment_ids) {
@@ -388,12 +398,15 @@ kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, co
   for (const void *ptr : ptrs)
     if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
   const bool has_seg = segment_ids != nullptr;
-  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16, has_seg);
+  const bool tc_ok = bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16);
   if ((impl == KDA_IMPL_TC || impl == KDA_IMPL_SPLIT) && !tc_ok) return KDA_ERR_UNSUPPORTED;
   const bool use_tc = impl == KDA_IMPL_TC || impl == KDA_IMPL_SPLIT ||
                       (impl == KDA_IMPL_AUTO && tc_ok);
-  const size_t need = kda_chunk_bwd_workspace_size_for(s, has_seg ? 1 : 0,
-                                                       use_tc ? KDA_IMPL_TC : KDA_IMPL_SIMT);
+  // the tensor-core path with segment ids takes any workspace that holds the
+  // chunks of T per row (more runs than it has room for: KDA_DEVICE_WORKSPACE)
+  const size_t need = use_tc ? bwd_tc_workspace_bytes(s->B, s->T, s->H, has_seg, 0)
+                             : kda_chunk_bwd_workspace_size_for(s, has_seg ? 1 : 0,
+                                                                KDA_IMPL_SIMT);
   if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
 
@@ -427,9 +440,17 @@ kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, co
     p.runs.total_runs = &reinterpret_cast<WsHeader *>(ws)->total_runs;
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (use_tc)
-    return from_cuda(launch_bwd_tc(p, workspace, workspace_bytes, dq, dk, dg, dbeta,
-                                   &reinterpret_cast<WsHeader *>(ws)->status, cs));
+  if (use_tc) {
+    if (has_seg) {
+      // runs and chunk tables; dv = 0 on padding; d_initial = d_final (or 0)
+      // for rows without a run
+      cudaError_t e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, dv, 0,
+                                          d_final, d_initial, workspace, cs, true);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
+    return from_cuda(launch_bwd_tc(p, segment_ids, workspace, workspace_bytes, dq, dk, dg,
+                                   dbeta, &reinterpret_cast<WsHeader *>(ws)->status, cs));
+  }
   if (has_seg) {
     // Runs; dv = 0 on padding; d_initial = d_final (or 0) for rows without a run.
     cudaError_t e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, dv, 0,

@@ -1,5 +1,5 @@
 // kda_bwd_tc.cu -- the chunked backward of the KDA forward on the tensor cores
-// (bf16 q, k, v, d_o; K = V = 128; rows without segment ids).
+// (bf16 q, k, v, d_o; K = V = 128; with or without segment ids).
 //
 // Page "feat(kda): integrate KDA attention with tokamax backend and CP
 // support", section "Delta Rule formulation", gives the forward; the pages
@@ -28,9 +28,9 @@
 // Three passes:
 //  1. the forward's prep kernel with larger items (also T, A_kk and K e^G)
 //     and its recurrence in save mode (the state entering every chunk, U);
-//  2. bwd_chain_kernel: the dS chain, one CTA per (row, head, value tile),
+//  2. bwd_chain_kernel: the dS chain, one CTA per (run, head, value tile),
 //     chunks from the last; it saves dS' and dU per chunk and writes
-//     d_initial;
+//     d_initial (a row's first run; later runs start from a reset state);
 //  3. bwd_grad_kernel: every (chunk, head) independently, all gradients of
 //     the chunk's tokens from the saved S, U, dS', dU and the inputs: a
 //     dozen MMA groups on tcgen05 (TMEM accumulators), the intra-chunk
@@ -54,6 +54,7 @@ struct BwdTcParams {
   const unsigned char *items;
   unsigned char *saves;
   ChunkTable ct;
+  RunTable runs;  // with segment ids: the run list (units are runs); else none
   int v_tile, n_vtiles;
   uint32_t *status;
 };
@@ -150,14 +151,15 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
   };
 
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
-  const uint32_t n_units = fits ? (uint32_t)p.B * (uint32_t)H * (uint32_t)p.n_vtiles : 0u;
-  const int nc = ct.n_chunks_row;
+  const uint32_t n_units = fits ? total_units(p.runs, p.B, H, p.n_vtiles) : 0u;
   for (uint32_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const int vt = (int)(unit % (uint32_t)p.n_vtiles);
-    const int h = (int)((unit / (uint32_t)p.n_vtiles) % (uint32_t)H);
-    const int b = (int)(unit / ((uint32_t)p.n_vtiles * (uint32_t)H));
+    // one run (the whole row without segment ids) of one head, VTR columns
+    const Unit u = decode_unit(p.runs, unit, p.B, T, H, p.n_vtiles);
+    const int vt = u.vt, h = u.h, b = u.b;
     const int vc0 = vt * VTR;
-    const uint32_t cbase = (uint32_t)b * (uint32_t)nc;
+    const uint32_t cbase = run_chunk_base(ct, b, T, u.run_in_row);
+    const int nc = u.end > u.start ? (u.end - u.start + C - 1) / C : 0;
+    if (nc == 0) continue;
     auto item_ptr = [&](int c) {
       return p.items + ((size_t)(cbase + c) * H + h) * ct.item_stride;
     };
@@ -170,10 +172,11 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
       bulk_load(dst, src, Lay::S_ITEM, bar);
       bulk_load(dst + Lay::S_GAM, src + I_GAM, 512, bar);
       for (int j = 0; j < VTR / 8; ++j)
-        tma_load_2d(dst + Lay::S_DO + 1024u * j, &tm_do, h * VD + vc0 + 8 * j, b * T + c * C, bar);
+        tma_load_2d(dst + Lay::S_DO + 1024u * j, &tm_do, h * VD + vc0 + 8 * j,
+                    b * T + u.start + c * C, bar);
     };
     float dS[CPT];  // gradient of the state leaving the chunk, [key L][col0 ..]
-    if (p.d_final) {
+    if (u.last && p.d_final) {  // the row's last run leaves the final state
       const float4 *src = reinterpret_cast<const float4 *>(
           p.d_final + (((size_t)b * H + h) * KD + L) * VD + vc0 + col0);
 #pragma unroll
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
 
     for (int i = 0; i < nc; ++i) {
       const int c = nc - 1 - i, s = i & 1;
-      const int n = min(C, T - c * C);
+      const int n = min(C, u.end - (u.start + c * C));
       unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
       const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
       unsigned char *sv = p.saves + ((size_t)(cbase + c) * H + h) * SV_BYTES;
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
         st_issued |= 1u << s;
       }
     }
-    if (p.d_initial) {
+    if (u.first && p.d_initial) {  // the row's first run starts from the initial state
       float4 *dst = reinterpret_cast<float4 *>(
           p.d_initial + (((size_t)b * H + h) * KD + L) * VD + vc0 + col0);
 #pragma unroll
@@ -436,12 +439,11 @@ __global__ void __launch_bounds__(256, 1)
 
   const uint32_t n_items = total_chunk_count(ct, p.B) <= ct.capacity
                                ? total_chunk_count(ct, p.B) * (uint32_t)H : 0u;
-  const int nc = ct.n_chunks_row;
   for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int h = (int)(item % (uint32_t)H);
-    const uint32_t chunk = item / (uint32_t)H;
-    const int b = (int)(chunk / (uint32_t)nc), c = (int)(chunk % (uint32_t)nc);
-    const int t0 = c * C, n = min(C, T - t0);
+    int b, t0, end;
+    chunk_of(ct, T, item / (uint32_t)H, b, t0, end);
+    const int n = min(C, end - t0);
     const size_t tok0 = (size_t)b * T + t0;
     const unsigned char *gi = p.items + (size_t)item * ct.item_stride;
     const unsigned char *sv = p.saves + (size_t)item * SV_BYTES;
@@ -483,8 +485,9 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0 && item + gridDim.x < n_items) {
       const uint32_t nx = item + gridDim.x;
       const int hn = (int)(nx % (uint32_t)H);
-      const uint32_t cn = nx / (uint32_t)H;
-      const int yn = (int)((size_t)(cn / (uint32_t)nc) * T + (cn % (uint32_t)nc) * C);
+      int bn, tn, en;
+      chunk_of(ct, T, nx / (uint32_t)H, bn, tn, en);
+      const int yn = bn * T + tn;
       const unsigned char *svn = p.saves + (size_t)nx * SV_BYTES;
       const unsigned char *gin = p.items + (size_t)nx * ct.item_stride;
       if (lane < 6) prefetch_l2(svn + 16384u * lane, 16384);
@@ -886,6 +889,22 @@ done:
   }
 }
 
+// Zero gradients for padding tokens (segment id 0): one warp per token.
+__global__ void __launch_bounds__(256)
+    bwd_zero_padding_kernel(const int32_t *segment_ids, int BT, int H, float *dq, float *dk,
+                            float *dg, float *dbeta) {
+  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (tok >= BT || segment_ids[tok] != 0) return;
+  const size_t base = (size_t)tok * H * KD;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = lane; i < H * KD / 4; i += 32) {
+    reinterpret_cast<float4 *>(dq + base)[i] = z;
+    reinterpret_cast<float4 *>(dk + base)[i] = z;
+    reinterpret_cast<float4 *>(dg + base)[i] = z;
+  }
+  for (int i = lane; i < H; i += 32) dbeta[(size_t)tok * H + i] = 0.f;
+}
+
 template <int VTR>
 cudaError_t launch_chain(const BwdTcParams &p, const CUtensorMap &m_do, cudaStream_t stream) {
   using Lay = ChainLayout<VTR>;
@@ -893,7 +912,8 @@ cudaError_t launch_chain(const BwdTcParams &p, const CUtensorMap &m_do, cudaStre
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Lay::ALLOC);
   if (e != cudaSuccess) return e;
-  const long units = (long)p.B * p.H * p.n_vtiles, sms = num_sms();
+  const long rows = p.runs.runs ? (long)p.B * p.T : (long)p.B;  // an upper bound of the runs
+  const long units = rows * p.H * p.n_vtiles, sms = num_sms();
   const int grid = (int)(units < sms ? units : sms);
   bwd_chain_kernel<VTR><<<grid > 0 ? grid : 1, Lay::THREADS, Lay::ALLOC, stream>>>(p, m_do);
   return cudaGetLastError();
@@ -901,18 +921,17 @@ cudaError_t launch_chain(const BwdTcParams &p, const CUtensorMap &m_do, cudaStre
 
 }  // namespace
 
-bool bwd_tc_supported(int K, int V, bool bf16, bool has_seg) {
-  return bf16 && !has_seg && K == KD && V == VD;
+bool bwd_tc_supported(int K, int V, bool bf16) { return bf16 && K == KD && V == VD; }
+
+size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row) {
+  return split::bwd_tc_workspace_bytes(B, T, H, has_seg, max_runs_per_row);
 }
 
-size_t bwd_tc_workspace_bytes(int B, int T, int H) {
-  return split::bwd_tc_workspace_bytes(B, T, H, false);
-}
-
-cudaError_t launch_bwd_tc(const BwdParams &bp, void *workspace, size_t workspace_bytes,
-                          float *dq, float *dk, float *dg, float *dbeta, uint32_t *status,
-                          cudaStream_t stream) {
-  if (bp.runs.runs != nullptr || bp.K != KD || bp.V != VD) return cudaErrorNotSupported;
+cudaError_t launch_bwd_tc(const BwdParams &bp, const int32_t *segment_ids, void *workspace,
+                          size_t workspace_bytes, float *dq, float *dk, float *dg, float *dbeta,
+                          uint32_t *status, cudaStream_t stream) {
+  if (bp.K != KD || bp.V != VD || (segment_ids != nullptr) != (bp.runs.runs != nullptr))
+    return cudaErrorNotSupported;
   FwdParams fp;
   memset(&fp, 0, sizeof(fp));
   fp.B = bp.B; fp.T = bp.T; fp.H = bp.H; fp.K = bp.K; fp.V = bp.V;
@@ -920,6 +939,7 @@ cudaError_t launch_bwd_tc(const BwdParams &bp, void *workspace, size_t workspace
   fp.scale = bp.scale;
   fp.initial_state = bp.initial_state;
   fp.status = status;
+  fp.runs = bp.runs;
   BwdLayout lay;
   cudaError_t e = launch_fwd_for_bwd(fp, workspace, workspace_bytes, &lay, stream);
   if (e != cudaSuccess) return e;
@@ -933,9 +953,12 @@ cudaError_t launch_bwd_tc(const BwdParams &bp, void *workspace, size_t workspace
   p.items = lay.items;
   p.saves = lay.saves;
   p.ct = lay.ct;
+  p.runs = bp.runs;
   p.status = status;
   const long bh = (long)p.B * p.H, sms = num_sms();
-  p.v_tile = bh * 4 <= sms ? 32 : (bh * 2 <= sms ? 64 : 128);
+  // value tile of the chain: as the forward recurrence (many short runs:
+  // 128 columns, each item read once)
+  p.v_tile = bp.runs.runs ? 128 : (bh * 4 <= sms ? 32 : (bh * 2 <= sms ? 64 : 128));
   p.n_vtiles = VD / p.v_tile;
   const uint64_t rows = (uint64_t)p.B * p.T;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -953,9 +976,14 @@ cudaError_t launch_bwd_tc(const BwdParams &bp, void *workspace, size_t workspace
   e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)gl::ALLOC);
   if (e != cudaSuccess) return e;
-  const long items = (long)lay.ct.n_chunks_row * p.B * p.H;
+  const long items = (long)lay.ct.capacity * p.H;  // an upper bound of the real count
   const int grid = (int)(items < sms ? items : sms);
   bwd_grad_kernel<<<grid > 0 ? grid : 1, 256, gl::ALLOC, stream>>>(p, gm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !segment_ids) return e;
+  const int bt = p.B * p.T;
+  bwd_zero_padding_kernel<<<(bt + 7) / 8, 256, 0, stream>>>(segment_ids, bt, p.H, dq, dk, dg,
+                                                            dbeta);
   return cudaGetLastError();
 }
 

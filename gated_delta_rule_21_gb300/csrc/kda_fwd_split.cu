@@ -1336,10 +1336,10 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
 }
 
 // ---- the forward pass the tensor-core backward starts from ------------------
-size_t split::bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg) {
-  if (has_seg) return 0;  // rows without segment ids only
-  const size_t chunks = (size_t)B * (((size_t)T + C - 1) / C);
-  return items_offset(B, T, false) + chunks * H * ((size_t)ITEM_BYTES_BWD + SV_BYTES);
+size_t split::bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row) {
+  const size_t nc = ((size_t)T + C - 1) / C;
+  const size_t chunks = (size_t)B * (nc + (has_seg && max_runs_per_row > 0 ? (size_t)max_runs_per_row : 0));
+  return items_offset(B, T, has_seg) + chunks * H * ((size_t)ITEM_BYTES_BWD + SV_BYTES);
 }
 
 // Items of ITEM_BYTES_BWD (the forward's, plus T, A_kk and K e^G), then the
@@ -1348,25 +1348,28 @@ size_t split::bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg) {
 cudaError_t split::launch_fwd_for_bwd(const FwdParams &p_in, void *workspace,
                                       size_t workspace_bytes, BwdLayout *out,
                                       cudaStream_t stream) {
-  if (p_in.runs.runs != nullptr || !fwd_split_supported(p_in.K, p_in.V, true, false, 0))
-    return cudaErrorNotSupported;
-  const size_t need = bwd_tc_workspace_bytes(p_in.B, p_in.T, p_in.H, false);
-  if (workspace_bytes < need) return cudaErrorInvalidValue;
+  const bool has_seg = p_in.runs.runs != nullptr;
+  if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, 0)) return cudaErrorNotSupported;
+  const size_t ioff = items_offset(p_in.B, p_in.T, has_seg);
+  const size_t per_chunk = (size_t)p_in.H * ((size_t)ITEM_BYTES_BWD + SV_BYTES);
+  if (workspace_bytes < ioff + per_chunk) return cudaErrorInvalidValue;
+  // every row's chunks without segment ids; with them, the chunks of all
+  // runs (counted on the device; an overflow is reported, nothing is done)
+  const size_t cap = (workspace_bytes - ioff) / per_chunk;
+  if (!has_seg && cap < (size_t)p_in.B * ((p_in.T + C - 1) / C)) return cudaErrorInvalidValue;
   FwdParams p = p_in;
-  p.v_tile = fit_tile((long)p.B * p.H, VD);
+  p.v_tile = has_seg ? 128 : fit_tile((long)p.B * p.H, VD);
   p.n_vtiles = VD / p.v_tile;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
-  const size_t ioff = items_offset(p.B, p.T, false);
-  const size_t n_items = (size_t)p.B * ((p.T + C - 1) / C) * p.H;
-  const size_t items_end = ioff + n_items * ITEM_BYTES_BWD;
+  const size_t items_end = ioff + cap * p.H * ITEM_BYTES_BWD;
   BwdLayout lay;
   lay.items = ws + ioff;
   lay.saves = ws + items_end;
-  lay.ct = make_table(p, ws, ioff, items_end, ITEM_BYTES_BWD, false, false);
+  lay.ct = make_table(p, ws, ioff, items_end, ITEM_BYTES_BWD, has_seg, false);
   cudaError_t e = launch_prep(p, lay.items, lay.ct, stream);
   if (e != cudaSuccess) return e;
   const ScanParams sc = {0, 0, nullptr, nullptr, lay.saves};
-  e = launch_rec_tile<2>(p, lay.items, lay.ct, false, sc, stream);
+  e = launch_rec_tile<2>(p, lay.items, lay.ct, has_seg, sc, stream);
   if (e == cudaSuccess && out) *out = lay;
   return e;
 }

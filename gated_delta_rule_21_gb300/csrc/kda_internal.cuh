@@ -144,14 +144,17 @@ bool bwd_supported(int K, int V);
 cudaError_t launch_bwd(const BwdParams &p, bool bf16, const int32_t *segment_ids,
                        float *dq, float *dk, float *dg, float *dbeta, cudaStream_t stream);
 
-// Tensor-core backward (kda_bwd_tc.cu): bf16, K = V = 128, rows without
-// segment ids; its workspace holds the forward's per-chunk items and the
-// saved states (bwd_tc_workspace_bytes).
-bool bwd_tc_supported(int K, int V, bool bf16, bool has_seg);
-size_t bwd_tc_workspace_bytes(int B, int T, int H);
-cudaError_t launch_bwd_tc(const BwdParams &p, void *workspace, size_t workspace_bytes,
-                          float *dq, float *dk, float *dg, float *dbeta, uint32_t *status,
-                          cudaStream_t stream);
+// Tensor-core backward (kda_bwd_tc.cu): bf16, K = V = 128; its workspace
+// holds the forward's per-chunk items and the saved states
+// (bwd_tc_workspace_bytes; with segment ids, for at most max_runs_per_row
+// runs per row, after the run builder's tables).  With segment ids the run
+// builder (launch_segment_runs with chunk tables) must have run on the
+// workspace; padding tokens get zero gradients.
+bool bwd_tc_supported(int K, int V, bool bf16);
+size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row);
+cudaError_t launch_bwd_tc(const BwdParams &p, const int32_t *segment_ids, void *workspace,
+                          size_t workspace_bytes, float *dq, float *dk, float *dg,
+                          float *dbeta, uint32_t *status, cudaStream_t stream);
 
 cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
                               cudaStream_t stream);

@@ -114,13 +114,16 @@ size_t items_offset(int B, int T, bool has_seg);
 
 // What the backward needs from the forward: items of ITEM_BYTES_BWD and the
 // saved S and U of every chunk (launch_fwd_for_bwd), in a workspace laid out
-// [items_offset][items][saves]; the chunk table of that call.
+// [items_offset][items][saves] (with segment ids, after the run list and
+// chunk tables the run builder wrote); the chunk table of that call.
 struct BwdLayout {
   unsigned char *items;
   unsigned char *saves;
   ChunkTable ct;
 };
-size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg);
+// With segment ids the items and saves are sized for at most
+// max_runs_per_row runs per row (each run adds at most one partial chunk).
+size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row);
 cudaError_t launch_fwd_for_bwd(const FwdParams &p, void *workspace, size_t workspace_bytes,
                                BwdLayout *out, cudaStream_t stream);
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,

@@ -379,13 +379,21 @@ KDA_API kda_status kda_chunk_fwd_host(const kda_shape *s, const void *q, const v
  * d_initial.  Supports K and V in {32, 64, 128}.
  * Two implementations; kda_chunk_bwd runs KDA_IMPL_AUTO (see _ex):
  *   tensor cores (KDA_IMPL_TC; KDA_IMPL_SPLIT names the same path): bf16
- *     q/k/v/d_o, K = V = 128, segment_ids NULL.  The chunked backward: the
- *     forward's per-chunk prep and its recurrence, which saves the state
- *     entering every chunk and U; the reverse chain of the state gradient
- *     (which saves dS' and dU per chunk); and a per-chunk kernel that forms
- *     every gradient of the chunk's tokens on tcgen05.  Workspace: the
- *     chunk items and saves, 208.5 KiB per (chunk, head) plus 1 KiB
- *     (874 MB for B=1, T=8192, H=32).
+ *     q/k/v/d_o, K = V = 128, with or without segment_ids.  The chunked
+ *     backward: the forward's per-chunk prep and its recurrence, which saves
+ *     the state entering every chunk and U; the reverse chain of the state
+ *     gradient (which saves dS' and dU per chunk); and a per-chunk kernel
+ *     that forms every gradient of the chunk's tokens on tcgen05.
+ *     Workspace: the chunk items and saves, 208.5 KiB per (chunk, head)
+ *     plus 1 KiB (874 MB for B=1, T=8192, H=32).  With segment ids the
+ *     workspace also holds the run list and chunk tables, and its items
+ *     cover ceil(T/64) chunks per row plus one per run up to a bound:
+ *     kda_chunk_bwd_workspace_size(_for) allows ceil(T/64) runs per row,
+ *     kda_chunk_bwd_workspace_size_packed a bound of the caller's choice,
+ *     and any workspace with room for ceil(T/64) chunks per row is accepted;
+ *     when the runs of a call need more chunks than the workspace holds,
+ *     the kernels compute nothing and set KDA_DEVICE_WORKSPACE in the status
+ *     word (kda_read_device_status then returns KDA_ERR_WORKSPACE).
  *   CUDA cores (KDA_IMPL_SIMT): every supported shape, fp32.  It recomputes
  *     the states from checkpoints every 8 tokens and walks each (run, head,
  *     32-column value tile) backwards; its workspace holds the run list, the
@@ -412,6 +420,12 @@ KDA_API kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *
  */
 KDA_API size_t kda_chunk_bwd_workspace_size_for(const kda_shape *s, int has_segment_ids,
                                                 kda_impl impl);
+/*
+ * Tensor-core backward workspace for inputs with segment ids and at most
+ * max_runs_per_row runs in any row (0 for an invalid or unsupported shape
+ * or max_runs_per_row < 1).
+ */
+KDA_API size_t kda_chunk_bwd_workspace_size_packed(const kda_shape *s, int max_runs_per_row);
 /*
  * kda_chunk_bwd with an explicit implementation: KDA_IMPL_AUTO (tensor
  * cores where they apply, else CUDA cores), KDA_IMPL_SIMT, or KDA_IMPL_TC /

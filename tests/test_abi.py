@@ -214,9 +214,18 @@ def test_backward_workspace_size_and_argument_checks(L):
     assert kda.bwd_workspace_size(1, 8192, 32, 128, 128, impl="auto") == tc
     assert kda.bwd_workspace_size(1, 100, 2, 128, 128, torch.float32, impl="tc") == 0
     assert kda.bwd_workspace_size(1, 100, 2, 64, 64, impl="tc") == 0
-    assert kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="tc") == 0
-    assert kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True) == \
-        kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="simt")
+    # with segment ids: the run list and chunk tables, then items and saves for
+    # ceil(T/64) chunks per row plus ceil(T/64) runs per row (AUTO's size), or
+    # a bound of the caller's choice
+    tcs = kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True, impl="tc")
+    assert tcs == kda.bwd_workspace_size(1, 100, 2, 128, 128, has_segment_ids=True)
+    assert tcs == kda.bwd_workspace_size_packed(1, 100, 2, 128, 128, max_runs_per_row=2)
+    per_chunk = 2 * (115200 + 98304)
+    assert kda.bwd_workspace_size_packed(1, 100, 2, 128, 128, 5) == tcs + 3 * per_chunk
+    assert kda.bwd_workspace_size_packed(1, 100, 2, 128, 128, 0) == 0
+    assert kda.bwd_workspace_size_packed(1, 100, 2, 64, 64, 4) == 0
+    assert kda.bwd_workspace_size(1, 100, 2, 64, 64, has_segment_ids=True) == \
+        kda.bwd_workspace_size(1, 100, 2, 64, 64, has_segment_ids=True, impl="simt")
     assert kda.bwd_workspace_size(1, 100, 2, 64, 64) == \
         kda.bwd_workspace_size(1, 100, 2, 64, 64, impl="simt")
     assert kda.bwd_workspace_size(1, 100, 2, 64, 64, has_segment_ids=True) > \
@@ -254,7 +263,8 @@ def test_backward_workspace_size_and_argument_checks(L):
     assert call_ex(7) == 1                                      # unknown impl
     assert call_ex(2, shape=(1, 64, 2, 64, 64, 1)) == 2          # TC: K, V
     assert call_ex(2, shape=(1, 64, 2, 128, 128, 0)) == 2        # TC: fp32 inputs
-    assert call_ex(2, seg=FAKE) == 2                             # TC: segment ids
+    min_seg = kda.bwd_workspace_size_packed(1, 64, 2, 128, 128, 1) - 2 * (115200 + 98304)
+    assert call_ex(2, seg=FAKE, nbytes=min_seg - 1) == 4         # TC: room for T's chunks
     assert call_ex(2, nbytes=nb - 1) == 4                        # TC: small workspace
     simt_nb = kda.bwd_workspace_size(1, 64, 2, 128, 128, impl="simt")
     assert call_ex(1, nbytes=simt_nb - 1) == 4                   # SIMT: its own size

@@ -1,10 +1,11 @@
 """GPU parity of the tensor-core backward (kda_chunk_bwd_ex with KDA_IMPL_TC,
-and KDA_IMPL_AUTO, which picks it for bf16 K = V = 128 without segment
-ids) against the fp64 backward oracle on the same seeded inputs and
-upstream gradients: every gradient, on one chunk, several chunks, ragged
-last chunks, two rows, gates at the contract's lower bound, with and
-without an initial state and d_final, and two heads of the B1 H32 T8192
-workload.
+and KDA_IMPL_AUTO, which picks it for bf16 K = V = 128) against the fp64
+backward oracle on the same seeded inputs and upstream gradients: every
+gradient, on one chunk, several chunks, ragged last chunks, two rows, gates
+at the contract's lower bound, with and without an initial state and
+d_final, packed rows (runs of one token, runs across chunk boundaries,
+padding, rows without a run), the item overflow report, and two heads of
+the fixed and the packed B1 H32 T8192 workloads.
 
 Tolerance: the bounds the forward's bf16 parity uses (relative L2 <= 1e-2;
 max-abs <= 2e-2, here relative to each gradient's largest magnitude, since
@@ -153,3 +154,75 @@ def test_tc_and_simt_backward_agree():
     simt = [t.cpu().numpy() for t in _gpu(x, u, impl="simt")]
     for name, a, b in zip(NAMES, tc, simt):
         _check(name, a, b, "tc vs simt")
+
+
+PACKED = {
+    "packed_pads": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1,
+                        segments=[[("pad", 3), 100, 1, 1, ("pad", 5), 120, 70],
+                                  [64, 64, ("pad", 2), 170]]),
+    "padding_rows_between": dict(B=4, T=96, H=2, K=128, V=128, init_state_std=0.1,
+                                 segments=[[("pad", 96)], [40, ("pad", 6), 50],
+                                           [("pad", 96)], [96]]),
+    "short_runs": dict(B=1, T=40, H=2, K=128, V=128, init_state_std=0.1,
+                       segments=[1, 1, 3, ("pad", 1), 7, 1, 2, 24]),
+    "runs_across_chunks": dict(B=1, T=400, H=3, K=128, V=128,
+                               segments=[65, 63, 1, 130, ("pad", 13), 128]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(PACKED))
+def test_tc_backward_packed_matches_oracle(case):
+    """Packed rows (segment ids): every run from a reset state, only the
+    row's first run sees the initial state and only its last run d_final;
+    padding tokens get zero gradients."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.custom_workload(name=case, **PACKED[case])
+    x, u = _inputs(w, seed=5)
+    # room for every run (rows with more runs than ceil(T/64) need more than
+    # the default size)
+    runs = int(max(len(torch.unique(r[r > 0])) for r in x["segment_ids"]))
+    ws = torch.zeros(kda.bwd_workspace_size_packed(w.B, w.T, w.H, w.K, w.V, max(runs, 1)),
+                     dtype=torch.uint8, device="cuda")
+    got = [t.cpu().numpy() for t in _gpu(x, u, workspace=ws)]
+    assert kda.read_device_status(ws) == 0
+    ref = _oracle(x, u)
+    for name, a, b in zip(NAMES, got, ref):
+        _check(name, a, b, case)
+    pad = (x["segment_ids"] == 0).numpy()
+    for name, a in zip(NAMES[:5], got[:5]):
+        assert np.all(a[pad] == 0), f"{case} {name} not zero on padding"
+
+
+def test_tc_backward_packed_full_size_sampled_heads():
+    """The packed B1 H32 T8192 workload (25 runs) through the tensor-core
+    path; the oracle checks two heads."""
+    w = ki.WORKLOADS["packed_bf16_h32_t8192_25seg"]
+    x, u = _inputs(w, seed=0)
+    got = _gpu(x, u)
+    hs = [0, 31]
+    got = [g[:, :, hs].cpu().numpy() if i < 5 else g[:, hs].cpu().numpy()
+           for i, g in enumerate(got)]
+    ref = _oracle(x, u, heads=hs)
+    for name, a, b in zip(NAMES, got, ref):
+        _check(name, a, b, "packed B1 H32 T8192")
+
+
+def test_tc_backward_packed_overflow_is_reported():
+    """A workspace sized for one run per row, inputs with four: the kernels
+    compute nothing and the status word says KDA_DEVICE_WORKSPACE (the
+    status read returns KDA_ERR_WORKSPACE); nothing faults."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.custom_workload(B=1, T=128, H=2, K=128, V=128, init_state_std=0.1,
+                           segments=[32, 32, 32, 32], name="overflow")
+    x, u = _inputs(w, seed=2)
+    ws = torch.zeros(kda.bwd_workspace_size_packed(1, 128, 2, 128, 128, 1), dtype=torch.uint8,
+                     device="cuda")
+    _gpu(x, u, workspace=ws)
+    assert kda.read_device_status(ws) == 4
+    ws2 = torch.zeros(kda.bwd_workspace_size_packed(1, 128, 2, 128, 128, 4), dtype=torch.uint8,
+                      device="cuda")
+    got = [t.cpu().numpy() for t in _gpu(x, u, workspace=ws2)]
+    assert kda.read_device_status(ws2) == 0
+    ref = _oracle(x, u)
+    for name, a, b in zip(NAMES, got, ref):
+        _check(name, a, b, "four runs, room for four")
