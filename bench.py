@@ -102,11 +102,16 @@ def measured_peaks():
 
 
 def kernel_source_digest(impl_name: str) -> str:
-    fname = {"tc": "kda_fwd_tc.cu", "simt": "kda_fwd_simt.cu", "split": "kda_fwd_split.cu",
-             "conv": "kda_conv.cu", "bwd": "kda_bwd.cu", "bwd_tc": "kda_bwd_tc.cu"}[impl_name]
-    path = os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Digest of the source(s) of a path's kernels (the tensor-core backward
+    also runs the split forward's prep and recurrence)."""
+    fnames = {"tc": ("kda_fwd_tc.cu",), "simt": ("kda_fwd_simt.cu",),
+              "split": ("kda_fwd_split.cu",), "conv": ("kda_conv.cu",), "bwd": ("kda_bwd.cu",),
+              "bwd_tc": ("kda_bwd_tc.cu", "kda_fwd_split.cu")}[impl_name]
+    h = hashlib.sha256()
+    for fname in fnames:
+        with open(os.path.join(ROOT, "gated_delta_rule_21_gb300", "csrc", fname), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(impl_name: str, workload: str):

@@ -80,6 +80,11 @@ WORKLOADS = {
     "fixed_bf16_h8_t32768": Workload(
         "fixed_bf16_h8_t32768", B=1, T=32768, H=8, K=128, V=128,
         init_state_std=0.1),
+    # not one of the pages' workloads: the B1 H32 T8192 shape at a quarter of
+    # the tokens, the size the detailed (many-pass) profiles are taken on
+    "fixed_bf16_h32_t2048": Workload(
+        "fixed_bf16_h32_t2048", B=1, T=2048, H=32, K=128, V=128,
+        init_state_std=0.1),
 }
 
 
