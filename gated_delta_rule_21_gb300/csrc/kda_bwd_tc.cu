@@ -330,14 +330,16 @@ constexpr uint32_t DGAM = BETA + 256;    // dgam, 128 fp32
 constexpr uint32_t DB = DGAM + 512;      // dbeta parts [3][64] fp32
 constexpr uint32_t GP = DB + 768;        // dG half sums [2][128] fp32
 constexpr uint32_t GCP = GP + 1024;      // sum_r dK^ K^ halves [2][128] fp32
-constexpr uint32_t BAR = GCP + 1024;     // load (phase A inputs), load (the rest), mma
-constexpr uint32_t SLOT = BAR + 24;
+constexpr uint32_t BAR = GCP + 1024;     // loads A, G, R; mma
+constexpr uint32_t SLOT = BAR + 32;
 constexpr uint32_t ABORT = SLOT + 4;
 constexpr uint32_t ALLOC = ABORT + 12 + 1024;
-// two load groups: what the first products and the cumsum read (saves, d_o,
-// g), then what the later phases read (v, T, K e^G, q, k)
-constexpr uint32_t LOAD1_TX = SV_BYTES + 16384 + 32768;
-constexpr uint32_t LOAD2_TX = 16384 + 8192 + 16384 + 16384 * 2;
+// three load groups: what the first products read (saves, d_o), issued
+// while the previous item's final readout runs (those regions are dead
+// then); g for the cumsum; what the later phases read (v, T, K e^G, q, k)
+constexpr uint32_t LOADA_TX = SV_BYTES + 16384;
+constexpr uint32_t LOADG_TX = 32768;
+constexpr uint32_t LOADR_TX = 16384 + 8192 + 16384 + 16384 * 2;
 // after the first products
 constexpr uint32_t DAQ = 0;              // scale dO U^T (j <= r), op_off(r, j, 64)
 constexpr uint32_t DAK = 8192;           // diag(beta) dL, op_off(r, j, 64)
@@ -357,7 +359,7 @@ constexpr uint32_t OYK = OYQ + 16384;
 __host__ __device__ constexpr uint32_t kk_off(int b) { return 2048u * b * (b + 1); }
 __host__ __device__ constexpr uint32_t w_col(int b) { return 8u * b * (b + 1); }
 static_assert(OYK + 16384 <= GG, "decayed-product operands below G");
-static_assert(64 * 128 * 4 <= OYQ - OKK + 16384 * 2, "dG rows fit over the operands");
+static_assert(64 * 128 * 4 <= GG - VV, "dG rows fit over v, T and K e^G");
 static_assert(DW + 16384 + 1024 <= S_DU, "dw and its transposed view's overrun");
 static_assert(ALLOC <= 232448, "grad smem fits");
 // TMEM columns
@@ -382,7 +384,8 @@ __global__ void __launch_bounds__(256, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   volatile uint32_t *sAbort = reinterpret_cast<volatile uint32_t *>(smem + ABORT);
-  const uint32_t ld_bar = sb + BAR, ld2_bar = sb + BAR + 8, mma_bar = sb + BAR + 16;
+  const uint32_t lda_bar = sb + BAR, ldg_bar = sb + BAR + 8, ldr_bar = sb + BAR + 16;
+  const uint32_t mma_bar = sb + BAR + 24;
   float *sBeta = reinterpret_cast<float *>(smem + BETA);
   float *sDgam = reinterpret_cast<float *>(smem + DGAM);
   float *sDb = reinterpret_cast<float *>(smem + DB);
@@ -397,8 +400,9 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) tmem_alloc(sb + SLOT, 512);
   if (tid == 0) {
-    mbar_init(ld_bar, 1);
-    mbar_init(ld2_bar, 1);
+    mbar_init(lda_bar, 1);
+    mbar_init(ldg_bar, 1);
+    mbar_init(ldr_bar, 1);
     mbar_init(mma_bar, 1);
     *sAbort = 0u;
     fence_mbar_init();
@@ -408,8 +412,10 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SLOT);
   const uint32_t tq = tmem + ((uint32_t)(32 * quad) << 16);
-  uint32_t ld_phase = 0, n_mma = 0;
-  bool ld_inflight = false, ld2_inflight = false, mma_inflight = false;
+  // each load barrier completes once per item: ph_a / ph_g / ph_r are the
+  // parities of the next completion to wait for
+  uint32_t ph_a = 0, ph_g = 0, ph_r = 0, n_mma = 0;
+  bool lda_inflight = false, ldg_inflight = false, ldr_inflight = false, mma_inflight = false;
   auto abort_all = [&]() {
     *sAbort = 1u;
     set_status(p.status, KDA_DEVICE_TIMEOUT);
@@ -439,6 +445,20 @@ __global__ void __launch_bounds__(256, 1)
 
   const uint32_t n_items = total_chunk_count(ct, p.B) <= ct.capacity
                                ? total_chunk_count(ct, p.B) * (uint32_t)H : 0u;
+  // group A of an item (warp 0): the saves and d_o
+  auto issue_a = [&](uint32_t it) {
+    const int hx = (int)(it % (uint32_t)H);
+    int bx, tx, ex;
+    chunk_of(ct, T, it / (uint32_t)H, bx, tx, ex);
+    if (lane == 0) {
+      mbar_expect_tx(lda_bar, LOADA_TX);
+      bulk_load(sb + SV, p.saves + (size_t)it * SV_BYTES, SV_BYTES, lda_bar);
+    }
+    __syncwarp();
+    if (lane < 16) tma_load_2d(sb + DO + 1024u * lane, &maps.d_o, hx * VD + 8 * lane, bx * T + tx, lda_bar);
+  };
+  if (warp == 0 && blockIdx.x < n_items) issue_a(blockIdx.x);
+  lda_inflight = blockIdx.x < n_items;
   for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int h = (int)(item % (uint32_t)H);
     int b, t0, end;
@@ -446,71 +466,55 @@ __global__ void __launch_bounds__(256, 1)
     const int n = min(C, end - t0);
     const size_t tok0 = (size_t)b * T + t0;
     const unsigned char *gi = p.items + (size_t)item * ct.item_stride;
-    const unsigned char *sv = p.saves + (size_t)item * SV_BYTES;
 
-    // ---- loads
+    // ---- loads: g, then v, T, K e^G, q, k (group A was issued earlier)
     if (warp == 0) {
       if (lane == 0) {
-        mbar_expect_tx(ld_bar, LOAD1_TX);
-        mbar_expect_tx(ld2_bar, LOAD2_TX);
-        bulk_load(sb + SV, sv, SV_BYTES, ld_bar);
+        mbar_expect_tx(ldg_bar, LOADG_TX);
+        mbar_expect_tx(ldr_bar, LOADR_TX);
       }
       __syncwarp();
       const int y = (int)tok0;
-      if (lane < 16) {
-        tma_load_2d(sb + DO + 1024u * lane, &maps.d_o, h * VD + 8 * lane, y, ld_bar);
-      } else if (lane < 20) {
-        const int qd = lane - 16;
-        tma_load_2d(sb + GG + 8192u * qd, &maps.g, h * KD + 32 * qd, y, ld_bar);
-      }
+      if (lane < 4) tma_load_2d(sb + GG + 8192u * lane, &maps.g, h * KD + 32 * lane, y, ldg_bar);
       __syncwarp();
       if (lane == 0) {
-        bulk_load(sb + TT, gi + I_T, 8192, ld2_bar);
-        bulk_load(sb + KT, gi + I_KT, 16384, ld2_bar);
+        bulk_load(sb + TT, gi + I_T, 8192, ldr_bar);
+        bulk_load(sb + KT, gi + I_KT, 16384, ldr_bar);
       }
       if (lane < 16) {
-        tma_load_2d(sb + VV + 1024u * lane, &maps.v, h * VD + 8 * lane, y, ld2_bar);
+        tma_load_2d(sb + VV + 1024u * lane, &maps.v, h * VD + 8 * lane, y, ldr_bar);
       } else if (lane < 18) {
         const int hf = lane - 16;
-        tma_load_2d(sb + QQ + 8192u * hf, &maps.q, h * KD + 64 * hf, y, ld2_bar);
-        tma_load_2d(sb + KK + 8192u * hf, &maps.k, h * KD + 64 * hf, y, ld2_bar);
+        tma_load_2d(sb + QQ + 8192u * hf, &maps.q, h * KD + 64 * hf, y, ldr_bar);
+        tma_load_2d(sb + KK + 8192u * hf, &maps.k, h * KD + 64 * hf, y, ldr_bar);
       }
     }
-    ld_inflight = ld2_inflight = true;
+    ldg_inflight = ldr_inflight = true;
     if (tid < C) sBeta[tid] = tid < n ? p.beta[(tok0 + tid) * H + h] : 0.f;
-    if (!mbar_wait(ld_bar, ld_phase)) abort_all();
-    else ld_inflight = false;
-    ld_phase ^= 1u;
-    // the next item's inputs into L2 while this one computes
+    if (!mbar_wait(lda_bar, ph_a)) abort_all();
+    else lda_inflight = false;
+    ph_a ^= 1u;
+    // the next item's later inputs into L2 while this one computes
     if (warp == 0 && item + gridDim.x < n_items) {
       const uint32_t nx = item + gridDim.x;
       const int hn = (int)(nx % (uint32_t)H);
       int bn, tn, en;
       chunk_of(ct, T, nx / (uint32_t)H, bn, tn, en);
       const int yn = bn * T + tn;
-      const unsigned char *svn = p.saves + (size_t)nx * SV_BYTES;
       const unsigned char *gin = p.items + (size_t)nx * ct.item_stride;
-      if (lane < 6) prefetch_l2(svn + 16384u * lane, 16384);
-      else if (lane == 6) prefetch_l2(gin + I_T, 8192);
-      else if (lane == 7) prefetch_l2(gin + I_KT, 16384);
-      else if (lane == 8) prefetch_l2(gin + I_AKK, 16384);
-      else if (lane < 13) tma_prefetch_2d(&maps.g, hn * KD + 32 * (lane - 9), yn);
-      else if (lane < 15) tma_prefetch_2d(&maps.q, hn * KD + 64 * (lane - 13), yn);
-      else if (lane < 17) tma_prefetch_2d(&maps.k, hn * KD + 64 * (lane - 15), yn);
-      if (lane < 16) {
-        tma_prefetch_2d(&maps.v, hn * VD + 8 * lane, yn);
-        tma_prefetch_2d(&maps.d_o, hn * VD + 8 * lane, yn);
-      }
+      if (lane == 0) prefetch_l2(gin + I_T, 8192);
+      else if (lane == 1) prefetch_l2(gin + I_KT, 16384);
+      else if (lane == 2) prefetch_l2(gin + I_AKK, 16384);
+      else if (lane < 7) tma_prefetch_2d(&maps.g, hn * KD + 32 * (lane - 3), yn);
+      else if (lane < 9) tma_prefetch_2d(&maps.q, hn * KD + 64 * (lane - 7), yn);
+      else if (lane < 11) tma_prefetch_2d(&maps.k, hn * KD + 64 * (lane - 9), yn);
+      if (lane < 16) tma_prefetch_2d(&maps.v, hn * VD + 8 * lane, yn);
     }
     if (n < C) {  // rows past the chunk's end: zero (they may hold the next row)
       const int m = C - n;
       for (int i = tid; i < 16 * m; i += 256) {
         const int grp = i / m, r = n + i % m;
         *reinterpret_cast<uint4 *>(smem + DO + 1024 * grp + 16 * r) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      for (int i = tid; i < 4 * 8 * m; i += 256) {  // g: 8 x 16 B per row and quarter
-        const int qd = i / (8 * m), rem = i % (8 * m), r = n + rem / 8, part = rem % 8;
-        *reinterpret_cast<uint4 *>(smem + GG + 8192 * qd + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     sync_smem();
@@ -527,6 +531,17 @@ __global__ void __launch_bounds__(256, 1)
       mma_commit(mma_bar);
     }
     // meanwhile: G = cumsum(g) (log2 units) per channel; dgam = rowsum(S * dS')
+    if (!mbar_wait(ldg_bar, ph_g)) abort_all();
+    else ldg_inflight = false;
+    ph_g ^= 1u;
+    if (n < C) {
+      const int m = C - n;
+      for (int i = tid; i < 4 * 8 * m; i += 256) {  // g: 8 x 16 B per row and quarter
+        const int qd = i / (8 * m), rem = i % (8 * m), r = n + rem / 8, part = rem % 8;
+        *reinterpret_cast<uint4 *>(smem + GG + 8192 * qd + 128 * r + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
+    }
     if (hh == 0) {
       const int ch = L;
       float acc = 0.f;
@@ -576,8 +591,9 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     // the later phases' inputs (issued with the first group)
-    if (!mbar_wait(ld2_bar, ld_phase ^ 1u)) abort_all();
-    else ld2_inflight = false;
+    if (!mbar_wait(ldr_bar, ph_r)) abort_all();
+    else ldr_inflight = false;
+    ph_r ^= 1u;
     if (n < C) {
       const int m = C - n;
       for (int i = tid; i < 16 * m; i += 256) {
@@ -770,6 +786,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     mma_wait();
     if (*sAbort) goto done;
+    // every reader of the saves and d_o regions is done: the next item's
+    // group A loads while this item's final readout runs
+    if (item + gridDim.x < n_items) {
+      if (warp == 0) issue_a(item + gridDim.x);
+      lda_inflight = true;
+    }
 
     // ---- final: this thread's channel c = L and rows 32 hh .. 32 hh + 31
     {
@@ -778,9 +800,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int i = 0; i < kNumSub; ++i) E[i] = Gat(16 * i + 15, ch);
       const float GC = E[kNumSub - 1];
-      // dG per row into shared memory ([row][channel] fp32, over the decayed
-      // products' operands, which the MMAs above were the last to read)
-      float *sDG = reinterpret_cast<float *>(smem + OKK);
+      // dG per row into shared memory ([row][channel] fp32, over v, T and
+      // K e^G, whose last readers were the T products)
+      float *sDG = reinterpret_cast<float *>(smem + VV);
       float gsum = 0.f, gcp = 0.f;
       // the bf16 values the MMAs read, recomputed bit for bit as the operand
       // build formed them (same expressions, round to nearest even)
@@ -877,8 +899,9 @@ __global__ void __launch_bounds__(256, 1)
 
 done:
   if (tid == 0) {
-    if (ld_inflight) mbar_wait(ld_bar, ld_phase);
-    if (ld2_inflight) mbar_wait(ld2_bar, ld_inflight ? ld_phase : ld_phase ^ 1u);
+    if (lda_inflight) mbar_wait(lda_bar, ph_a);
+    if (ldg_inflight) mbar_wait(ldg_bar, ph_g);
+    if (ldr_inflight) mbar_wait(ldr_bar, ph_r);
     if (mma_inflight) mbar_wait(mma_bar, (n_mma - 1) & 1u);
   }
   tc_fence_before();
