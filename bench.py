@@ -498,9 +498,49 @@ def run_ours(args, dist):
                                        "bwd_chain_kernel + bwd_grad_kernel") if tc
                             else "bwd_simt_kernel + bwd_reduce_kernel"},
                "impl": "tc" if tc else "simt",
-               # tensor cores: prep, recurrence (save), chain, gradients;
+               # tensor cores: prep, recurrence (save), chain, gradients (with
+               # segment ids also the run builder and the padding zero-fill);
                # CUDA cores: (runs +) the backward kernel + the reduction
-               "gpu_launches": steps * (4 if tc else (3 if has_seg else 2))}
+               "gpu_launches": steps * ((6 if has_seg else 4) if tc else (3 if has_seg else 2))}
+        if tc:
+            # a training step without repeated work: the forward that saves
+            # (kda_chunk_fwd_save), then the backward on its saves
+            # (kda_chunk_bwd_from_saved); each timed alone and as the pair
+            tws = torch.zeros(kda.fwd_save_workspace_size(w.B, w.T, w.H, w.K, w.V, d["q"].dtype,
+                                                          has_seg),
+                              dtype=torch.uint8, device=dev)
+
+            def fwd_save():
+                kda.chunk_fwd_save(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                                   initial_state=d["initial_state"],
+                                   segment_ids=d["segment_ids"], workspace=tws, stream=stream)
+
+            def bwd_saved():
+                kda.chunk_bwd_from_saved(d["q"], d["k"], d["v"], d["g"], d["beta"], d_o, tws,
+                                         scale=x["scale"], initial_state=d["initial_state"],
+                                         segment_ids=d["segment_ids"], d_final=d_f,
+                                         stream=stream)
+
+            def pair():
+                fwd_save()
+                bwd_saved()
+
+            t_f, _ = time_steps(fwd_save, steps, args.warmup, stream, flush, dist, clocks)
+            t_b, _ = time_steps(bwd_saved, steps, args.warmup, stream, flush, dist, clocks)
+            t_p, _ = time_steps(pair, steps, args.warmup, stream, flush, dist, clocks)
+            ms_p = dist.max(statistics.mean(t_p))
+            res["training_step"] = {
+                "fwd_save_ms": dist.max(statistics.mean(t_f)),
+                "bwd_from_saved_ms": dist.max(statistics.mean(t_b)),
+                "ms_per_step": ms_p, "unit": "tokens/s",
+                "value": whole_job_value(dist.world, w.B * w.T, ms_p),
+                "note": "forward (o, final state, saves) + backward from the saves; "
+                        "against the separate forward and backward calls",
+                # fwd_save: prep + recurrence; bwd_from_saved: chain + gradients,
+                # each alone and as the pair (with segment ids also the run
+                # builder in both and the padding zero-fill in the backward)
+                "gpu_launches": steps * (14 if has_seg else 8)}
+            res["gpu_launches"] += res["training_step"]["gpu_launches"]
         if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline_backward(w, args.seed, budget_s=args.cpu_seconds / 2)
         return res

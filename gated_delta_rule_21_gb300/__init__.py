@@ -107,6 +107,13 @@ def lib():
         L.kda_chunk_bwd_workspace_size_for.restype = u64
         L.kda_chunk_bwd_workspace_size_packed.argtypes = [sp, i]
         L.kda_chunk_bwd_workspace_size_packed.restype = u64
+        L.kda_chunk_fwd_save_workspace_size.argtypes = [sp, i]
+        L.kda_chunk_fwd_save_workspace_size.restype = u64
+        L.kda_chunk_fwd_save.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, u64, vp]
+        L.kda_chunk_fwd_save.restype = i
+        L.kda_chunk_bwd_from_saved.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp,
+                                               vp, vp, vp, vp, vp, vp, u64, vp]
+        L.kda_chunk_bwd_from_saved.restype = i
         L.kda_chunk_bwd_ex.argtypes = [sp, vp, vp, vp, vp, vp, f, i, vp, vp, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, u64, i, vp]
         L.kda_chunk_bwd_ex.restype = i
@@ -371,6 +378,81 @@ def chunk_bwd(q, k, v, g, beta, d_o, scale=None, chunk_size=CHUNK, initial_state
         _stream_ptr(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_bwd_ex")
+    return dq, dk, dv, dg, dbeta, d_init
+
+
+def fwd_save_workspace_size(B, T, H, K, V, dtype=torch.bfloat16, has_segment_ids=False) -> int:
+    """Workspace bytes of chunk_fwd_save (0 when that path does not apply)."""
+    s = make_shape(B, T, H, K, V, dtype)
+    return int(lib().kda_chunk_fwd_save_workspace_size(ctypes.byref(s), int(bool(has_segment_ids))))
+
+
+def chunk_fwd_save(q, k, v, g, beta, scale=None, chunk_size=CHUNK, initial_state=None,
+                   segment_ids=None, output_final_state=True, workspace=None, stream=None):
+    """The forward of a training step (``kda_chunk_fwd_save``): returns
+    ``(o, final_state or None, workspace)``, o and the final state as
+    chunk_fwd's split path computes them, the workspace holding what
+    chunk_bwd_from_saved reads.  bf16, K = V = 128."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("chunk_fwd_save needs CUDA tensors")
+    dt = q.dtype
+    _check(q, "q", (B, T, H, K), dt, dev)
+    _check(k, "k", (B, T, H, K), dt, dev)
+    _check(v, "v", (B, T, H, V), dt, dev)
+    _check(g, "g", (B, T, H, K), torch.float32, dev)
+    _check(beta, "beta", (B, T, H), torch.float32, dev)
+    _check(initial_state, "initial_state", (B, H, K, V), torch.float32, dev)
+    _check(segment_ids, "segment_ids", (B, T), torch.int32, dev)
+    if scale is None:
+        scale = K ** -0.5
+    o = torch.empty(B, T, H, V, dtype=dt, device=dev)
+    fs = torch.empty(B, H, K, V, dtype=torch.float32, device=dev) if output_final_state else None
+    if workspace is None:
+        n = fwd_save_workspace_size(B, T, H, K, V, dt, segment_ids is not None)
+        if n == 0:
+            raise KdaError(2, "kda_chunk_fwd_save_workspace_size")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_fwd_save(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        int(chunk_size), _ptr(initial_state), _ptr(segment_ids), _ptr(o), _ptr(fs),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_save")
+    return o, fs, workspace
+
+
+def chunk_bwd_from_saved(q, k, v, g, beta, d_o, workspace, scale=None, chunk_size=CHUNK,
+                         initial_state=None, segment_ids=None, d_final=None,
+                         want_d_initial=True, stream=None):
+    """The backward of a training step (``kda_chunk_bwd_from_saved``) on the
+    workspace a chunk_fwd_save of the same inputs left: returns the
+    gradients as chunk_bwd."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    dt = q.dtype
+    _check(d_o, "d_o", (B, T, H, V), dt, dev)
+    _check(d_final, "d_final", (B, H, K, V), torch.float32, dev)
+    if scale is None:
+        scale = K ** -0.5
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty(B, T, H, K, **f32) for _ in range(3))
+    dv = torch.empty(B, T, H, V, **f32)
+    dbeta = torch.empty(B, T, H, **f32)
+    d_init = torch.empty(B, H, K, V, **f32) if want_d_initial else None
+    s = make_shape(B, T, H, K, V, dt)
+    st = lib().kda_chunk_bwd_from_saved(
+        ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        int(chunk_size), _ptr(initial_state), _ptr(segment_ids), _ptr(d_o), _ptr(d_final),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(d_init), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream_ptr(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_bwd_from_saved")
     return dq, dk, dv, dg, dbeta, d_init
 
 

@@ -376,13 +376,17 @@ kda_status kda_chunk_bwd(const kda_shape *s, const void *q, const void *k, const
                           workspace_bytes, KDA_IMPL_AUTO, stream);
 }
 
-kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, const void *v,
-                            const float *g, const float *beta, float scale, int chunk_size,
-                            const float *initial_state, const int32_t *segment_ids,
-                            const void *d_o, const float *d_final, float *dq, float *dk,
-                            float *dv, float *dg, float *dbeta, float *d_initial,
-                            void *workspace, size_t workspace_bytes, kda_impl impl,
-                            kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// kda_chunk_bwd_ex and kda_chunk_bwd_from_saved (from_saved: the
+// tensor-core path on the items and saves a kda_chunk_fwd_save left).
+kda_status bwd_entry(const kda_shape *s, const void *q, const void *k, const void *v,
+                     const float *g, const float *beta, float scale, int chunk_size,
+                     const float *initial_state, const int32_t *segment_ids, const void *d_o,
+                     const float *d_final, float *dq, float *dk, float *dv, float *dg,
+                     float *dbeta, float *d_initial, void *workspace, size_t workspace_bytes,
+                     kda_impl impl, bool from_saved, kda_stream_t stream) {
   kda_status st = check_shape(s);
   if (st != KDA_OK) return st;
   if (!bwd_supported(s->K, s->V)) return KDA_ERR_UNSUPPORTED;
@@ -449,7 +453,8 @@ kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, co
       if (e != cudaSuccess) return from_cuda(e);
     }
     return from_cuda(launch_bwd_tc(p, segment_ids, workspace, workspace_bytes, dq, dk, dg,
-                                   dbeta, &reinterpret_cast<WsHeader *>(ws)->status, cs));
+                                   dbeta, &reinterpret_cast<WsHeader *>(ws)->status, cs,
+                                   from_saved));
   }
   if (has_seg) {
     // Runs; dv = 0 on padding; d_initial = d_final (or 0) for rows without a run.
@@ -459,6 +464,79 @@ kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, co
   }
   return from_cuda(launch_bwd(p, s->qkv_dtype == KDA_DTYPE_BF16, segment_ids, dq, dk, dg,
                               dbeta, cs));
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, float scale, int chunk_size,
+                            const float *initial_state, const int32_t *segment_ids,
+                            const void *d_o, const float *d_final, float *dq, float *dk,
+                            float *dv, float *dg, float *dbeta, float *d_initial,
+                            void *workspace, size_t workspace_bytes, kda_impl impl,
+                            kda_stream_t stream) {
+  return bwd_entry(s, q, k, v, g, beta, scale, chunk_size, initial_state, segment_ids, d_o,
+                   d_final, dq, dk, dv, dg, dbeta, d_initial, workspace, workspace_bytes, impl,
+                   false, stream);
+}
+
+size_t kda_chunk_fwd_save_workspace_size(const kda_shape *s, int has_segment_ids) {
+  return kda_chunk_bwd_workspace_size_for(s, has_segment_ids, KDA_IMPL_TC);
+}
+
+kda_status kda_chunk_fwd_save(const kda_shape *s, const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, float scale, int chunk_size,
+                              const float *initial_state, const int32_t *segment_ids, void *o,
+                              float *final_state, void *workspace, size_t workspace_bytes,
+                              kda_stream_t stream) {
+  kda_status st = check_shape(s);
+  if (st != KDA_OK) return st;
+  if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+  if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return KDA_ERR_INVALID_ARG;
+  if (!bwd_tc_supported(s->K, s->V, s->qkv_dtype == KDA_DTYPE_BF16)) return KDA_ERR_UNSUPPORTED;
+  const void *ptrs[] = {q, k, v, g, beta, o, initial_state, final_state, segment_ids};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned(ptr, 16)) return KDA_ERR_ALIGNMENT;
+  const bool has_seg = segment_ids != nullptr;
+  if (!workspace || workspace_bytes < bwd_tc_workspace_bytes(s->B, s->T, s->H, has_seg, 0))
+    return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = s->B; p.T = s->T; p.H = s->H; p.K = s->K; p.V = s->V;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.scale = scale;
+  p.initial_state = initial_state;
+  p.o = o;
+  p.final_state = final_state;
+  char *ws = static_cast<char *>(workspace);
+  p.status = &reinterpret_cast<WsHeader *>(ws)->status;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (has_seg) {
+    p.runs.row_offsets = reinterpret_cast<const int32_t *>(ws + sizeof(WsHeader));
+    p.runs.runs = reinterpret_cast<const int2 *>(ws + sizeof(WsHeader) +
+                                                 ws_row_offsets_bytes(s->B));
+    p.runs.total_runs = &reinterpret_cast<WsHeader *>(ws)->total_runs;
+    cudaError_t e = launch_segment_runs(s->B, s->T, s->H, s->K, s->V, segment_ids, o, 1,
+                                        initial_state, final_state, workspace, cs, true);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return from_cuda(launch_fwd_save(p, workspace, workspace_bytes, cs));
+}
+
+kda_status kda_chunk_bwd_from_saved(const kda_shape *s, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    float scale, int chunk_size, const float *initial_state,
+                                    const int32_t *segment_ids, const void *d_o,
+                                    const float *d_final, float *dq, float *dk, float *dv,
+                                    float *dg, float *dbeta, float *d_initial,
+                                    void *workspace, size_t workspace_bytes,
+                                    kda_stream_t stream) {
+  return bwd_entry(s, q, k, v, g, beta, scale, chunk_size, initial_state, segment_ids, d_o,
+                   d_final, dq, dk, dv, dg, dbeta, d_initial, workspace, workspace_bytes,
+                   KDA_IMPL_TC, true, stream);
 }
 
 }  // extern "C"

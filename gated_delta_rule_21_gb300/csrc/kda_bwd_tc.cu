@@ -950,9 +950,14 @@ size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_pe
   return split::bwd_tc_workspace_bytes(B, T, H, has_seg, max_runs_per_row);
 }
 
+cudaError_t launch_fwd_save(const FwdParams &p, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return launch_fwd_for_bwd(p, workspace, workspace_bytes, nullptr, stream, true);
+}
+
 cudaError_t launch_bwd_tc(const BwdParams &bp, const int32_t *segment_ids, void *workspace,
                           size_t workspace_bytes, float *dq, float *dk, float *dg, float *dbeta,
-                          uint32_t *status, cudaStream_t stream) {
+                          uint32_t *status, cudaStream_t stream, bool from_saved) {
   if (bp.K != KD || bp.V != VD || (segment_ids != nullptr) != (bp.runs.runs != nullptr))
     return cudaErrorNotSupported;
   FwdParams fp;
@@ -964,8 +969,13 @@ cudaError_t launch_bwd_tc(const BwdParams &bp, const int32_t *segment_ids, void 
   fp.status = status;
   fp.runs = bp.runs;
   BwdLayout lay;
-  cudaError_t e = launch_fwd_for_bwd(fp, workspace, workspace_bytes, &lay, stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (from_saved) {  // a saving forward on the same inputs left items and saves
+    if (!bwd_layout(fp, workspace, workspace_bytes, &lay)) return cudaErrorInvalidValue;
+  } else {
+    e = launch_fwd_for_bwd(fp, workspace, workspace_bytes, &lay, stream);
+    if (e != cudaSuccess) return e;
+  }
 
   BwdTcParams p;
   memset(&p, 0, sizeof(p));

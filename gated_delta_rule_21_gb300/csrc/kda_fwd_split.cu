@@ -675,8 +675,9 @@ struct ScanParams {
   int n_segs, cps;
   float *maps;
   float *starts;
-  // Save pass for the backward (MODE = 2): per (chunk, head), at the item's
-  // index, SV_BYTES holding the state entering the chunk and U (bf16).
+  // Saves for the backward (MODE = 2, or MODE = 0 when set): per (chunk,
+  // head), at the item's index, SV_BYTES holding the state entering the
+  // chunk and U (bf16).
   unsigned char *save;
 };
 
@@ -713,9 +714,9 @@ struct RecLayout {
 // D2 is issued before the o product, so the state update, and with it the
 // next chunk's first MMA, waits only for the products on the serial chain;
 // the o product runs on the tensor pipe while the CUDA cores update S.
-// MODE 0: the forward; 1: the scan's map pass (see ScanParams); 2: the
-// backward's save pass (no outputs; each chunk's entering state and U are
-// written to sc.save).
+// MODE 0: the forward (which also saves like MODE 2 when sc.save is set);
+// 1: the scan's map pass (see ScanParams); 2: the backward's save pass (no
+// outputs; each chunk's entering state and U are written to sc.save).
 template <int VTR, int NST, int MODE>
 __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     fwd_rec_kernel(const FwdParams p, const unsigned char *items, const ChunkTable ct,
@@ -819,6 +820,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
   float S[CPT];  // S[key row L][col0 .. col0 + CPT - 1], fp32
   const bool fits = total_chunk_count(ct, p.B) <= ct.capacity;
   constexpr bool MAP = MODE == 1, SAVE = MODE == 2;
+  // the forward also saves for the backward when given a save area
+  const bool save_on = SAVE || (MODE == 0 && sc.save != nullptr);
   const int seg_units = MAP ? sc.n_segs - 1 : sc.n_segs;
   const uint32_t n_units =
       !fits ? 0u
@@ -909,8 +912,8 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
       const unsigned char *stg = smem + (uint32_t)s * Lay::STAGE;
       const uint32_t sstg = sb + (uint32_t)s * Lay::STAGE;
       const uint32_t d1 = Lay::TM_D1 + (uint32_t)VTR * (uint32_t)(c & 1);
-      unsigned char *sv = SAVE ? sc.save + ((size_t)(cbase + c) * H + h) * SV_BYTES : nullptr;
-      if (SAVE) {  // the state entering this chunk
+      unsigned char *sv = save_on ? sc.save + ((size_t)(cbase + c) * H + h) * SV_BYTES : nullptr;
+      if (save_on) {  // the state entering this chunk
 #pragma unroll
         for (int e = 0; e < CPT / 8; ++e) {
           float t8[8];
@@ -943,7 +946,7 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) a[i] = uu[i] - v[8 * e + i];
           st_bf16x8(smem, Lay::UT + mn_off(col, r, C), a);
-          if (SAVE) st_g16(sv, SV_U + op_off(r, vc0 + col, KD), a);
+          if (save_on) st_g16(sv, SV_U + op_off(r, vc0 + col, KD), a);
         }
       }
       fence_proxy_async();
@@ -1345,31 +1348,46 @@ size_t split::bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_
 // Items of ITEM_BYTES_BWD (the forward's, plus T, A_kk and K e^G), then the
 // recurrence in its save mode: the state entering every chunk and U, no o
 // and no final state.
-cudaError_t split::launch_fwd_for_bwd(const FwdParams &p_in, void *workspace,
-                                      size_t workspace_bytes, BwdLayout *out,
-                                      cudaStream_t stream) {
+bool split::bwd_layout(const FwdParams &p_in, void *workspace, size_t workspace_bytes,
+                       BwdLayout *out) {
   const bool has_seg = p_in.runs.runs != nullptr;
-  if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, 0)) return cudaErrorNotSupported;
   const size_t ioff = items_offset(p_in.B, p_in.T, has_seg);
   const size_t per_chunk = (size_t)p_in.H * ((size_t)ITEM_BYTES_BWD + SV_BYTES);
-  if (workspace_bytes < ioff + per_chunk) return cudaErrorInvalidValue;
+  if (workspace_bytes < ioff + per_chunk) return false;
   // every row's chunks without segment ids; with them, the chunks of all
   // runs (counted on the device; an overflow is reported, nothing is done)
   const size_t cap = (workspace_bytes - ioff) / per_chunk;
-  if (!has_seg && cap < (size_t)p_in.B * ((p_in.T + C - 1) / C)) return cudaErrorInvalidValue;
-  FwdParams p = p_in;
-  p.v_tile = has_seg ? 128 : fit_tile((long)p.B * p.H, VD);
-  p.n_vtiles = VD / p.v_tile;
+  if (!has_seg && cap < (size_t)p_in.B * ((p_in.T + C - 1) / C)) return false;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
-  const size_t items_end = ioff + cap * p.H * ITEM_BYTES_BWD;
+  const size_t items_end = ioff + cap * p_in.H * ITEM_BYTES_BWD;
+  out->items = ws + ioff;
+  out->saves = ws + items_end;
+  out->ct = make_table(p_in, ws, ioff, items_end, ITEM_BYTES_BWD, has_seg, false);
+  return true;
+}
+
+cudaError_t split::launch_fwd_for_bwd(const FwdParams &p_in, void *workspace,
+                                      size_t workspace_bytes, BwdLayout *out,
+                                      cudaStream_t stream, bool with_outputs) {
+  const bool has_seg = p_in.runs.runs != nullptr;
+  if (!fwd_split_supported(p_in.K, p_in.V, true, has_seg, 0)) return cudaErrorNotSupported;
   BwdLayout lay;
-  lay.items = ws + ioff;
-  lay.saves = ws + items_end;
-  lay.ct = make_table(p, ws, ioff, items_end, ITEM_BYTES_BWD, has_seg, false);
+  if (!bwd_layout(p_in, workspace, workspace_bytes, &lay)) return cudaErrorInvalidValue;
+  FwdParams p = p_in;
+  if (with_outputs) {  // the forward's own value tile (as launch_fwd_split)
+    const long bh = (long)p.B * p.H, sms = num_sms();
+    p.v_tile = has_seg ? 128 : (bh * 4 <= sms ? 32 : (bh * 2 <= sms ? 64 : 128));
+  } else {
+    p.v_tile = has_seg ? 128 : fit_tile((long)p.B * p.H, VD);
+    p.o = nullptr;
+    p.final_state = nullptr;
+  }
+  p.n_vtiles = VD / p.v_tile;
   cudaError_t e = launch_prep(p, lay.items, lay.ct, stream);
   if (e != cudaSuccess) return e;
   const ScanParams sc = {0, 0, nullptr, nullptr, lay.saves};
-  e = launch_rec_tile<2>(p, lay.items, lay.ct, has_seg, sc, stream);
+  e = with_outputs ? launch_rec_tile<0>(p, lay.items, lay.ct, has_seg, sc, stream)
+                   : launch_rec_tile<2>(p, lay.items, lay.ct, has_seg, sc, stream);
   if (e == cudaSuccess && out) *out = lay;
   return e;
 }

@@ -152,9 +152,17 @@ cudaError_t launch_bwd(const BwdParams &p, bool bf16, const int32_t *segment_ids
 // workspace; padding tokens get zero gradients.
 bool bwd_tc_supported(int K, int V, bool bf16);
 size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row);
+// from_saved: the items and saves come from a preceding launch_fwd_save
+// on the same inputs and workspace (the forward passes are skipped).
 cudaError_t launch_bwd_tc(const BwdParams &p, const int32_t *segment_ids, void *workspace,
                           size_t workspace_bytes, float *dq, float *dk, float *dg,
-                          float *dbeta, uint32_t *status, cudaStream_t stream);
+                          float *dbeta, uint32_t *status, cudaStream_t stream,
+                          bool from_saved = false);
+// The forward (o, final state of p) that also leaves in the workspace what
+// launch_bwd_tc(from_saved) reads; with segment ids the run builder (with
+// chunk tables) must have run on the workspace.
+cudaError_t launch_fwd_save(const FwdParams &p, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 cudaError_t launch_short_conv(const ConvParams &p, bool bf16,
                               cudaStream_t stream);

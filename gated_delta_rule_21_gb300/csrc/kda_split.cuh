@@ -124,8 +124,13 @@ struct BwdLayout {
 // With segment ids the items and saves are sized for at most
 // max_runs_per_row runs per row (each run adds at most one partial chunk).
 size_t bwd_tc_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per_row);
+// The layout of such a workspace (false when it is too small).
+bool bwd_layout(const FwdParams &p, void *workspace, size_t workspace_bytes, BwdLayout *out);
+// The prep kernel with backward items, then the recurrence saving S and U:
+// in its save mode (no o, no final state), or with with_outputs as the
+// forward itself (o and the final state of p) that also saves.
 cudaError_t launch_fwd_for_bwd(const FwdParams &p, void *workspace, size_t workspace_bytes,
-                               BwdLayout *out, cudaStream_t stream);
+                               BwdLayout *out, cudaStream_t stream, bool with_outputs = false);
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
               uint64_t cols, uint64_t rows, uint32_t box_cols, CUtensorMapSwizzle swz);
 

@@ -443,6 +443,45 @@ KDA_API kda_status kda_chunk_bwd_ex(const kda_shape *s, const void *q, const voi
                                     kda_stream_t stream);
 
 /*
+ * A training step's forward and backward without repeating work: the
+ * forward kda_chunk_fwd_save computes o and final_state exactly as
+ * kda_chunk_fwd's split tensor-core path does (bit for bit) and also
+ * leaves in `workspace` what the tensor-core backward reads (the per-chunk
+ * items with T, A_kk and K e^G, and the state entering every chunk and U);
+ * kda_chunk_bwd_from_saved then runs only the state-gradient chain and the
+ * per-chunk gradient kernel on it, with results bit for bit those of
+ * kda_chunk_bwd_ex(KDA_IMPL_TC) on the same inputs.
+ * Supported: bf16 q/k/v/d_o, K = V = 128, with or without segment ids
+ * (KDA_ERR_UNSUPPORTED otherwise).  Arguments as kda_chunk_fwd and
+ * kda_chunk_bwd; the workspace (256-byte aligned, zero-filled before first
+ * use) must hold kda_chunk_fwd_save_workspace_size bytes (the tensor-core
+ * backward's size; with segment ids any workspace with room for ceil(T/64)
+ * chunks per row is accepted and an overflow is reported as in
+ * kda_chunk_bwd).  The caller passes kda_chunk_bwd_from_saved the same
+ * shape, inputs (unchanged since the forward), segment ids and workspace
+ * as the forward, with nothing written to the workspace in between; the
+ * backward keeps the workspace's contents, so it may run again.  Both calls
+ * are asynchronous on `stream`; errors as kda_chunk_fwd and kda_chunk_bwd.
+ */
+KDA_API size_t kda_chunk_fwd_save_workspace_size(const kda_shape *s, int has_segment_ids);
+KDA_API kda_status kda_chunk_fwd_save(const kda_shape *s, const void *q, const void *k,
+                                      const void *v, const float *g, const float *beta,
+                                      float scale, int chunk_size,
+                                      const float *initial_state,
+                                      const int32_t *segment_ids, void *o,
+                                      float *final_state, void *workspace,
+                                      size_t workspace_bytes, kda_stream_t stream);
+KDA_API kda_status kda_chunk_bwd_from_saved(const kda_shape *s, const void *q, const void *k,
+                                            const void *v, const float *g, const float *beta,
+                                            float scale, int chunk_size,
+                                            const float *initial_state,
+                                            const int32_t *segment_ids, const void *d_o,
+                                            const float *d_final, float *dq, float *dk,
+                                            float *dv, float *dg, float *dbeta,
+                                            float *d_initial, void *workspace,
+                                            size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * Test hook for failure detection (no counterpart in the pages): enqueues
  * one thread that waits, for at most `limit_cycles` SM clocks (1 .. about
  * 2^31), on an mbarrier nothing ever arrives at, using the bounded wait of

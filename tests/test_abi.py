@@ -268,5 +268,36 @@ def test_backward_workspace_size_and_argument_checks(L):
     assert call_ex(2, nbytes=nb - 1) == 4                        # TC: small workspace
     simt_nb = kda.bwd_workspace_size(1, 64, 2, 128, 128, impl="simt")
     assert call_ex(1, nbytes=simt_nb - 1) == 4                   # SIMT: its own size
+    # the training-step pair: the tensor-core backward's workspace and shapes
+    assert kda.fwd_save_workspace_size(1, 64, 2, 128, 128) == \
+        kda.bwd_workspace_size(1, 64, 2, 128, 128, impl="tc")
+    assert kda.fwd_save_workspace_size(1, 64, 2, 64, 64) == 0
+    assert kda.fwd_save_workspace_size(1, 64, 2, 128, 128, torch.float32) == 0
+
+    def call_save(shape=(1, 64, 2, 128, 128, 1), o=FAKE, nbytes=None, chunk=64, ws=FAKE):
+        s2 = kda.kda_shape(*shape)
+        return L.kda_chunk_fwd_save(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                    vp(FAKE), 0.1, chunk, None, None, None if o is None else vp(o),
+                                    None, None if ws is None else vp(ws),
+                                    nb if nbytes is None else nbytes, None)
+    assert call_save(o=None) == 1
+    assert call_save(chunk=32) == 2
+    assert call_save(shape=(1, 64, 2, 64, 64, 1)) == 2
+    assert call_save(shape=(1, 64, 2, 128, 128, 0)) == 2
+    assert call_save(o=FAKE + 2) == 3
+    assert call_save(nbytes=nb - 1) == 4
+    assert call_save(ws=None) == 4
+    assert call_save(ws=FAKE + 16) == 3
+
+    def call_from_saved(shape=(1, 64, 2, 128, 128, 1), nbytes=None, d_o=FAKE):
+        s2 = kda.kda_shape(*shape)
+        return L.kda_chunk_bwd_from_saved(ctypes.byref(s2), vp(FAKE), vp(FAKE), vp(FAKE),
+                                          vp(FAKE), vp(FAKE), 0.1, 64, None, None,
+                                          None if d_o is None else vp(d_o), None, vp(FAKE),
+                                          vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None,
+                                          vp(FAKE), nb if nbytes is None else nbytes, None)
+    assert call_from_saved(d_o=None) == 1
+    assert call_from_saved(shape=(1, 64, 2, 64, 64, 1)) == 2
+    assert call_from_saved(nbytes=nb - 1) == 4
     s48 = kda.kda_shape(1, 64, 2, 128, 48, 1)
     assert L.kda_chunk_bwd_workspace_size(ctypes.byref(s48), 0) == 0

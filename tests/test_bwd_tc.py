@@ -226,3 +226,45 @@ def test_tc_backward_packed_overflow_is_reported():
     ref = _oracle(x, u)
     for name, a, b in zip(NAMES, got, ref):
         _check(name, a, b, "four runs, room for four")
+
+
+TRAIN = {
+    "fixed_t300": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1),
+    "packed": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1,
+                   segments=[[("pad", 3), 100, 1, 1, ("pad", 5), 120, 70],
+                             [64, 64, ("pad", 2), 170]]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(TRAIN))
+def test_training_step_pair_equals_separate_calls(case):
+    """kda_chunk_fwd_save gives chunk_fwd's split-path o and final state bit
+    for bit, and kda_chunk_bwd_from_saved on its workspace gives the
+    tensor-core chunk_bwd's gradients bit for bit (the same kernels on the
+    same items and saves); run twice on one workspace, the backward repeats."""
+    import gated_delta_rule_21_gb300 as kda
+    w = ki.custom_workload(name=case, **TRAIN[case])
+    x, u = _inputs(w, seed=21)
+    dev = lambda t: None if t is None else to_dev(t)
+    d = {n: dev(x[n]) for n in ("q", "k", "v", "g", "beta", "initial_state", "segment_ids")}
+    o_s, fs_s, ws = kda.chunk_fwd_save(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                       scale=x["scale"], initial_state=d["initial_state"],
+                                       segment_ids=d["segment_ids"])
+    o, fs = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"],
+                          initial_state=d["initial_state"], segment_ids=d["segment_ids"],
+                          output_final_state=True, impl="split")
+    torch.cuda.synchronize()
+    assert torch.equal(o_s, o) and torch.equal(fs_s, fs)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], dev(u["d_o"]))
+    kw = dict(scale=x["scale"], initial_state=d["initial_state"],
+              segment_ids=d["segment_ids"], d_final=dev(u["d_final"]))
+    a = kda.chunk_bwd_from_saved(*args, ws, **kw)
+    b = kda.chunk_bwd_from_saved(*args, ws, **kw)
+    c = kda.chunk_bwd(*args, impl="tc", **kw)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(ws) == 0
+    for s_, t_, r_ in zip(a, b, c):
+        assert torch.equal(s_, t_) and torch.equal(s_, r_)
+    ref = _oracle(x, u)
+    for name, got, r in zip(NAMES, a, ref):
+        _check(name, got.cpu().numpy(), r, f"{case} from saved")
