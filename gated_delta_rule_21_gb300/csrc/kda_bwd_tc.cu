@@ -62,11 +62,12 @@ struct BwdTcParams {
 constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) / 1024u * 1024u; }
 
 // ---- the dS chain ---------------------------------------------------------------
-// A stage holds the item's [w ; Q e^G] | A_qk | (K e^{G_C-G})^T (one copy),
-// this unit's d_o columns (VTR / 8 boxes of 64 rows x 8, scaled by `scale`
-// in place and zero past the chunk's end) and e^{G_C}.  Per chunk:
-//   D_U  = A_qk^T (s dO) + K^ dS'        (u barrier; dU = D_U rows 0..63)
-//   D_S  = Q~^T (s dO) + w^T (-dU)       (s barrier; dS = gam dS' + D_S)
+// A stage holds the item's [w ; s Q e^G] | s A_qk | (K e^{G_C-G})^T (one
+// copy; the prep folds the attention scale s into Q e^G and A_qk), this
+// unit's d_o columns (VTR / 8 boxes of 64 rows x 8, zero past the chunk's
+// end) and e^{G_C}.  Per chunk:
+//   D_U  = (s A_qk)^T dO + K^ dS'        (u barrier; dU = D_U rows 0..63)
+//   D_S  = (s Q~)^T dO + w^T (-dU)       (s barrier; dS = gam dS' + D_S)
 // A_qk^T and K^ are read from the stored A_qk and K^^T through the
 // transposed view; Q~^T and w^T from [w ; Q e^G] as K-major operands.
 template <int VTR>
@@ -210,18 +211,14 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
       if (!mbar_wait(bar0 + 8u * s, st_phase[s])) abort_all();
       else st_issued &= ~(1u << s);
       st_phase[s] ^= 1u;
-      // ---- s dO in place; rows past the chunk's end zero
-      for (int j = tid; j < VTR * 8; j += Lay::THREADS) {
-        const int r = j & 63;
-        uint4 *ptr = reinterpret_cast<uint4 *>(stg + Lay::S_DO + 1024u * (j >> 6) + 16u * r);
-        if (r >= n) {
-          *ptr = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          float x[8];
-          ld_bf16x8(reinterpret_cast<const unsigned char *>(ptr), x);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) x[k] *= p.scale;
-          st_bf16x8(reinterpret_cast<unsigned char *>(ptr), 0, x);
+      // ---- d_o rows past the chunk's end zero (the items' A_qk and Q e^G
+      //      carry the scale, so d_o is used as loaded)
+      if (n < C) {
+        const int m = C - n;
+        for (int j = tid; j < (VTR / 8) * m; j += Lay::THREADS) {
+          const int r = n + j % m;
+          *reinterpret_cast<uint4 *>(stg + Lay::S_DO + 1024u * (j / m) + 16u * r) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async();
@@ -230,13 +227,13 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
       if (*sAbort) goto done;
       if (tid == 0) {
         tc_fence_after();
-        // D_U = A_qk^T (s dO) + K^ dS'
+        // D_U = (s A_qk)^T dO + K^ dS'
         mma_k(tmem + Lay::TM_U, Opnd{sstg + I_AQK, 1024, 128}, 1,
               Opnd{sstg + Lay::S_DO, 128, 1024}, 1, 4, VTR, false);
         mma_k(tmem + Lay::TM_U, Opnd{sstg + I_KHT, 1024, 128}, 1,
               Opnd{sb + Lay::DST, 128, 2048}, 1, 8, VTR, true);
         commit(u_bar, c_u);
-        // D_S = Q~^T (s dO), completed below by w^T (-dU)
+        // D_S = (s Q~)^T dO, completed below by w^T (-dU)
         mma_k(tmem + Lay::TM_S, Opnd{sstg + I_WQ + 16384, 2048, 128}, 0,
               Opnd{sstg + Lay::S_DO, 128, 1024}, 1, 4, VTR, false);
       }

@@ -8,15 +8,16 @@
 //      blocked), and [w | u] = T diag(beta) [K e^G | V] on tcgen05, and
 //      writes the operands the recurrence needs into the workspace, already
 //      in the shared-memory layouts the tensor cores read:
-//         [w ; Q e^G] (128 x 128 bf16), A_qk (64 x 64 bf16),
-//         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 bf16), e^{G_C}.
+//         [w ; scale Q e^G] (128 x 128 bf16), scale A_qk (64 x 64 bf16),
+//         (K e^{G_C - G})^T (128 x 64 bf16), u (64 x 128 bf16), e^{G_C}
+//      (the attention scale is folded into the Q e^G and A_qk operands).
 //   2. fwd_rec_kernel: one CTA per (row, head, value tile of 32 or 64
 //      columns) walks
 //      the chunks in order with the fp32 state in registers; per chunk it
 //      bulk-copies the item (double-buffered) and runs only the
 //      state-dependent MMAs:  D1 = [w ; Q e^G] S,  U = u - w S,
 //      D1 += [0 ; A_qk] U,  D2 = (K e^{G_C-G})^T U,  S <- e^{G_C} S + D2,
-//      o = scale * D1[64:128].
+//      o = D1[64:128] (already scaled).
 //
 // The arithmetic is the same chunk form, sub-block factors and rounding
 // points as the fused kernel (kda_fwd_tc.cu); see there for the algebra.
@@ -349,6 +350,7 @@ __global__ void __launch_bounds__(PT, 2)
       const float E3 = eb + 1 < kNumSub ? E2 + bs[min(eb + 1, kNumSub - 1)] : E2;
       const float E4 = eb + 2 < kNumSub ? E3 + bs[min(eb + 2, kNumSub - 1)] : E3;
       const float pre = ex2(P2);        // e^{G before the block}
+      const float pre_s = pre * p.scale;
       const float suf = ex2(GC2 - E2);  // e^{G_C - E_b}
       const float rD = ex2(P2 - E2);    // 1 / D_b
       const float x2 = ex2(E3 - E2);    // D_{b+1}
@@ -396,7 +398,8 @@ __global__ void __launch_bounds__(PT, 2)
             *reinterpret_cast<uint4 *>(smem + P_KT + op_off(ch, r8, C)) = kt;
             if (bwd_items) *reinterpret_cast<uint4 *>(gi + I_KT + op_off(ch, r8, C)) = kt;
           }
-          *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8x2s(xq, pre);
+          // scale folded in: the o rows of D1 and the o product come out scaled
+          *reinterpret_cast<uint4 *>(gi + I_WQ + mn_off(64 + r8, ch, KD)) = pack8x2s(xq, pre_s);
           *reinterpret_cast<uint4 *>(gi + I_KHT + op_off(ch, r8, C)) = pack8x2s(ke, suf);
         }
       };
@@ -466,8 +469,8 @@ __global__ void __launch_bounds__(PT, 2)
             float a0[8], a1[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              a0[i] = (j0 + i <= r) ? v[e][i] : 0.f;
-              a1[i] = (j0 + 8 + i <= r) ? v[e][8 + i] : 0.f;
+              a0[i] = (j0 + i <= r) ? p.scale * v[e][i] : 0.f;
+              a1[i] = (j0 + 8 + i <= r) ? p.scale * v[e][8 + i] : 0.f;
             }
             st_g16(gi, I_AQK + op_off(r, j0, C), a0);
             st_g16(gi, I_AQK + op_off(r, j0 + 8, C), a1);
@@ -1014,10 +1017,10 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < CPT / 8; ++e) {
             uint4 w;
-            w.x = pack_bf16(p.scale * v[8 * e + 0], p.scale * v[8 * e + 1]);
-            w.y = pack_bf16(p.scale * v[8 * e + 2], p.scale * v[8 * e + 3]);
-            w.z = pack_bf16(p.scale * v[8 * e + 4], p.scale * v[8 * e + 5]);
-            w.w = pack_bf16(p.scale * v[8 * e + 6], p.scale * v[8 * e + 7]);
+            w.x = pack_bf16(v[8 * e + 0], v[8 * e + 1]);  // D1's o rows carry the scale
+            w.y = pack_bf16(v[8 * e + 2], v[8 * e + 3]);
+            w.z = pack_bf16(v[8 * e + 4], v[8 * e + 5]);
+            w.w = pack_bf16(v[8 * e + 6], v[8 * e + 7]);
             dst[e] = w;
           }
         }

@@ -20,8 +20,10 @@ constexpr int VT = 32;
 // ---- one workspace item (per row, chunk, head) ----------------------------
 // Each region is already in the shared-memory operand layout the recurrence
 // kernel's MMAs read, so a stage is a plain bulk copy of the item.
-constexpr uint32_t I_WQ = 0;          // [w ; Q e^G]: MN-major, 128 rows x Kd 128 channels
-constexpr uint32_t I_AQK = 32768;     // A_qk: K-major, 64 rows, Kd 64
+// Q e^G and A_qk carry the attention scale (folded in by the prep), so the
+// products that read them come out scaled.
+constexpr uint32_t I_WQ = 0;          // [w ; scale Q e^G]: MN-major, 128 rows x Kd 128 channels
+constexpr uint32_t I_AQK = 32768;     // scale A_qk: K-major, 64 rows, Kd 64
 constexpr uint32_t I_KHT = 40960;     // (K e^{G_C-G})^T: K-major, 128 channels x Kd 64 rows
 constexpr uint32_t I_U = 57344;       // u bf16, 4 tiles of 32 columns, see u_off
 constexpr uint32_t I_GAM = 73728;     // e^{G_C} fp32 [128]
