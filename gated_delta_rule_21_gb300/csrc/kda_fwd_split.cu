@@ -93,6 +93,8 @@ constexpr uint32_t P_TF = P_AKK + 64 * LDF * 4;    // fp32 64 x 68 (T)
 constexpr uint32_t P_SCR = P_TF + 64 * LDF * 4;    // 10 blocks of 16 x LDS fp32
 constexpr int LDS = 20;                            // padded: conflict-free rows
 static_assert(P_SCR + 10 * 16 * LDS * 4 <= P_Y, "solver buffers stay in RAW + X");
+static_assert(LDF % 4 == 0 && LDS % 4 == 0 && P_TF % 16 == 0 && P_SCR % 16 == 0,
+              "16-byte rows for the block products' vector loads");
 static_assert(P_TB + 16384 <= P_V + 16384, "the u product's 128-row A operand stays in smem");
 static_assert(P_X % 1024 == 0 && P_Y % 1024 == 0 && P_KT % 1024 == 0 && P_V % 1024 == 0,
               "operand alignment");
@@ -120,24 +122,37 @@ __device__ __forceinline__ void piece(int quad, int i, int &b, int &pp) {
 
 // One 16 x 16 block product on the CUDA cores by one warp (e = lane: rows
 // e / 4 and e / 4 + 8, four columns each): dst = sgn X Y + add_sgn add.
+// Column pairs accumulate in packed f32x2 registers (each lane an ordinary
+// fp32 FMA, in the same order over t as the scalar loop), and X is read
+// four k-steps per 16-byte load (ldx and the row starts are multiples of 4).
 __device__ __forceinline__ void blk_prod(float *dst, int ldd, const float *X, int ldx,
                                          const float *Y, int ldy, float sgn, const float *add,
                                          int lda, int e, float add_sgn = -1.f) {
   const int r = e >> 2, c4 = (e & 3) * 4;
-  float a[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  u64 a[2][2] = {{0ull, 0ull}, {0ull, 0ull}};  // [row r | r + 8][columns c4.. | c4 + 2..]
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const float x0 = X[r * ldx + t], x1 = X[(r + 8) * ldx + t];
-    const float4 y = *reinterpret_cast<const float4 *>(Y + t * ldy + c4);
-    a[0][0] = fmaf(x0, y.x, a[0][0]); a[0][1] = fmaf(x0, y.y, a[0][1]);
-    a[0][2] = fmaf(x0, y.z, a[0][2]); a[0][3] = fmaf(x0, y.w, a[0][3]);
-    a[1][0] = fmaf(x1, y.x, a[1][0]); a[1][1] = fmaf(x1, y.y, a[1][1]);
-    a[1][2] = fmaf(x1, y.z, a[1][2]); a[1][3] = fmaf(x1, y.w, a[1][3]);
+  for (int t4 = 0; t4 < 4; ++t4) {
+    const float4 x0 = *reinterpret_cast<const float4 *>(X + r * ldx + 4 * t4);
+    const float4 x1 = *reinterpret_cast<const float4 *>(X + (r + 8) * ldx + 4 * t4);
+    const float xa[4] = {x0.x, x0.y, x0.z, x0.w}, xb[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const float4 y = *reinterpret_cast<const float4 *>(Y + (4 * t4 + tt) * ldy + c4);
+      const u64 y01 = pk2(y.x, y.y), y23 = pk2(y.z, y.w);
+      const u64 xa2 = pk2(xa[tt], xa[tt]), xb2 = pk2(xb[tt], xb[tt]);
+      a[0][0] = fma2(xa2, y01, a[0][0]);
+      a[0][1] = fma2(xa2, y23, a[0][1]);
+      a[1][0] = fma2(xb2, y01, a[1][0]);
+      a[1][1] = fma2(xb2, y23, a[1][1]);
+    }
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int rr = r + 8 * h;
-    float4 o = make_float4(sgn * a[h][0], sgn * a[h][1], sgn * a[h][2], sgn * a[h][3]);
+    float4 o;
+    upk2(a[h][0], o.x, o.y);
+    upk2(a[h][1], o.z, o.w);
+    o = make_float4(sgn * o.x, sgn * o.y, sgn * o.z, sgn * o.w);
     if (add) {
       const float4 z = *reinterpret_cast<const float4 *>(add + rr * lda + c4);
       o.x = fmaf(add_sgn, z.x, o.x);
