@@ -338,8 +338,14 @@ constexpr uint32_t LOADA_TX = SV_BYTES + 16384;
 constexpr uint32_t LOADG_TX = 32768;
 constexpr uint32_t LOADR_TX = 16384 + 8192 + 16384 + 16384 * 2;
 // after the first products
-constexpr uint32_t DAQ = 0;              // scale dO U^T (j <= r), op_off(r, j, 64)
-constexpr uint32_t DAK = 8192;           // diag(beta) dL, op_off(r, j, 64)
+// dA tiles, 16 KiB: per 16-row block b, the block's rows of scale dO U^T
+// (j <= r; "q") then of diag(beta) dL ("k"), each K-major over j, so the
+// two form one 32-row operand for the block's row sums
+constexpr uint32_t DA = 0;
+__host__ __device__ constexpr uint32_t da_off(int kq, int r, int j) {
+  return 4096u * (uint32_t)(r >> 4) + 2048u * (uint32_t)kq +
+         (uint32_t)((r & 7) * 16 + ((r >> 3) & 1) * 1024 + (j >> 3) * 128 + (j & 7) * 2);
+}
 constexpr uint32_t DTS = 16384;          // dT = dT' diag(beta), op_off(r, j, 64)
 constexpr uint32_t DTU = 24576;          // dT', mn_off(j, r, 64)
 constexpr uint32_t PP = 32768;           // P = dT T^T, mn_off(b, r, 64)
@@ -456,6 +462,16 @@ __global__ void __launch_bounds__(256, 1)
   };
   if (warp == 0 && blockIdx.x < n_items) issue_a(blockIdx.x);
   lda_inflight = blockIdx.x < n_items;
+  // beta of an item's rows (threads < C), loaded one item ahead into a
+  // register so the load's latency is spent while the previous item computes
+  auto load_beta = [&](uint32_t it) -> float {
+    const int hx = (int)(it % (uint32_t)H);
+    int bx, tx, ex;
+    chunk_of(ct, T, it / (uint32_t)H, bx, tx, ex);
+    return tid < min(C, ex - tx) ? p.beta[((size_t)bx * T + tx + tid) * H + hx] : 0.f;
+  };
+  float beta_next = 0.f;
+  if (tid < C && blockIdx.x < n_items) beta_next = load_beta(blockIdx.x);
   for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int h = (int)(item % (uint32_t)H);
     int b, t0, end;
@@ -487,7 +503,10 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     ldg_inflight = ldr_inflight = true;
-    if (tid < C) sBeta[tid] = tid < n ? p.beta[(tok0 + tid) * H + h] : 0.f;
+    if (tid < C) {
+      sBeta[tid] = beta_next;
+      if (item + gridDim.x < n_items) beta_next = load_beta(item + gridDim.x);
+    }
     if (!mbar_wait(lda_bar, ph_a)) abort_all();
     else lda_inflight = false;
     ph_a ^= 1u;
@@ -583,7 +602,7 @@ __global__ void __launch_bounds__(256, 1)
           float a[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) a[k] = j8 + k <= r ? scale * v[8 * e + k] : 0.f;
-          st_bf16x8(smem, DAQ + op_off(r, j8, C), a);
+          st_bf16x8(smem, DA + da_off(0, r, j8), a);
         }
       }
     }
@@ -719,7 +738,7 @@ __global__ void __launch_bounds__(256, 1)
             db = fmaf(dl, ak[k], db);
             d[k] = ba * dl;
           }
-          st_bf16x8(smem, DAK + op_off(a_, b8, C), d);
+          st_bf16x8(smem, DA + da_off(1, a_, b8), d);
         }
         sDb[64 * (1 + hh) + a_] = db;
       }
@@ -767,17 +786,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int bb = 0; bb < kNumSub; ++bb) {
         const uint32_t sbo = 256u * (bb + 1);
-        // row sums of block bb: [c][r in block bb] = sum_j KK_bb[c][j] dA[r][j]
+        // row sums of block bb: [c][r in block bb, q rows | k rows] =
+        // sum_j KK_bb[c][j] dA[r][j], one N = 32 product over both tiles
         mma_k(tmem + C_ROW + 32 * bb, Opnd{sb + OKK + kk_off(bb), 128, sbo}, 0,
-              Opnd{sb + DAQ + 2048u * bb, 128, 1024}, 0, bb + 1, 16, false);
-        mma_k(tmem + C_ROW + 32 * bb + 16, Opnd{sb + OKK + kk_off(bb), 128, sbo}, 0,
-              Opnd{sb + DAK + 2048u * bb, 128, 1024}, 0, bb + 1, 16, false);
+              Opnd{sb + DA + 4096u * bb, 128, 1024}, 0, bb + 1, 32, false);
         // column sums of block bb: W_bb[c][j] = sum_{r in bb} YK[c][r] dA_kk[r][j]
         //   + YQ[c][r] dA_qk[r][j], j < 16 (bb + 1) (dA read transposed)
         mma_k(tmem + C_W + w_col(bb), Opnd{sb + OYK + 256u * bb, 128, 1024}, 0,
-              Opnd{sb + DAK + 2048u * bb, 1024, 128}, 1, 1, 16 * (bb + 1), false);
+              Opnd{sb + DA + 4096u * bb + 2048u, 1024, 128}, 1, 1, 16 * (bb + 1), false);
         mma_k(tmem + C_W + w_col(bb), Opnd{sb + OYQ + 256u * bb, 128, 1024}, 0,
-              Opnd{sb + DAQ + 2048u * bb, 1024, 128}, 1, 1, 16 * (bb + 1), true);
+              Opnd{sb + DA + 4096u * bb, 1024, 128}, 1, 1, 16 * (bb + 1), true);
       }
       mma_commit(mma_bar);
     }
