@@ -176,6 +176,11 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
         tma_load_2d(dst + Lay::S_DO + 1024u * j, &tm_do, h * VD + vc0 + 8 * j,
                     b * T + u.start + c * C, bar);
     };
+    // the first stages' copies go out before d_final's load, so the two
+    // latencies overlap (the previous unit's MMAs finished before its last
+    // barrier)
+    if (tid == 0)
+      for (int i = 0; i < 2 && i < nc; ++i) issue_stage(i, nc - 1 - i);
     float dS[CPT];  // gradient of the state leaving the chunk, [key L][col0 ..]
     if (u.last && p.d_final) {  // the row's last run leaves the final state
       const float4 *src = reinterpret_cast<const float4 *>(
@@ -189,8 +194,6 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < CPT; ++i) dS[i] = 0.f;
     }
-    if (tid == 0)
-      for (int i = 0; i < 2 && i < nc; ++i) issue_stage(i, nc - 1 - i);
     st_issued = nc >= 2 ? 3u : 1u;
 
     for (int i = 0; i < nc; ++i) {

@@ -881,6 +881,13 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
     auto item_ptr = [&](int c) {
       return items + ((size_t)(cbase + c) * H + h) * ct.item_stride;
     };
+    // the first stages' copies go out before the entering state's load, so
+    // the two latencies overlap (the previous unit's readers of the stages
+    // and of S^T finished before its closing barrier)
+    if (tid == 0) {
+      for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt_u);
+      for (int c = NST; c < NST + kRecPrefetch && c < n_chunks; ++c) prefetch_l2(item_ptr(c), ITEM_BYTES);
+    }
     // state entering the run (or segment); S^T operand (MN-major: v contiguous)
     const float *s_src = nullptr;
     if (!MAP) {
@@ -904,10 +911,6 @@ __global__ void __launch_bounds__(RecLayout<VTR, NST>::THREADS, 1)
       for (int i = 0; i < CPT; ++i) S[i] = 0.f;
     }
     store_st(S, L);
-    if (tid == 0) {
-      for (int c = 0; c < NST && c < n_chunks; ++c) issue_stage(c, item_ptr(c), vt_u);
-      for (int c = NST; c < NST + kRecPrefetch && c < n_chunks; ++c) prefetch_l2(item_ptr(c), ITEM_BYTES);
-    }
     st_issued = (1u << (NST < n_chunks ? NST : n_chunks)) - 1u;
     fence_proxy_async();
     wait_stage(0);
