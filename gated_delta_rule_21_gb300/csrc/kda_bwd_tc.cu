@@ -296,6 +296,9 @@ __global__ void __launch_bounds__(ChainLayout<VTR>::THREADS, 1)
   }
 
 done:
+  // one more commit covers every MMA thread 0 issued (after an abort the
+  // (s Q~)^T dO product can follow the last commit)
+  if (tid == 0 && committed) commit(u_bar, c_u);
   for (int s = 0; s < 2; ++s)
     if (tid == 0 && (st_issued & (1u << s))) mbar_wait(bar0 + 8u * s, st_phase[s]);
   if (tid == 0 && committed) mbar_wait(last_bar, last_k & 1u);
