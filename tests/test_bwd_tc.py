@@ -90,6 +90,10 @@ CASES = {
     "gate_lower_bound": (dict(B=1, T=256, H=2, K=128, V=128, init_state_std=0.1),
                          dict(g_fill=-5.0)),
     "gate_zero": (dict(B=1, T=256, H=2, K=128, V=128, init_state_std=0.1), dict(g_fill=0.0)),
+    # B*H picks the chain's and the saving recurrence's value tile (152 SMs):
+    # up to 38 units 32 columns, up to 76 64 columns, above that 128
+    "bh40_tile64": (dict(B=2, T=130, H=20, K=128, V=128, init_state_std=0.1), {}),
+    "bh80_tile128": (dict(B=2, T=70, H=40, K=128, V=128, init_state_std=0.1), {}),
 }
 
 
@@ -230,6 +234,7 @@ def test_tc_backward_packed_overflow_is_reported():
 
 TRAIN = {
     "fixed_t300": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1),
+    "fixed_bh40_tile64": dict(B=2, T=130, H=20, K=128, V=128, init_state_std=0.1),
     "packed": dict(B=2, T=300, H=2, K=128, V=128, init_state_std=0.1,
                    segments=[[("pad", 3), 100, 1, 1, ("pad", 5), 120, 70],
                              [64, 64, ("pad", 2), 170]]),
