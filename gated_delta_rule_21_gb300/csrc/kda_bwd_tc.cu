@@ -38,6 +38,7 @@
 //     exponentials and the reverse cumsum on the CUDA cores.
 #include <cuda.h>
 
+#include "kda_f32x2.cuh"
 #include "kda_split.cuh"
 
 namespace kda {
@@ -827,7 +828,13 @@ __global__ void __launch_bounds__(256, 1)
       float gsum = 0.f, gcp = 0.f;
       // the bf16 values the MMAs read, recomputed bit for bit as the operand
       // build formed them (same expressions, round to nearest even)
-      auto bfr = [](float x) { return __bfloat162float(__float2bfloat16_rn(x)); };
+      auto bfr2 = [](u64 x) {  // both lanes rounded to bf16 (nearest even) and back
+        float a, b;
+        upk2(x, a, b);
+        const uint32_t hw = pack_bf16(a, b);
+        return pk2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xffff0000u));
+      };
+      auto neg2 = [](u64 x) { return x ^ 0x8000000080000000ull; };
 #pragma unroll 1
       for (int e = 0; e < 4; ++e) {
         const int r8 = 32 * hh + 8 * e;
@@ -866,34 +873,55 @@ __global__ void __launch_bounds__(256, 1)
         // with every partial product <= 1 (no overflow; underflow only where
         // the value itself is below the fp32 range)
         const float ePr = ex2(Pr), fE = ex2(E[br] - Pr), fC = ex2(GC - E[br]);
+        // rows in pairs (k, k + 1): packed f32x2 arithmetic, each lane the
+        // fp32 operation of its row
+        const u64 ePr2 = pk2(ePr, ePr), fE2 = pk2(fE, fE), fC2 = pk2(fC, fC);
+        const u64 sc2 = pk2(scale, scale);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 8; k += 2) {
           const int r = r8 + k;
-          const float Gr = Gat(r, ch);
-          const float e1 = ex2(Gr - Pr), ie1 = ex2(Pr - Gr);
-          const float eG = e1 * ePr, eH = (ie1 * fE) * fC;
-          const float kr = raw_at(KK, r, ch), qr = raw_at(QQ, r, ch);
-          const float yq = bfr(qr * e1), yk = bfr(kr * e1);
-          const float ik = kr * ie1;
-          float ccol = 0.f, gcol = 0.f;  // column sums: dk (fp32 factors), dG (the KK values)
+          const float Ga = Gat(r, ch), Gb = Gat(r + 1, ch);
+          const u64 e1 = pk2(ex2(Ga - Pr), ex2(Gb - Pr));
+          const u64 ie1 = pk2(ex2(Pr - Ga), ex2(Pr - Gb));
+          const u64 eG = mul2(e1, ePr2), eH = mul2(mul2(ie1, fE2), fC2);
+          const float kra = raw_at(KK, r, ch), krb = raw_at(KK, r + 1, ch);
+          const u64 kr = pk2(kra, krb), qr = pk2(raw_at(QQ, r, ch), raw_at(QQ, r + 1, ch));
+          const u64 yq = bfr2(mul2(qr, e1)), yk = bfr2(mul2(kr, e1));
+          const u64 ik = mul2(kr, ie1);
+          u64 ccol = 0ull, gcol = 0ull;  // column sums: dk (fp32 factors), dG (the KK values)
 #pragma unroll
           for (int bb = 0; bb < kNumSub; ++bb) {
             if (bb < br) continue;
-            ccol = fmaf(w[bb][k], fac[bb], ccol);
-            gcol = fmaf(w[bb][k], bfr(ik * fac[bb]), gcol);
+            const u64 w2 = pk2(w[bb][k], w[bb][k + 1]), f2 = pk2(fac[bb], fac[bb]);
+            ccol = fma2(w2, f2, ccol);
+            gcol = fma2(w2, bfr2(mul2(ik, f2)), gcol);
           }
-          const float dQt = scale * dqt[k] * eG;        // dQ~ e^G
-          const float dKt = sBeta[r] * dyk[k] * eG;     // dK~ e^G
-          const float dKh = dkh[k] * eH;                // dK^ e^{G_C - G}
-          const float dq = e1 * rq[k] + dQt;
-          const float dk = e1 * rk[k] + ie1 * ccol + dKt + dKh;
-          const float dGr = (yq * rq[k] + yk * rk[k] - gcol) + qr * dQt + kr * (dKt - dKh);
-          sDG[r * KD + ch] = dGr;
-          gsum += dGr;
-          gcp = fmaf(kr, dKh, gcp);
+          const u64 rq2 = pk2(rq[k], rq[k + 1]), rk2 = pk2(rk[k], rk[k + 1]);
+          const u64 dQt = mul2(mul2(sc2, pk2(dqt[k], dqt[k + 1])), eG);              // dQ~ e^G
+          const u64 dKt = mul2(mul2(pk2(sBeta[r], sBeta[r + 1]), pk2(dyk[k], dyk[k + 1])), eG);  // dK~ e^G
+          const u64 dKh = mul2(pk2(dkh[k], dkh[k + 1]), eH);                         // dK^ e^{G_C - G}
+          const u64 dq = fma2(e1, rq2, dQt);
+          const u64 dk = add2(add2(fma2(e1, rk2, mul2(ie1, ccol)), dKt), dKh);
+          const u64 dG = fma2(kr, add2(dKt, neg2(dKh)),
+                              fma2(qr, dQt, add2(fma2(yq, rq2, mul2(yk, rk2)), neg2(gcol))));
+          float dga, dgb, dqa, dqb, dka, dkb, dha, dhb;
+          upk2(dG, dga, dgb);
+          upk2(dq, dqa, dqb);
+          upk2(dk, dka, dkb);
+          upk2(dKh, dha, dhb);
+          sDG[r * KD + ch] = dga;
+          sDG[(r + 1) * KD + ch] = dgb;
+          gsum += dga;
+          gsum += dgb;
+          gcp = fmaf(kra, dha, gcp);
+          gcp = fmaf(krb, dhb, gcp);
           if (r < n) {
-            p.dq[((tok0 + r) * H + h) * KD + ch] = dq;
-            p.dk[((tok0 + r) * H + h) * KD + ch] = dk;
+            p.dq[((tok0 + r) * H + h) * KD + ch] = dqa;
+            p.dk[((tok0 + r) * H + h) * KD + ch] = dka;
+          }
+          if (r + 1 < n) {
+            p.dq[((tok0 + r + 1) * H + h) * KD + ch] = dqb;
+            p.dk[((tok0 + r + 1) * H + h) * KD + ch] = dkb;
           }
         }
       }
