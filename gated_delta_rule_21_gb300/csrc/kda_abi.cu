@@ -51,8 +51,9 @@ int default_runs_bound(int T) { return (T + kChunk - 1) / kChunk; }
 // AUTO takes the chunk-parallel scan (rows without segment ids) when the
 // single chains would leave most SMs idle and stay long: at least 3
 // segments fill the SMs and every segment keeps 16 or more chunks.  (Measured
-// on B1 H8 T32768: 0.53 ms with 4 segments against 0.75 ms; on B1 H32 T8192,
-// 2 segments: 0.38 ms against 0.32 ms.)
+// with the default segment count: B1 H8 T32768, 9 segments, 0.43 ms against
+// 0.76 ms for the chain; B1 H16 T16384, 4: 0.42 against 0.46; B1 H4 T65536,
+// 19: 0.50 against 1.35; B1 H32 T8192, 2: 0.37 against 0.31, so the chain.)
 bool scan_preferred(const kda_shape *s) {
   const int P = scan_segments(s->B, s->T, s->H, 0);
   const int nc = (s->T + kChunk - 1) / kChunk;

@@ -1185,8 +1185,8 @@ size_t split_workspace_bytes(int B, int T, int H, bool has_seg, int max_runs_per
 
 int scan_segments(int B, int T, int H, int n_segs) {
   const int nc = (T + C - 1) / C;
-  if (n_segs == 0) {  // fill the GPU with the finish pass's 32-column units
-    const long units = (long)B * H * (VD / 32);
+  if (n_segs == 0) {  // as many as the finish pass's 64-column units fit the SMs
+    const long units = (long)B * H * (VD / 64);
     n_segs = (int)(num_sms() / (units > 0 ? units : 1));
   }
   if (n_segs < 2) n_segs = 2;

@@ -214,8 +214,9 @@ KDA_API kda_status kda_chunk_fwd_ex(const kda_shape *s, const void *q, const voi
  * shorter, which pays when few (row, head) pairs leave SMs idle and T is
  * long.  Arguments, layouts and results are those of kda_chunk_fwd with
  * segment_ids = NULL (up to rounding: the maps are rounded like the state).
- *   n_segments  0 (choose: enough segments to fill the GPU's SMs with the
- *               final pass, at least 2) or >= 2; capped at ceil(T/64) and
+ *   n_segments  0 (choose: as many segments as the final pass's units of
+ *               64 state columns fit the GPU's SMs, i.e. SMs / (2 B H), at
+ *               least 2) or >= 2; capped at ceil(T/64) and
  *               rounded so every segment holds at least one chunk.
  *   workspace   device, kda_chunk_fwd_scan_workspace_size(s, n_segments)
  *               bytes, 256-byte aligned, zero-filled before first use.
