@@ -1077,63 +1077,88 @@ done:
 }
 
 // S_start(s + 1) = M_s S_start(s) + B_s for s = 0 .. n_segs - 2, in fp32:
-// one CTA per (row, head, 32 columns of S), each thread a 4 x 4 register
-// tile (rows 4 kq .., columns 4 cq ..); S_start(0) is the initial state (or
-// zero).  M_s is staged in shared memory with a padded row (129 floats), so
-// the 4 rows a thread reads per step are in distinct banks.
-constexpr int kCombLd = KD + 1;
-constexpr uint32_t kCombSmem = (uint32_t)(KD * kCombLd + KD * 32) * 4;
+// one CTA per (row, head, 8 columns of S), each thread rows r, r + 64 by two
+// columns (r = tid / 4); S_start(0) is the initial state (or zero).  M_s is
+// staged in shared memory by 16-byte cp.async copies, the next step's while
+// this one computes (two buffers); its rows are padded to 132 floats (16-byte
+// rows for the copies; the 8 rows a warp reads per step fall in distinct
+// banks).  Each output accumulates B_s, then m = 0 .. K-1 in order.
+constexpr int kCombCols = 8;
+constexpr int kCombLd = KD + 4;
+constexpr uint32_t kCombSmem = (uint32_t)(2 * KD * kCombLd + KD * kCombCols) * 4;
+static_assert((kCombLd * 4) % 16 == 0, "16-byte rows for cp.async");
+
+__device__ __forceinline__ void comb_cp16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void comb_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
 __global__ void __launch_bounds__(256)
     scan_combine_kernel(const FwdParams p, const ScanParams sc) {
-  extern __shared__ float csm[];
-  float *sM = csm;                  // M_s [KD][kCombLd]
-  float *sS = csm + KD * kCombLd;   // S_start(s)[:, tile] [KD][32]
-  const int tile = blockIdx.x % (VD / 32), bh = blockIdx.x / (VD / 32);
+  extern __shared__ __align__(16) float csm[];
+  float *sM = csm;                          // M_s, two buffers [2][KD][kCombLd]
+  float *sS = csm + 2 * KD * kCombLd;       // S_start(s)[:, tile] [KD][kCombCols]
+  const int tile = blockIdx.x % (VD / kCombCols), bh = blockIdx.x / (VD / kCombCols);
   const int h = bh % p.H, b = bh / p.H;
-  const int tid = threadIdx.x, kq = tid >> 3, cq = tid & 7;
-  for (int i = tid; i < KD * 32; i += 256) {
-    const int kk = i >> 5, cc = i & 31;
+  const int tid = threadIdx.x, r0 = tid >> 2, c0 = 2 * (tid & 3);
+  const int col = kCombCols * tile;
+  auto map_of = [&](int s) {
+    return sc.maps + (((size_t)b * (sc.n_segs - 1) + s) * p.H + h) * KD * (VD + KD);
+  };
+  auto prefetch = [&](int s, int buf) {  // M_s = map[:, VD:] into buffer buf
+    const float *map = map_of(s);
+    float *dst = sM + buf * KD * kCombLd;
+    for (int i = tid; i < KD * KD / 4; i += 256) {
+      const int kk = i / (KD / 4), m4 = i % (KD / 4);
+      comb_cp16(smem_u32(dst + kk * kCombLd + 4 * m4), map + (size_t)kk * (VD + KD) + VD + 4 * m4);
+    }
+    comb_commit();
+  };
+  for (int i = tid; i < KD * kCombCols; i += 256) {
+    const int kk = i / kCombCols, cc = i % kCombCols;
     sS[i] = p.initial_state
-                ? p.initial_state[(((size_t)b * p.H + h) * KD + kk) * VD + 32 * tile + cc]
+                ? p.initial_state[(((size_t)b * p.H + h) * KD + kk) * VD + col + cc]
                 : 0.f;
   }
+  if (sc.n_segs > 1) prefetch(0, 0);
   for (int s = 0; s + 1 < sc.n_segs; ++s) {
-    const float *map = sc.maps + (((size_t)b * (sc.n_segs - 1) + s) * p.H + h) * KD * (VD + KD);
-    __syncthreads();  // sS of this step written, sM of the last step read
-    for (int i = tid; i < KD * KD / 4; i += 256) {  // M_s = map[:, VD:]
-      const int kk = i / (KD / 4), m4 = i % (KD / 4);
-      const float4 x = *reinterpret_cast<const float4 *>(map + (size_t)kk * (VD + KD) + VD + 4 * m4);
-      float *d = sM + kk * kCombLd + 4 * m4;
-      d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+    const int buf = s & 1;
+    // the next step's M (its buffer was last read before the previous
+    // step's closing barrier); then wait for this step's copies
+    if (s + 2 < sc.n_segs) {
+      prefetch(s + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    float acc[4][4];
+    const float *map = map_of(s);
+    float acc[2][2];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {  // B_s
-      const float4 x = *reinterpret_cast<const float4 *>(
-          map + (size_t)(4 * kq + r) * (VD + KD) + 32 * tile + 4 * cq);
-      acc[r][0] = x.x; acc[r][1] = x.y; acc[r][2] = x.z; acc[r][3] = x.w;
+    for (int rr = 0; rr < 2; ++rr) {  // B_s
+      const float2 x = *reinterpret_cast<const float2 *>(
+          map + (size_t)(r0 + 64 * rr) * (VD + KD) + col + c0);
+      acc[rr][0] = x.x; acc[rr][1] = x.y;
     }
-    __syncthreads();
-#pragma unroll 4
+    __syncthreads();  // every thread's copies of M_s landed; sS of this step written
+    const float *M = sM + buf * KD * kCombLd;
+#pragma unroll 8
     for (int m = 0; m < KD; ++m) {
-      const float4 sv = *reinterpret_cast<const float4 *>(sS + m * 32 + 4 * cq);
+      const float2 sv = *reinterpret_cast<const float2 *>(sS + m * kCombCols + c0);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float mv = sM[(4 * kq + r) * kCombLd + m];
-        acc[r][0] = fmaf(mv, sv.x, acc[r][0]);
-        acc[r][1] = fmaf(mv, sv.y, acc[r][1]);
-        acc[r][2] = fmaf(mv, sv.z, acc[r][2]);
-        acc[r][3] = fmaf(mv, sv.w, acc[r][3]);
+      for (int rr = 0; rr < 2; ++rr) {
+        const float mv = M[(r0 + 64 * rr) * kCombLd + m];
+        acc[rr][0] = fmaf(mv, sv.x, acc[rr][0]);
+        acc[rr][1] = fmaf(mv, sv.y, acc[rr][1]);
       }
     }
-    __syncthreads();  // every thread has read sS
+    __syncthreads();  // every thread has read sS and this buffer of M
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float4 x = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      *reinterpret_cast<float4 *>(sS + (4 * kq + r) * 32 + 4 * cq) = x;
-      *reinterpret_cast<float4 *>(
-          sc.starts + ((((size_t)b * sc.n_segs + s + 1) * p.H + h) * KD + 4 * kq + r) * VD +
-          32 * tile + 4 * cq) = x;
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = r0 + 64 * rr;
+      const float2 x = make_float2(acc[rr][0], acc[rr][1]);
+      *reinterpret_cast<float2 *>(sS + r * kCombCols + c0) = x;
+      *reinterpret_cast<float2 *>(
+          sc.starts + ((((size_t)b * sc.n_segs + s + 1) * p.H + h) * KD + r) * VD + col + c0) = x;
     }
   }
 }
@@ -1343,7 +1368,7 @@ cudaError_t launch_fwd_split(const FwdParams &p_in, void *workspace, size_t work
     e = cudaFuncSetAttribute(scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kCombSmem);
     if (e != cudaSuccess) return e;
-    scan_combine_kernel<<<p.B * p.H * (VD / 32), 256, kCombSmem, stream>>>(p, sc);
+    scan_combine_kernel<<<p.B * p.H * (VD / kCombCols), 256, kCombSmem, stream>>>(p, sc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p_in.v_tile == 0) p.v_tile = fit_tile((long)p.B * p.H * sc.n_segs, VD);
