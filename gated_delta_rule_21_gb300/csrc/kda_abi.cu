@@ -49,15 +49,20 @@ namespace {
 int default_runs_bound(int T) { return (T + kChunk - 1) / kChunk; }
 
 // AUTO takes the chunk-parallel scan (rows without segment ids) when the
-// single chains would leave most SMs idle and stay long: at least 3
-// segments fill the SMs and every segment keeps 16 or more chunks.  (Measured
-// with the default segment count: B1 H8 T32768, 9 segments, 0.43 ms against
-// 0.76 ms for the chain; B1 H16 T16384, 4: 0.42 against 0.46; B1 H4 T65536,
-// 19: 0.50 against 1.35; B1 H32 T8192, 2: 0.37 against 0.31, so the chain.)
+// single chains would leave SMs idle and the segments stay long enough to
+// pay for the map pass (about twice the per-chunk work): at least 3
+// segments, and 8 or more chunks per segment when there are 8 or more
+// segments (the chains would then fill at most a quarter of the SMs), else
+// 32 or more.  Measured (default segment count; scan against chain, ms):
+// B1 H8 T4096 0.099 / 0.113, B1 H8 T8192 0.146 / 0.208, B1 H8 T32768 0.388 /
+// 0.758, B1 H4 T65536 0.406 / 1.348, B1 H16 T8192 0.234 / 0.244, B1 H16
+// T16384 0.407 / 0.460, but B1 H16 T4096 (16 chunks per segment) 0.146 /
+// 0.134 and B1 H32 T8192 (2 segments) 0.377 / 0.315.
 bool scan_preferred(const kda_shape *s) {
   const int P = scan_segments(s->B, s->T, s->H, 0);
   const int nc = (s->T + kChunk - 1) / kChunk;
-  return P >= 3 && nc >= 16 * P;
+  const int per_segment = P > 0 ? (nc + P - 1) / P : 0;
+  return P >= 3 && per_segment >= (P >= 8 ? 8 : 32);
 }
 
 kda_status from_cuda(cudaError_t e) {

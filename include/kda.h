@@ -84,9 +84,10 @@ typedef enum kda_impl {
                          ids and the split path it always computes the
                          result: runs that overflow the split workspace are
                          served by the fused TC kernel on the device.
-                         Without segment ids, when at least 3 segments of
-                         16 or more chunks fill the SMs (few rows x heads,
-                         long T) and the workspace holds the scan's
+                         Without segment ids, when at least 3 segments fill
+                         the SMs (few rows x heads) and each holds 8 or
+                         more chunks (32 or more when there are fewer than
+                         8 segments), and the workspace holds the scan's
                          buffers, SPLIT runs as the chunk-parallel scan of
                          kda_chunk_fwd_scan.                                */
   KDA_IMPL_SIMT = 1,  /* fp32 CUDA-core kernel (every supported shape)      */
