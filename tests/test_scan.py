@@ -144,6 +144,12 @@ def test_auto_workspace_covers_the_scan_on_long_few_head_rows(kda):
         kda.workspace_size(1, 8192, 32, 128, 128, impl="split")
     assert kda.workspace_size(1, 1024, 8, 128, 128) == \
         kda.workspace_size(1, 1024, 8, 128, 128, impl="split")       # short rows
+    # 152 SMs: 9 segments of 15 chunks (8 or more per segment suffice with 8
+    # or more segments) against 4 segments of 16 (32 needed with fewer)
+    assert kda.workspace_size(1, 8192, 8, 128, 128) == \
+        kda.scan_workspace_size(1, 8192, 8, 128, 128)
+    assert kda.workspace_size(1, 4096, 16, 128, 128) == \
+        kda.workspace_size(1, 4096, 16, 128, 128, impl="split")
 
 
 @pytest.mark.gpu
